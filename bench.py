@@ -1,0 +1,406 @@
+"""Benchmark: ZoomR decode steps/s on the 8B shape at 16K context, batch 8, 32 layers.
+
+One step = the whole hot path (summary score -> top-k -> paged gather ->
+attention -> merge) for all 32 layers of one decode step, each layer with its
+own K/V pool, summaries and queries (Llama-3.1-8B attention: 32 query / 8 KV
+heads, d = 128, bf16; 16-token blocks in a shuffled pool; segments U[64, 512];
+top-k 16; window 256). Inputs are seeded synthetic data resident in HBM; one
+step reads ~5.1 GB, far more than the 129 MB L2, so no flush is needed between
+steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl zoomr|reference]
+
+Prints one JSON line (rank 0). Under torchrun each rank runs its own replica of
+the workload on its own GPU (weak scaling) and the reported time is the max over
+ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from hierarchical_sparse_kv_gb300 import accounting as A  # noqa: E402
+from hierarchical_sparse_kv_gb300 import workloads as W  # noqa: E402
+
+METRIC = "decode attention steps/s at 8B shape, 16K ctx, batch 8; HBM GB/s vs peak"
+WORKLOAD_ID = 2
+PEAK_FALLBACK_GBS = 6800.0
+KERNEL_SOURCES = ["hierarchical_sparse_kv_gb300/csrc/zoomr_kernels.cu",
+                  "hierarchical_sparse_kv_gb300/csrc/zoomr_internal.h"]
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "attend_mma_llama8b_16k_b8.json")
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def read_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return PEAK_FALLBACK_GBS, "fallback"
+
+
+def read_traffic():
+    """DRAM bytes per attend launch from the committed ncu summary, if the kernel is unchanged since."""
+    try:
+        with open(PROFILE_SUMMARY) as f:
+            prof = json.load(f)
+        if prof.get("kernel_source_hash") == kernel_source_hash():
+            return float(prof["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+# ---------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.lines = []
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = [l.split(",") for l in out.strip().splitlines() if l.count(",") >= 8]
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if "Active" in r[5 + i] and "Not" not in r[5 + i]})
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------- inputs
+def make_inputs(device, layers=None):
+    spec = W.WORKLOADS[WORKLOAD_ID]
+    st = W.make_structure(spec)
+    nl = spec.layers if layers is None else layers
+    lts = [W.make_layer(st, l, device) for l in range(nl)]
+    return spec, st, lts
+
+
+def config_dict(spec, extra=None):
+    d = {"workload": spec.name, "batch": spec.batch, "seq_len": spec.seq_len, "layers": spec.layers,
+         "q_heads": spec.num_q_heads, "kv_heads": spec.num_kv_heads, "head_dim": spec.head_dim,
+         "top_k": spec.topk, "window": spec.window, "segment_len": list(spec.seg_len_range), "block_size": 16,
+         "l2": "inputs exceed L2 (each step reads ~5.1 GB of K/V; no flush)"}
+    if extra:
+        d.update(extra)
+    return d
+
+
+# ---------------------------------------------------------------------- oracle timing
+def time_oracle(st, lt, budget_s: float, max_units=None):
+    """Run the CPU oracle unit by unit on one layer until ``budget_s`` elapses.
+    Returns (units done, seconds)."""
+    from oracle import zoomr_oracle as O
+
+    q = W.to_numpy32(lt.q)
+    kp = W.to_numpy32(lt.k_pool)
+    vp = W.to_numpy32(lt.v_pool)
+    sk = W.to_numpy32(lt.sum_k)
+    sv = W.to_numpy32(lt.sum_v)
+    units = [(b, g) for b in range(st.batch) for g in range(st.spec.num_kv_heads)]
+    done = 0
+    t0 = time.perf_counter()
+    for (b, g) in units:
+        O.decode_step(q, kp, vp, st.block_tables, st.seg_ptr, st.seg_bounds, sk, sv, st.topk, st.window,
+                      units=[(b, g)])
+        done += 1
+        if (max_units and done >= max_units) or time.perf_counter() - t0 >= budget_s:
+            break
+    return done, time.perf_counter() - t0
+
+
+def oracle_threads_env():
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ.setdefault(k, "1")
+
+
+# ---------------------------------------------------------------------- distributed
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------- reference arm
+def run_reference(args):
+    world, rank, local = dist_setup(args.gpus)
+    if rank != 0:
+        return 0
+    oracle_threads_env()
+    spec = W.WORKLOADS[WORKLOAD_ID]
+    st = W.make_structure(spec)
+    device = "cuda" if torch.cuda.is_available() else "cpu"
+    lt = W.make_layer(st, 0, device)
+    units_per_step = spec.layers * st.batch * spec.num_kv_heads
+    sample_units = max(1, args.ref_units)
+    for _ in range(args.warmup):
+        time_oracle(st, lt, 1e9, max_units=1)
+    times, units = [], 0
+    for _ in range(args.steps):
+        n, t = time_oracle(st, lt, 1e9, max_units=sample_units)
+        times.append(t)
+        units += n
+    per_unit = sum(times) / units
+    value = 1.0 / (per_unit * units_per_step)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_unit * units_per_step * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded)", "config": config_dict(spec),
+            "cpu_baseline": {"value": value, "unit": "steps/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{sample_units} of the {units_per_step} (layer, sequence, KV head) units of "
+                                       f"one step per timed step, scaled to a full step"},
+            "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------- our arm
+def run_zoomr(args):
+    world, rank, local = dist_setup(args.gpus)
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: the ZoomR path needs a CUDA GPU")
+    from hierarchical_sparse_kv_gb300 import build as B
+    from hierarchical_sparse_kv_gb300 import zoomr as Z
+
+    if rank == 0 or world == 1:
+        B.build()
+    barrier(world)
+    Z.load()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    spec, st, lts = make_inputs(dev)
+    L = len(lts)
+    plan = Z.DecodePlan.from_structure(st, device=dev)
+    bt = torch.from_numpy(st.block_tables.astype(np.int32)).to(dev)
+    outs = [torch.empty(lt.q.shape, dtype=torch.float32, device=dev) for lt in lts]
+    G = spec.num_q_heads // spec.num_kv_heads
+
+    # Algorithmic bytes of each layer's attend launch (from that layer's selection).
+    dbg = plan.new_debug_outputs()
+    attend_bytes, select_bytes, tok_total = [], 0, 0
+    for l, lt in enumerate(lts):
+        plan.run(lt.q, lt.k_pool, lt.v_pool, bt, lt.sum_k, lt.sum_v, outs[l], dbg)
+        _, rng, nr = (x.cpu().numpy() for x in dbg)
+        tot = 0
+        for b in range(st.batch):
+            n_b = st.num_segments(b)
+            k_b = min(int(st.topk[b]), n_b)
+            for g in range(spec.num_kv_heads):
+                r = rng[b, g, :nr[b, g]]
+                ntok = A.ranges_token_count(r)
+                tok_total += ntok
+                tot += A.attend_bytes_per_unit(ntok, n_b - k_b, A.ranges_block_count(r), G, spec.head_dim, 2)
+                select_bytes += A.select_bytes_per_unit(n_b, G, spec.head_dim, 2)
+        attend_bytes.append(tot)
+    torch.cuda.synchronize()
+    assert plan.device_error() == 0
+    out_bytes = L * st.batch * spec.num_q_heads * spec.head_dim * 4
+    step_bytes = sum(attend_bytes) + select_bytes + out_bytes
+
+    stream = torch.cuda.Stream(device=dev)
+    n_graphs = max(1, min(args.steps, args.max_graphs))
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(L)]
+           for _ in range(n_graphs)]
+
+    def step(ev_set, s):
+        for l, lt in enumerate(lts):
+            if ev_set is None:
+                plan.run(lt.q, lt.k_pool, lt.v_pool, bt, lt.sum_k, lt.sum_v, outs[l], stream=s)
+            else:
+                plan.run_timed(lt.q, lt.k_pool, lt.v_pool, bt, lt.sum_k, lt.sum_v, outs[l], ev_set[l][0],
+                               ev_set[l][1], stream=s)
+
+    stream.wait_stream(torch.cuda.current_stream())
+    graphs = []
+    with torch.cuda.stream(stream):
+        step(evs[0], stream)  # eager warm-up on the capture stream
+        if not args.no_graph:
+            for i in range(n_graphs):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    step(evs[i], stream)
+                graphs.append(g)
+    torch.cuda.current_stream().wait_stream(stream)
+    torch.cuda.synchronize()
+
+    def replay(i):
+        with torch.cuda.stream(stream):
+            if graphs:
+                graphs[i % n_graphs].replay()
+            else:
+                step(evs[i % n_graphs], stream)
+
+    for i in range(args.warmup):
+        replay(i)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = ClockSampler(dev.index) if rank == 0 else None
+    time.sleep(0.25 if clocks and clocks.proc else 0)
+    t_start, t_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    barrier(world)
+    t_start.record(stream)
+    for i in range(args.steps):
+        replay(i)
+    t_stop.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop() if clocks else None
+    ms = t_start.elapsed_time(t_stop) / args.steps
+    ms = max_over_ranks(ms, world)
+    # attend kernel: average launch duration over the events of the last replay of each graph
+    durs = []
+    for i in range(min(n_graphs, args.steps)):
+        for l in range(L):
+            durs.append(evs[i][l][0].elapsed_time(evs[i][l][1]))
+    attend_ms = float(np.mean(durs))
+    attend_bytes_avg = float(np.mean(attend_bytes))
+
+    # e2e through the public API with host buffers: H2D of every layer's queries from pinned
+    # memory, the step, D2H of every layer's output into pinned memory.
+    host_q = [lt.q.cpu().pin_memory() for lt in lts]
+    host_out = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
+    h2d = sum(x.numel() * x.element_size() for x in host_q)
+    d2h = sum(x.numel() * x.element_size() for x in host_out)
+    e2e_steps = max(3, min(args.steps, 50))
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            for l, lt in enumerate(lts):
+                lt.q.copy_(host_q[l], non_blocking=True)
+            step(None, stream)
+            for l in range(L):
+                host_out[l].copy_(outs[l], non_blocking=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            for l, lt in enumerate(lts):
+                lt.q.copy_(host_q[l], non_blocking=True)
+            step(None, stream)
+            for l in range(L):
+                host_out[l].copy_(outs[l], non_blocking=True)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
+
+    peak, peak_kind = read_peak()
+    achieved = attend_bytes_avg / (attend_ms * 1e-3) / 1e9
+    traffic = read_traffic()
+    line = {
+        "impl": "zoomr", "metric": METRIC, "value": world * 1e3 / ms, "unit": "steps/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) K/V, segment-mean summaries + N(0,0.1), queries near segment means)",
+        "config": config_dict(spec, {"graph": not args.no_graph, "replicas_per_gpu": 1}),
+        "hbm_gbs": step_bytes / (ms * 1e-3) / 1e9,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_kind": f"{peak_kind} copy bandwidth", "traffic": traffic,
+                     "kernel": "zr_attend_mma_kernel<128>", "attend_us": attend_ms * 1e3,
+                     "alg_bytes_per_launch": attend_bytes_avg},
+        "e2e": {"value": world * 1e3 / e2e_ms, "unit": "steps/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": 3 * L * args.steps,
+        "clocks": clk,
+        "tokens_gathered_per_step": tok_total,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        oracle_threads_env()
+        n, t = time_oracle(st, lts[0], args.cpu_budget)
+        units_per_step = L * st.batch * spec.num_kv_heads
+        v = n / t / units_per_step
+        line["cpu_baseline"] = {"value": v, "unit": "steps/s", "cores": 1, "kind": "oracle",
+                                "sample": f"{n} of the {units_per_step} (layer, sequence, KV head) units of one step "
+                                          f"({t:.1f} s), scaled to a full step"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    plan.close()
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["zoomr", "reference"], default="zoomr")
+    ap.add_argument("--no-graph", action="store_true", help="launch eagerly instead of replaying CUDA graphs")
+    ap.add_argument("--max-graphs", type=int, default=64, help="distinct captured steps (each with its own events)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--ref-units", type=int, default=16, help="oracle units per reference-arm step")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    return run_reference(args) if args.impl == "reference" else run_zoomr(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,750 @@
+// sm_103a kernels of the ZoomR decode step and their launch sequence.
+//
+//   select  one CTA per (sequence b, KV head g) unit: scores every segment's
+//           summary key (ZoomR page, 3.3 "Per-Head Importance Scoring and
+//           Voting"), picks the top-k by rank counting (ties to the lower
+//           index), and writes the unit's gathered token ranges (the window
+//           merged with the selected segments, 3.3 "Constructing the Final
+//           Multi-Granularity Context") and its summary list.
+//   attend  one warp per split slot: walks up to kChunkRows gathered rows
+//           (tokens through the block table, then summary rows), computes the
+//           group's logits and an online softmax, and writes one unnormalised
+//           partial (m, l, o) per query head (ZoomR 2 "Background", the
+//           softmax(q K^T / sqrt d) V equation; rows fetched as on the
+//           "KV-cache management" page, "Paged KV cache (PagedAttention)").
+//           bf16: tensor cores (mma.sync m16n8k16) with K/V rows loaded straight
+//           from HBM into fragment registers; f32: CUDA-core FMA.
+//   merge   one warp per (sequence, query head): log-sum-exp combination of the
+//           unit's partials into the fp32 output.
+//
+// Launches are chained with programmatic dependent launch: every kernel waits
+// (griddepcontrol.wait) for its predecessor before touching the workspace.
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "zoomr_internal.h"
+
+namespace zr {
+namespace {
+
+constexpr unsigned kFull = 0xFFFFFFFFu;
+
+// ------------------------------------------------------------------ helpers
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// 16-byte streaming load that bypasses L1 (each byte is used once).
+__device__ __forceinline__ uint4 ld_stream16(const void* p) {
+  uint4 v;
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t x) { return __uint_as_float(x << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t x) { return __uint_as_float(x & 0xFFFF0000u); }
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+template <typename T>
+__device__ __forceinline__ float to_float(T x);
+template <>
+__device__ __forceinline__ float to_float<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ float to_float<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+// Load 8 consecutive elements (16 B for bf16, 32 B for f32) as floats.
+template <typename T>
+__device__ __forceinline__ void load8(const T* p, float (&v)[8]);
+template <>
+__device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16* p, float (&v)[8]) {
+  const uint4 w = *reinterpret_cast<const uint4*>(p);
+  v[0] = bf16_lo(w.x); v[1] = bf16_hi(w.x); v[2] = bf16_lo(w.y); v[3] = bf16_hi(w.y);
+  v[4] = bf16_lo(w.z); v[5] = bf16_hi(w.z); v[6] = bf16_lo(w.w); v[7] = bf16_hi(w.w);
+}
+template <>
+__device__ __forceinline__ void load8<float>(const float* p, float (&v)[8]) {
+  const float4 a = *reinterpret_cast<const float4*>(p);
+  const float4 b = *reinterpret_cast<const float4*>(p + 4);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
+// Load E (= 2 or 4) consecutive elements as floats.
+template <typename T, int E>
+__device__ __forceinline__ void load_e(const T* p, float (&v)[E]) {
+  if constexpr (sizeof(T) == 4) {
+    if constexpr (E == 4) {
+      const float4 a = *reinterpret_cast<const float4*>(p);
+      v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    } else {
+      const float2 a = *reinterpret_cast<const float2*>(p);
+      v[0] = a.x; v[1] = a.y;
+    }
+  } else {
+    if constexpr (E == 4) {
+      const uint2 a = *reinterpret_cast<const uint2*>(p);
+      v[0] = bf16_lo(a.x); v[1] = bf16_hi(a.x); v[2] = bf16_lo(a.y); v[3] = bf16_hi(a.y);
+    } else {
+      const uint32_t a = *reinterpret_cast<const uint32_t*>(p);
+      v[0] = bf16_lo(a); v[1] = bf16_hi(a);
+    }
+  }
+}
+
+// D = A * B + D, m16n8k16, bf16 inputs, fp32 accumulators.
+__device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Exclusive prefix sum of one int per thread over the CTA; *total receives the sum.
+__device__ int block_exclusive_scan(int v, int* total) {
+  __shared__ int wsum[32];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(kFull, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) wsum[w] = x;
+  __syncthreads();
+  if (w == 0) {
+    int t = lane < nw ? wsum[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(kFull, t, o);
+      if (lane >= o) t += y;
+    }
+    wsum[lane] = t;
+  }
+  __syncthreads();
+  const int base = w > 0 ? wsum[w - 1] : 0;
+  *total = wsum[nw - 1];
+  __syncthreads();
+  return base + x - v;
+}
+
+// ------------------------------------------------------------------ select
+// Shared memory: q [kMaxGroup][D] f32 | keys [n_max] | flag [n_max+2] | bounds [n_max+1]
+//                | list [n_max] | runs_s [n_max] | runs_e [n_max]
+template <typename T, int D>
+__global__ void __launch_bounds__(kSelectThreads) zr_select_kernel(StepArgs a) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  const int g = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+  const int u = b * a.Hkv + g;
+  const int G = a.G, nmax = a.n_max;
+  float* qs = reinterpret_cast<float*>(smem_raw);
+  float* keys = qs + kMaxGroup * D;
+  int* flag = reinterpret_cast<int*>(keys + nmax);
+  int* bnd = flag + nmax + 2;
+  int* list = bnd + nmax + 1;
+  int* runs_s = list + nmax;
+  int* runs_e = runs_s + nmax;
+  __shared__ int s_rstar;
+
+  pdl_trigger();
+  pdl_wait();
+
+  const int s0 = a.meta.seg_ptr[b];
+  const int n = a.meta.seg_ptr[b + 1] - s0;
+  const int L = a.meta.seq_lens[b];
+  const int k = a.meta.topk[b];
+  const T* qg = static_cast<const T*>(a.q) + (static_cast<size_t>(b) * a.Hq + static_cast<size_t>(g) * G) * D;
+  for (int i = tid; i < G * D; i += blockDim.x) qs[i] = to_float(qg[i]);
+  for (int i = tid; i <= n; i += blockDim.x) bnd[i] = a.meta.seg_bounds[s0 + b + i];
+  __syncthreads();
+
+  // 1. ranking key: max over the group of the fp32 dot, products and sums rounded, ascending order.
+  const T* sk = static_cast<const T*>(a.sum_k);
+  for (int i = tid; i < n; i += blockDim.x) {
+    const T* row = sk + (static_cast<size_t>(s0 + i) * a.Hkv + g) * D;
+    float acc[kMaxGroup];
+#pragma unroll
+    for (int h = 0; h < kMaxGroup; ++h) acc[h] = 0.f;
+    for (int t0 = 0; t0 < D; t0 += 8) {
+      float sv[8];
+      load8<T>(row + t0, sv);
+#pragma unroll
+      for (int h = 0; h < kMaxGroup; ++h) {
+        if (h < G) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) acc[h] = __fadd_rn(acc[h], __fmul_rn(qs[h * D + t0 + e], sv[e]));
+        }
+      }
+    }
+    float key = acc[0];
+#pragma unroll
+    for (int h = 1; h < kMaxGroup; ++h)
+      if (h < G) key = fmaxf(key, acc[h]);
+    keys[i] = key;
+  }
+  __syncthreads();
+
+  // 2. top-k: segment i is selected iff fewer than k segments beat it (greater key, or equal key and lower index).
+  for (int i = tid; i < n; i += blockDim.x) {
+    const float ki = keys[i];
+    int cnt = 0;
+    for (int j = 0; j < n && cnt < k; ++j) {
+      const float kj = keys[j];
+      cnt += (kj > ki) || (kj == ki && j < i);
+    }
+    flag[i] = cnt < k ? 1 : 0;
+  }
+  __syncthreads();
+
+  // Compact the selected segments (ascending) and the summary list (the rest, ascending).
+  int* sel_ws = a.sel + static_cast<size_t>(u) * a.k_max;
+  int* sum_ws = a.sumlist + static_cast<size_t>(u) * a.n_max;
+  {
+    const int per = (n + blockDim.x - 1) / blockDim.x;
+    const int i0 = min(n, tid * per), i1 = min(n, i0 + per);
+    int local = 0;
+    for (int i = i0; i < i1; ++i) local += flag[i];
+    int total;
+    int pos = block_exclusive_scan(local, &total);
+    for (int i = i0; i < i1; ++i) {
+      if (flag[i]) {
+        list[pos] = i;
+        sel_ws[pos] = i;
+        ++pos;
+      } else {
+        sum_ws[i - pos] = i;
+      }
+    }
+  }
+  __syncthreads();
+
+  // 3. maximal runs of selected segments (adjacent segments touch: bound[i+1] == bound[i+1]).
+  int m;
+  {
+    const int per = (k + blockDim.x - 1) / blockDim.x;
+    const int j0 = min(k, tid * per), j1 = min(k, j0 + per);
+    int starts = 0;
+    for (int j = j0; j < j1; ++j) starts += (j == 0) || (bnd[list[j - 1] + 1] != bnd[list[j]]);
+    int ridx = block_exclusive_scan(starts, &m) - 1;
+    for (int j = j0; j < j1; ++j) {
+      const int seg = list[j];
+      if ((j == 0) || (bnd[list[j - 1] + 1] != bnd[seg])) runs_s[++ridx] = bnd[seg];
+      if ((j == k - 1) || (bnd[list[j + 1]] != bnd[seg + 1])) runs_e[ridx] = bnd[seg + 1];
+    }
+  }
+  if (tid == 0) s_rstar = m;
+  __syncthreads();
+  // Merge with the window [W0, L): the first run reaching W0 absorbs it; later runs lie inside it.
+  const int W0 = max(0, L - a.window);
+  for (int r = tid; r < m; r += blockDim.x)
+    if (runs_e[r] >= W0 && (r == 0 || runs_e[r - 1] < W0)) s_rstar = r;
+  __syncthreads();
+  const int rstar = s_rstar;
+  const int nr = rstar < m ? rstar + 1 : m + (W0 < L ? 1 : 0);
+  int* rg = a.ranges + static_cast<size_t>(u) * (a.k_max + 1) * 2;
+  int* lens = flag;  // flags are no longer needed
+  for (int r = tid; r < nr; r += blockDim.x) {
+    int s, e;
+    if (r < rstar) {
+      s = runs_s[r];
+      e = runs_e[r];
+    } else if (rstar < m) {
+      s = min(W0, runs_s[rstar]);
+      e = L;
+    } else {
+      s = W0;
+      e = L;
+    }
+    rg[2 * r] = s;
+    rg[2 * r + 1] = e;
+    lens[r] = e - s;
+    if (a.ranges_out) {
+      int* ro = a.ranges_out + static_cast<size_t>(u) * (a.k_max + 1) * 2;
+      ro[2 * r] = s;
+      ro[2 * r + 1] = e;
+    }
+  }
+  __syncthreads();
+  int* cum = a.cum + static_cast<size_t>(u) * (a.k_max + 2);
+  int n_tok;
+  {
+    const int per = (nr + blockDim.x - 1) / blockDim.x;
+    const int r0 = min(nr, tid * per), r1 = min(nr, r0 + per);
+    int local = 0;
+    for (int r = r0; r < r1; ++r) local += lens[r];
+    int run = block_exclusive_scan(local, &n_tok);
+    for (int r = r0; r < r1; ++r) {
+      cum[r] = run;
+      run += lens[r];
+    }
+  }
+  if (tid == 0) {
+    cum[nr] = n_tok;
+    const int n_sum = n - k;
+    const int rows = n_tok + n_sum;
+    int n_chunks = (rows + a.chunk_rows - 1) / a.chunk_rows;
+    if (n_chunks > a.meta.slots[b]) {
+      atomicOr(a.err, kErrSlots);
+      n_chunks = a.meta.slots[b];
+    }
+    a.unit_info[u] = make_int4(nr, n_tok, n_sum, n_chunks);
+    if (a.nranges_out) a.nranges_out[u] = nr;
+  }
+  if (a.sel_out) {
+    int* so = a.sel_out + static_cast<size_t>(u) * a.k_max;
+    for (int j = tid; j < a.k_max; j += blockDim.x) so[j] = j < k ? list[j] : -1;
+  }
+}
+
+// ------------------------------------------------------------------ attend: shared pieces
+struct SlotInfo {
+  int b, g, c, u;
+};
+
+// Which (sequence, KV head, chunk) a split slot belongs to. slot_base is strictly increasing.
+__device__ __forceinline__ SlotInfo decode_slot(const StepArgs& a, int slot, int lane) {
+  int b = 0;
+  for (int base = 0; base < a.B; base += 32) {
+    const int cand = base + lane;
+    const bool le = cand < a.B && a.meta.slot_base[cand] <= slot;
+    const unsigned m = __ballot_sync(kFull, le);
+    if (m) b = base + 31 - __clz(m);
+    if (m != kFull) break;
+  }
+  const int rel = slot - a.meta.slot_base[b];
+  const int S = a.meta.slots[b];
+  SlotInfo s;
+  s.b = b;
+  s.g = rel / S;
+  s.c = rel - s.g * S;
+  s.u = b * a.Hkv + s.g;
+  return s;
+}
+
+// Fill one warp's row table for rows [row0, row0 + nrows) of unit u: pool row id
+// ((block * Hkv + g) * 16 + slot) for gathered tokens, summary row id | flag after
+// them, kInvalidRow past the end or for a block id outside the pool.
+__device__ __forceinline__ void build_row_table(const StepArgs& a, const SlotInfo& s, int4 info, int row0,
+                                                int nrows, uint32_t* tab, int lane) {
+  const int n_tok = info.y;
+  const int32_t* rg = a.ranges + static_cast<size_t>(s.u) * (a.k_max + 1) * 2;
+  const int32_t* cum = a.cum + static_cast<size_t>(s.u) * (a.k_max + 2);
+  const int32_t* sl = a.sumlist + static_cast<size_t>(s.u) * a.n_max;
+  const int32_t* bt = a.block_tables + static_cast<size_t>(s.b) * a.max_blocks;
+  const int seg0 = a.meta.seg_ptr[s.b];
+  int r = 0;
+  for (int e = lane; e < a.chunk_rows; e += 32) {
+    uint32_t id = kInvalidRow;
+    if (e < nrows) {
+      const int j = row0 + e;
+      if (j < n_tok) {
+        while (r + 1 < info.x && cum[r + 1] <= j) ++r;
+        const int t = rg[2 * r] + (j - cum[r]);
+        const int phys = bt[t >> 4];
+        if (static_cast<unsigned>(phys) < static_cast<unsigned>(a.num_blocks)) {
+          id = ((static_cast<uint32_t>(phys) * a.Hkv + s.g) << 4) | static_cast<uint32_t>(t & 15);
+        } else {
+          atomicOr(a.err, kErrBadBlock);
+        }
+      } else {
+        const int seg = sl[j - n_tok];
+        id = (static_cast<uint32_t>(seg0 + seg) * a.Hkv + s.g) | kSummaryFlag;
+      }
+    }
+    tab[e] = id;
+  }
+  __syncwarp();
+}
+
+template <typename T, int D>
+__device__ __forceinline__ const T* row_ptr(uint32_t id, const T* pool, const T* sum) {
+  return (id & kSummaryFlag) ? sum + static_cast<size_t>(id & ~kSummaryFlag) * D : pool + static_cast<size_t>(id) * D;
+}
+
+// ------------------------------------------------------------------ attend: tensor cores (bf16, G <= 8)
+//
+// Per 16-row tile, with r = lane / 4 and c = lane % 4:
+//   S = Q K^T  as m16n8k16 with M = query heads (G valid of 16), N = 8 tokens (two tiles),
+//              K = d. Thread (r, c) feeds K rows r and r+8 (B operand), reading the d
+//              components 32q + 8c .. +7 with one 16-byte load per q; Q's A fragments use
+//              the same d order (a permutation of the contraction index).
+//   P          thread (r, c) then holds S[head r][tokens 2c, 2c+1, 2c+8, 2c+9], which is
+//              exactly the B fragment of P^T for the next product: no data movement.
+//              P is split into bf16 hi + lo parts (two MMAs) so it keeps ~16 bits.
+//   O^T += V^T P^T  with M = d (D/16 tiles), N = heads, K = 16 tokens. Thread (r, c) loads
+//              V rows 2c, 2c+1, 2c+8, 2c+9 at d = r*D/8 .. +D/8-1 and pairs tokens with
+//              byte permutes; M row r of tile i is d = r*D/8 + 2i, row r+8 is d + 1.
+template <int D>
+struct MmaTile {
+  uint32_t k[2][D / 32][4];  // K rows r, r+8
+  uint32_t v[4][D / 16];     // V rows 2c, 2c+1, 2c+8, 2c+9
+  uint32_t vmask;            // bit j: V row j of this thread is a real row
+};
+
+template <int D>
+__device__ __forceinline__ void mma_load_tile(MmaTile<D>& t, const uint32_t* tab, int t0, int r, int c,
+                                              const __nv_bfloat16* kp, const __nv_bfloat16* vp,
+                                              const __nv_bfloat16* skp, const __nv_bfloat16* svp) {
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const uint32_t id = tab[t0 + r + 8 * h];
+    if (id != kInvalidRow) {
+      const __nv_bfloat16* p = row_ptr<__nv_bfloat16, D>(id, kp, skp) + 8 * c;
+#pragma unroll
+      for (int q = 0; q < D / 32; ++q) {
+        const uint4 w = ld_stream16(p + 32 * q);
+        t.k[h][q][0] = w.x; t.k[h][q][1] = w.y; t.k[h][q][2] = w.z; t.k[h][q][3] = w.w;
+      }
+    } else {
+#pragma unroll
+      for (int q = 0; q < D / 32; ++q) t.k[h][q][0] = t.k[h][q][1] = t.k[h][q][2] = t.k[h][q][3] = 0u;
+    }
+  }
+  t.vmask = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int row = 2 * c + (j & 1) + 8 * (j >> 1);
+    const uint32_t id = tab[t0 + row];
+    if (id != kInvalidRow) {
+      t.vmask |= 1u << j;
+      const __nv_bfloat16* p = row_ptr<__nv_bfloat16, D>(id, vp, svp) + (D / 8) * r;
+#pragma unroll
+      for (int q = 0; q < D / 64; ++q) {
+        const uint4 w = ld_stream16(p + 8 * q);
+        t.v[j][4 * q + 0] = w.x; t.v[j][4 * q + 1] = w.y; t.v[j][4 * q + 2] = w.z; t.v[j][4 * q + 3] = w.w;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < D / 16; ++i) t.v[j][i] = 0u;
+    }
+  }
+}
+
+template <int D>
+struct MmaState {
+  uint32_t qa0[D / 16], qa2[D / 16];  // Q A-fragments (rows r < G), rows r+8 are zero
+  float o[D / 16][4];                  // O^T accumulators
+  float m;                             // running max (log2 units) of head r
+  float l;                             // this thread's part of head r's running sum
+};
+
+template <int D>
+__device__ __forceinline__ void mma_compute_tile(MmaState<D>& st, const MmaTile<D>& t, float scale_log2, int c) {
+  float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int s = 0; s < D / 16; ++s) {
+    const int q = s >> 1, hh = (s & 1) * 2;
+    mma_bf16(s0, st.qa0[s], 0u, st.qa2[s], 0u, t.k[0][q][hh], t.k[0][q][hh + 1]);
+    mma_bf16(s1, st.qa0[s], 0u, st.qa2[s], 0u, t.k[1][q][hh], t.k[1][q][hh + 1]);
+  }
+  const float ninf = -INFINITY;
+  const float x0 = (t.vmask & 1u) ? s0[0] * scale_log2 : ninf;
+  const float x1 = (t.vmask & 2u) ? s0[1] * scale_log2 : ninf;
+  const float x2 = (t.vmask & 4u) ? s1[0] * scale_log2 : ninf;
+  const float x3 = (t.vmask & 8u) ? s1[1] * scale_log2 : ninf;
+  float mt = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
+  mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 1));
+  mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 2));
+  const float m_new = fmaxf(st.m, mt);
+  const float alpha = fast_exp2(st.m - m_new);
+  const float p0 = fast_exp2(x0 - m_new), p1 = fast_exp2(x1 - m_new);
+  const float p2 = fast_exp2(x2 - m_new), p3 = fast_exp2(x3 - m_new);
+  st.l = st.l * alpha + ((p0 + p1) + (p2 + p3));
+  st.m = m_new;
+  const uint32_t bh0 = pack_bf16(p0, p1), bh1 = pack_bf16(p2, p3);
+  const uint32_t bl0 = pack_bf16(p0 - bf16_lo(bh0), p1 - bf16_hi(bh0));
+  const uint32_t bl1 = pack_bf16(p2 - bf16_lo(bh1), p3 - bf16_hi(bh1));
+  // O^T columns of this thread are heads 2c and 2c+1, whose alphas live in lanes 8c and 8c+4.
+  const float a_e = __shfl_sync(kFull, alpha, 8 * c);
+  const float a_o = __shfl_sync(kFull, alpha, 8 * c + 4);
+#pragma unroll
+  for (int i = 0; i < D / 16; ++i) {
+    st.o[i][0] *= a_e;
+    st.o[i][1] *= a_o;
+    st.o[i][2] *= a_e;
+    st.o[i][3] *= a_o;
+    const uint32_t a0 = __byte_perm(t.v[0][i], t.v[1][i], 0x5410);
+    const uint32_t a1 = __byte_perm(t.v[0][i], t.v[1][i], 0x7632);
+    const uint32_t a2 = __byte_perm(t.v[2][i], t.v[3][i], 0x5410);
+    const uint32_t a3 = __byte_perm(t.v[2][i], t.v[3][i], 0x7632);
+    mma_bf16(st.o[i], a0, a1, a2, a3, bh0, bh1);
+    mma_bf16(st.o[i], a0, a1, a2, a3, bl0, bl1);
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kAttendWarps * 32) zr_attend_mma_kernel(StepArgs a) {
+  __shared__ uint32_t rowtab[kAttendWarps][kChunkRows];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int slot = blockIdx.x * kAttendWarps + warp;
+  pdl_trigger();
+  if (slot >= a.total_slots) return;
+  const SlotInfo s = decode_slot(a, slot, lane);
+  pdl_wait();
+  const int4 info = a.unit_info[s.u];
+  if (s.c >= info.w) return;
+  const int rows = info.y + info.z;
+  const int row0 = s.c * a.chunk_rows;
+  const int nrows = min(a.chunk_rows, rows - row0);
+  uint32_t* tab = rowtab[warp];
+  build_row_table(a, s, info, row0, nrows, tab, lane);
+
+  const int r = lane >> 2, c = lane & 3;
+  const int G = a.G;
+  MmaState<D> st;
+  const __nv_bfloat16* qg =
+      static_cast<const __nv_bfloat16*>(a.q) + (static_cast<size_t>(s.b) * a.Hq + static_cast<size_t>(s.g) * G) * D;
+#pragma unroll
+  for (int k = 0; k < D / 16; ++k) {
+    const int d0 = 32 * (k >> 1) + 8 * c + 4 * (k & 1);
+    if (r < G) {
+      st.qa0[k] = *reinterpret_cast<const uint32_t*>(qg + r * D + d0);
+      st.qa2[k] = *reinterpret_cast<const uint32_t*>(qg + r * D + d0 + 2);
+    } else {
+      st.qa0[k] = 0u;
+      st.qa2[k] = 0u;
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < D / 16; ++i) st.o[i][0] = st.o[i][1] = st.o[i][2] = st.o[i][3] = 0.f;
+  st.m = -1e30f;
+  st.l = 0.f;
+
+  const __nv_bfloat16* kp = static_cast<const __nv_bfloat16*>(a.k_pool);
+  const __nv_bfloat16* vp = static_cast<const __nv_bfloat16*>(a.v_pool);
+  const __nv_bfloat16* skp = static_cast<const __nv_bfloat16*>(a.sum_k);
+  const __nv_bfloat16* svp = static_cast<const __nv_bfloat16*>(a.sum_v);
+  MmaTile<D> ta, tb;
+  mma_load_tile<D>(ta, tab, 0, r, c, kp, vp, skp, svp);
+  int t0 = 0;
+  while (true) {
+    if (t0 + 16 < nrows) mma_load_tile<D>(tb, tab, t0 + 16, r, c, kp, vp, skp, svp);
+    mma_compute_tile<D>(st, ta, a.scale_log2, c);
+    t0 += 16;
+    if (t0 >= nrows) break;
+    if (t0 + 16 < nrows) mma_load_tile<D>(ta, tab, t0 + 16, r, c, kp, vp, skp, svp);
+    mma_compute_tile<D>(st, tb, a.scale_log2, c);
+    t0 += 16;
+    if (t0 >= nrows) break;
+  }
+
+  // head r's sum: add the parts of the four lanes that share r.
+  float l = st.l;
+  l += __shfl_xor_sync(kFull, l, 1);
+  l += __shfl_xor_sync(kFull, l, 2);
+  if (c == 0 && r < G) a.part_ml[static_cast<size_t>(slot) * G + r] = make_float2(st.m, l);
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    const int h = 2 * c + e;
+    if (h < G) {
+      float* dst = a.part_o + (static_cast<size_t>(slot) * G + h) * D + (D / 8) * r;
+#pragma unroll
+      for (int i = 0; i < D / 16; i += 2) {
+        const float4 v = make_float4(st.o[i][e], st.o[i][e + 2], st.o[i + 1][e], st.o[i + 1][e + 2]);
+        *reinterpret_cast<float4*>(dst + 2 * i) = v;
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ attend: CUDA cores (f32, or any G)
+template <typename T, int D>
+__global__ void __launch_bounds__(kAttendWarps * 32) zr_attend_fma_kernel(StepArgs a) {
+  constexpr int E = D / 32;
+  __shared__ uint32_t rowtab[kAttendWarps][kChunkRows];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int slot = blockIdx.x * kAttendWarps + warp;
+  pdl_trigger();
+  if (slot >= a.total_slots) return;
+  const SlotInfo s = decode_slot(a, slot, lane);
+  pdl_wait();
+  const int4 info = a.unit_info[s.u];
+  if (s.c >= info.w) return;
+  const int rows = info.y + info.z;
+  const int row0 = s.c * a.chunk_rows;
+  const int nrows = min(a.chunk_rows, rows - row0);
+  uint32_t* tab = rowtab[warp];
+  build_row_table(a, s, info, row0, nrows, tab, lane);
+
+  const int G = a.G;
+  const T* qg = static_cast<const T*>(a.q) + (static_cast<size_t>(s.b) * a.Hq + static_cast<size_t>(s.g) * G) * D;
+  float qv[kMaxGroup][E], o[kMaxGroup][E], m[kMaxGroup], l[kMaxGroup];
+#pragma unroll
+  for (int h = 0; h < kMaxGroup; ++h) {
+    m[h] = -1e30f;
+    l[h] = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) o[h][e] = 0.f;
+    if (h < G) {
+      load_e<T, E>(qg + h * D + lane * E, qv[h]);
+    } else {
+#pragma unroll
+      for (int e = 0; e < E; ++e) qv[h][e] = 0.f;
+    }
+  }
+  const T* kp = static_cast<const T*>(a.k_pool);
+  const T* vp = static_cast<const T*>(a.v_pool);
+  const T* skp = static_cast<const T*>(a.sum_k);
+  const T* svp = static_cast<const T*>(a.sum_v);
+  for (int j = 0; j < nrows; ++j) {
+    const uint32_t id = tab[j];
+    if (id == kInvalidRow) continue;
+    float kv[E], vv[E];
+    load_e<T, E>(row_ptr<T, D>(id, kp, skp) + lane * E, kv);
+    load_e<T, E>(row_ptr<T, D>(id, vp, svp) + lane * E, vv);
+#pragma unroll
+    for (int h = 0; h < kMaxGroup; ++h) {
+      if (h < G) {
+        float dot = 0.f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) dot = fmaf(qv[h][e], kv[e], dot);
+#pragma unroll
+        for (int o2 = 16; o2 > 0; o2 >>= 1) dot += __shfl_xor_sync(kFull, dot, o2);
+        const float x = dot * a.scale_log2;
+        const float mn = fmaxf(m[h], x);
+        const float alpha = fast_exp2(m[h] - mn);
+        const float p = fast_exp2(x - mn);
+        l[h] = l[h] * alpha + p;
+#pragma unroll
+        for (int e = 0; e < E; ++e) o[h][e] = fmaf(p, vv[e], o[h][e] * alpha);
+        m[h] = mn;
+      }
+    }
+  }
+#pragma unroll
+  for (int h = 0; h < kMaxGroup; ++h) {
+    if (h < G) {
+      float* dst = a.part_o + (static_cast<size_t>(slot) * G + h) * D + lane * E;
+#pragma unroll
+      for (int e = 0; e < E; ++e) dst[e] = o[h][e];
+      if (lane == 0) a.part_ml[static_cast<size_t>(slot) * G + h] = make_float2(m[h], l[h]);
+    }
+  }
+}
+
+// ------------------------------------------------------------------ merge
+template <int D>
+__global__ void __launch_bounds__(kAttendWarps * 32) zr_merge_kernel(StepArgs a) {
+  constexpr int E = D / 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int w = blockIdx.x * kAttendWarps + warp;
+  pdl_trigger();
+  if (w >= a.B * a.Hq) return;
+  const int b = w / a.Hq, h = w - b * a.Hq;
+  const int G = a.G, g = h / G, hh = h - g * G;
+  const int u = b * a.Hkv + g;
+  const int base = a.meta.slot_base[b] + g * a.meta.slots[b];
+  pdl_wait();
+  const int nch = a.unit_info[u].w;
+  float M = -INFINITY;
+  for (int c = lane; c < nch; c += 32) M = fmaxf(M, a.part_ml[static_cast<size_t>(base + c) * G + hh].x);
+#pragma unroll
+  for (int o2 = 16; o2 > 0; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o2));
+  float acc[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  float Ls = 0.f;
+  for (int c = 0; c < nch; ++c) {
+    const float2 ml = a.part_ml[static_cast<size_t>(base + c) * G + hh];
+    const float wgt = fast_exp2(ml.x - M);
+    Ls = fmaf(ml.y, wgt, Ls);
+    const float* src = a.part_o + (static_cast<size_t>(base + c) * G + hh) * D + lane * E;
+    float v[E];
+    load_e<float, E>(src, v);
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] = fmaf(wgt, v[e], acc[e]);
+  }
+  const float inv = 1.f / Ls;
+  float* dst = a.out + (static_cast<size_t>(b) * a.Hq + h) * D + lane * E;
+#pragma unroll
+  for (int e = 0; e < E; ++e) dst[e] = acc[e] * inv;
+}
+
+// ------------------------------------------------------------------ launch
+template <typename Kern>
+cudaError_t launch_pdl(Kern kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t s, const StepArgs& a) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, a);
+}
+
+size_t select_smem_bytes(int d, int n_max) {
+  return static_cast<size_t>(kMaxGroup) * d * 4 + static_cast<size_t>(n_max) * 4 * 6 + 16;
+}
+
+template <typename T, int D>
+zr_status configure_for(Plan& p) {
+  p.select_smem = select_smem_bytes(D, p.n_max);
+  if (p.select_smem > 48 * 1024) {
+    if (cudaFuncSetAttribute(zr_select_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(p.select_smem)) != cudaSuccess) {
+      cudaGetLastError();
+      return ZR_ECUDA;
+    }
+  }
+  return ZR_OK;
+}
+
+template <typename T, int D>
+cudaError_t launch_for(const Plan& p, const StepArgs& a, cudaStream_t s, cudaEvent_t ev0, cudaEvent_t ev1) {
+  cudaError_t e = launch_pdl(zr_select_kernel<T, D>, dim3(p.Hkv, p.B), dim3(kSelectThreads), p.select_smem, s, a);
+  if (e != cudaSuccess) return e;
+  if (ev0 && (e = cudaEventRecordWithFlags(ev0, s, cudaEventRecordExternal)) != cudaSuccess) return e;
+  const dim3 grid_attend((p.total_slots + kAttendWarps - 1) / kAttendWarps);
+  bool use_mma = false;
+  if constexpr (sizeof(T) == 2) use_mma = p.G <= kMmaMaxGroup;
+  if (use_mma) {
+    if constexpr (sizeof(T) == 2) e = launch_pdl(zr_attend_mma_kernel<D>, grid_attend, dim3(kAttendWarps * 32), 0, s, a);
+  } else {
+    e = launch_pdl(zr_attend_fma_kernel<T, D>, grid_attend, dim3(kAttendWarps * 32), 0, s, a);
+  }
+  if (e != cudaSuccess) return e;
+  if (ev1 && (e = cudaEventRecordWithFlags(ev1, s, cudaEventRecordExternal)) != cudaSuccess) return e;
+  const dim3 grid_merge((p.B * p.Hq + kAttendWarps - 1) / kAttendWarps);
+  return launch_pdl(zr_merge_kernel<D>, grid_merge, dim3(kAttendWarps * 32), 0, s, a);
+}
+
+}  // namespace
+
+zr_status configure_kernels(Plan& p) {
+  if (p.cfg.dtype == ZR_BF16) return p.d == 64 ? configure_for<__nv_bfloat16, 64>(p) : configure_for<__nv_bfloat16, 128>(p);
+  return p.d == 64 ? configure_for<float, 64>(p) : configure_for<float, 128>(p);
+}
+
+zr_status launch_step(const Plan& p, const StepArgs& a, void* stream, void* ev_start, void* ev_stop) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaEvent_t e0 = static_cast<cudaEvent_t>(ev_start), e1 = static_cast<cudaEvent_t>(ev_stop);
+  cudaError_t e;
+  if (p.cfg.dtype == ZR_BF16)
+    e = p.d == 64 ? launch_for<__nv_bfloat16, 64>(p, a, s, e0, e1) : launch_for<__nv_bfloat16, 128>(p, a, s, e0, e1);
+  else
+    e = p.d == 64 ? launch_for<float, 64>(p, a, s, e0, e1) : launch_for<float, 128>(p, a, s, e0, e1);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return ZR_ECUDA;
+  }
+  return ZR_OK;
+}
+
+}  // namespace zr

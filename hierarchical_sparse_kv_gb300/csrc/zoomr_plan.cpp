@@ -1,0 +1,298 @@
+// Host side of the C ABI: validation of the problem statement, the plan, the
+// workspace layout, device-error readback.
+//
+// The plan turns the caller's host metadata (sequence lengths, segment bounds,
+// per-sequence top-k) into a few small device arrays and fixes, per sequence,
+// how many split slots each (sequence, KV head) unit may use. The bound on a
+// unit's gathered rows is exact arithmetic on the metadata: at most
+// min(L, min(w, L) + sum of the k largest segment lengths) tokens (the window
+// and the selected segments' ranges, ZoomR page 3.3 "Constructing the Final
+// Multi-Granularity Context") plus exactly n - k summary rows.
+
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <functional>
+#include <new>
+#include <vector>
+
+#include "zoomr_internal.h"
+
+namespace {
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+zr_status validate(const zr_config* c, const int32_t* seq_lens, const int32_t* seg_ptr, const int32_t* seg_bounds,
+                   const int32_t* topk) {
+  if (!c || !seq_lens || !seg_ptr || !seg_bounds || !topk) return ZR_EINVAL;
+  if (c->batch < 1 || c->num_q_heads < 1 || c->num_kv_heads < 1) return ZR_EINVAL;
+  if (c->num_q_heads % c->num_kv_heads != 0) return ZR_EINVAL;
+  if (c->block_size != zr::kBlockTokens) return ZR_EINVAL;
+  if (c->num_blocks < 1 || c->max_blocks_per_seq < 1 || c->window < 0) return ZR_EINVAL;
+  if (c->dtype != ZR_F32 && c->dtype != ZR_BF16) return ZR_EINVAL;
+  if (c->head_dim != 64 && c->head_dim != 128) return c->head_dim < 1 ? ZR_EINVAL : ZR_EUNSUPPORTED;
+  if (c->num_q_heads / c->num_kv_heads > zr::kMaxGroup) return ZR_EUNSUPPORTED;
+  // Row ids of the pool are (block * Hkv + head) * 16 + slot and must stay below 2^31.
+  if (static_cast<int64_t>(c->num_blocks) * c->num_kv_heads * zr::kBlockTokens >= (int64_t(1) << 31))
+    return ZR_EUNSUPPORTED;
+  if (seg_ptr[0] != 0) return ZR_EINVAL;
+  for (int b = 0; b < c->batch; ++b) {
+    const int32_t L = seq_lens[b];
+    if (L < 1 || static_cast<int64_t>(L) > static_cast<int64_t>(c->max_blocks_per_seq) * zr::kBlockTokens)
+      return ZR_EINVAL;
+    const int64_t n = static_cast<int64_t>(seg_ptr[b + 1]) - seg_ptr[b];
+    if (n < 1) return ZR_EINVAL;
+    if (n > zr::kMaxSegments) return ZR_EUNSUPPORTED;
+    if (topk[b] < 0) return ZR_EINVAL;
+  }
+  const int64_t total = seg_ptr[c->batch];
+  if (total * c->num_kv_heads >= (int64_t(1) << 31)) return ZR_EUNSUPPORTED;
+  for (int b = 0; b < c->batch; ++b) {
+    const int32_t* bd = seg_bounds + seg_ptr[b] + b;
+    const int n = seg_ptr[b + 1] - seg_ptr[b];
+    if (bd[0] != 0 || bd[n] != seq_lens[b]) return ZR_EINVAL;
+    for (int i = 0; i < n; ++i)
+      if (bd[i + 1] <= bd[i]) return ZR_EINVAL;
+  }
+  return ZR_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+zr_status zr_plan(const zr_config* cfg, const int32_t* seq_lens, const int32_t* seg_ptr, const int32_t* seg_bounds,
+                  const int32_t* topk, zr_plan_t* out_plan, size_t* workspace_bytes) {
+  if (!out_plan || !workspace_bytes) return ZR_EINVAL;
+  *out_plan = nullptr;
+  *workspace_bytes = 0;
+  zr_status st = validate(cfg, seq_lens, seg_ptr, seg_bounds, topk);
+  if (st != ZR_OK) return st;
+
+  struct zr_plan* P = new (std::nothrow) struct zr_plan();
+  if (!P) return ZR_ENOMEM;
+  zr::Plan& p = P->p;
+  p.cfg = *cfg;
+  p.B = cfg->batch;
+  p.Hq = cfg->num_q_heads;
+  p.Hkv = cfg->num_kv_heads;
+  p.G = p.Hq / p.Hkv;
+  p.d = cfg->head_dim;
+  p.window = cfg->window;
+  p.num_blocks = cfg->num_blocks;
+  p.max_blocks = cfg->max_blocks_per_seq;
+  p.total_segments = seg_ptr[p.B];
+  p.chunk_rows = zr::kChunkRows;
+
+  std::vector<int32_t> kclip(p.B), slots(p.B), slot_base(p.B + 1, 0);
+  p.k_max = 1;
+  p.n_max = 1;
+  int64_t total_slots = 0;
+  for (int b = 0; b < p.B; ++b) {
+    const int n = seg_ptr[b + 1] - seg_ptr[b];
+    const int32_t* bd = seg_bounds + seg_ptr[b] + b;
+    const int L = seq_lens[b];
+    kclip[b] = std::min(topk[b], n);
+    p.k_max = std::max(p.k_max, kclip[b]);
+    p.n_max = std::max(p.n_max, n);
+    std::vector<int32_t> lens(n);
+    for (int i = 0; i < n; ++i) lens[i] = bd[i + 1] - bd[i];
+    std::sort(lens.begin(), lens.end(), std::greater<int32_t>());
+    int64_t top = 0;
+    for (int i = 0; i < kclip[b]; ++i) top += lens[i];
+    const int64_t tok_bound = std::min<int64_t>(L, std::min<int64_t>(p.window, L) + top);
+    const int64_t rows_bound = tok_bound + (n - kclip[b]);
+    slots[b] = static_cast<int32_t>((rows_bound + p.chunk_rows - 1) / p.chunk_rows);
+    slot_base[b] = static_cast<int32_t>(total_slots);
+    total_slots += static_cast<int64_t>(slots[b]) * p.Hkv;
+    if (total_slots >= (int64_t(1) << 30)) {
+      delete P;
+      return ZR_EUNSUPPORTED;
+    }
+  }
+  slot_base[p.B] = static_cast<int32_t>(total_slots);
+  p.total_slots = static_cast<int>(total_slots);
+
+  // Workspace layout (each region 256-byte aligned).
+  const size_t U = static_cast<size_t>(p.B) * p.Hkv;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t at = off;
+    off = align_up(off + bytes, 256);
+    return at;
+  };
+  p.ws.err = take(sizeof(int32_t));
+  p.ws.unit_info = take(U * 4 * sizeof(int32_t));
+  p.ws.ranges = take(U * (p.k_max + 1) * 2 * sizeof(int32_t));
+  p.ws.cum = take(U * (p.k_max + 2) * sizeof(int32_t));
+  p.ws.sumlist = take(U * p.n_max * sizeof(int32_t));
+  p.ws.sel = take(U * p.k_max * sizeof(int32_t));
+  p.ws.part_o = take(static_cast<size_t>(p.total_slots) * p.G * p.d * sizeof(float));
+  p.ws.part_ml = take(static_cast<size_t>(p.total_slots) * p.G * 2 * sizeof(float));
+  p.ws.total = off;
+
+  // Device metadata: one allocation, synchronous copies.
+  const size_t nb = static_cast<size_t>(p.B);
+  const size_t n_bounds = static_cast<size_t>(p.total_segments) + nb;
+  size_t moff = 0;
+  auto mtake = [&](size_t count) {
+    size_t at = moff;
+    moff = align_up(moff + count * sizeof(int32_t), 256);
+    return at;
+  };
+  const size_t o_len = mtake(nb), o_ptr = mtake(nb + 1), o_bnd = mtake(n_bounds), o_topk = mtake(nb),
+               o_sbase = mtake(nb + 1), o_slots = mtake(nb);
+  if (cudaGetDevice(&p.device) != cudaSuccess) {
+    cudaGetLastError();
+    delete P;
+    return ZR_ECUDA;
+  }
+  void* base = nullptr;
+  cudaError_t ce = cudaMalloc(&base, moff);
+  if (ce != cudaSuccess) {
+    cudaGetLastError();
+    delete P;
+    return ce == cudaErrorMemoryAllocation ? ZR_ENOMEM : ZR_ECUDA;
+  }
+  p.d_meta_base = base;
+  char* cb = static_cast<char*>(base);
+  p.meta.seq_lens = reinterpret_cast<int32_t*>(cb + o_len);
+  p.meta.seg_ptr = reinterpret_cast<int32_t*>(cb + o_ptr);
+  p.meta.seg_bounds = reinterpret_cast<int32_t*>(cb + o_bnd);
+  p.meta.topk = reinterpret_cast<int32_t*>(cb + o_topk);
+  p.meta.slot_base = reinterpret_cast<int32_t*>(cb + o_sbase);
+  p.meta.slots = reinterpret_cast<int32_t*>(cb + o_slots);
+  bool ok = cudaMemcpy(p.meta.seq_lens, seq_lens, nb * 4, cudaMemcpyHostToDevice) == cudaSuccess &&
+            cudaMemcpy(p.meta.seg_ptr, seg_ptr, (nb + 1) * 4, cudaMemcpyHostToDevice) == cudaSuccess &&
+            cudaMemcpy(p.meta.seg_bounds, seg_bounds, n_bounds * 4, cudaMemcpyHostToDevice) == cudaSuccess &&
+            cudaMemcpy(p.meta.topk, kclip.data(), nb * 4, cudaMemcpyHostToDevice) == cudaSuccess &&
+            cudaMemcpy(p.meta.slot_base, slot_base.data(), (nb + 1) * 4, cudaMemcpyHostToDevice) == cudaSuccess &&
+            cudaMemcpy(p.meta.slots, slots.data(), nb * 4, cudaMemcpyHostToDevice) == cudaSuccess;
+  if (!ok) {
+    cudaGetLastError();
+    cudaFree(base);
+    delete P;
+    return ZR_ECUDA;
+  }
+  st = zr::configure_kernels(p);
+  if (st != ZR_OK) {
+    cudaFree(base);
+    delete P;
+    return st;
+  }
+  *out_plan = P;
+  *workspace_bytes = p.ws.total;
+  return ZR_OK;
+}
+
+zr_status zr_plan_dims(zr_plan_t plan, int32_t* k_max, int32_t* n_max) {
+  if (!plan || !k_max || !n_max) return ZR_EINVAL;
+  *k_max = plan->p.k_max;
+  *n_max = plan->p.n_max;
+  return ZR_OK;
+}
+
+static zr_status decode_common(zr_plan_t plan, void* workspace, const void* q, const void* k_pool, const void* v_pool,
+                               const int32_t* block_tables, const void* sum_k, const void* sum_v, float* out,
+                               int32_t* sel_out, int32_t* ranges_out, int32_t* nranges_out, void* stream,
+                               void* ev_start, void* ev_stop) {
+  if (!plan || !workspace || !q || !k_pool || !v_pool || !block_tables || !sum_k || !sum_v || !out) return ZR_EINVAL;
+  if (!aligned(workspace, 256) || !aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) ||
+      !aligned(sum_k, 16) || !aligned(sum_v, 16) || !aligned(out, 16) || !aligned(block_tables, 4))
+    return ZR_EINVAL;
+  const zr::Plan& p = plan->p;
+  char* ws = static_cast<char*>(workspace);
+  zr::StepArgs a;
+  a.q = q;
+  a.k_pool = k_pool;
+  a.v_pool = v_pool;
+  a.block_tables = block_tables;
+  a.sum_k = sum_k;
+  a.sum_v = sum_v;
+  a.out = out;
+  a.sel_out = sel_out;
+  a.ranges_out = ranges_out;
+  a.nranges_out = nranges_out;
+  a.meta = p.meta;
+  a.err = reinterpret_cast<int32_t*>(ws + p.ws.err);
+  a.unit_info = reinterpret_cast<int4*>(ws + p.ws.unit_info);
+  a.ranges = reinterpret_cast<int32_t*>(ws + p.ws.ranges);
+  a.cum = reinterpret_cast<int32_t*>(ws + p.ws.cum);
+  a.sumlist = reinterpret_cast<int32_t*>(ws + p.ws.sumlist);
+  a.sel = reinterpret_cast<int32_t*>(ws + p.ws.sel);
+  a.part_o = reinterpret_cast<float*>(ws + p.ws.part_o);
+  a.part_ml = reinterpret_cast<float2*>(ws + p.ws.part_ml);
+  a.B = p.B;
+  a.Hq = p.Hq;
+  a.Hkv = p.Hkv;
+  a.G = p.G;
+  a.window = p.window;
+  a.num_blocks = p.num_blocks;
+  a.max_blocks = p.max_blocks;
+  a.k_max = p.k_max;
+  a.n_max = p.n_max;
+  a.total_slots = p.total_slots;
+  a.chunk_rows = p.chunk_rows;
+  a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(p.d)));
+  return zr::launch_step(p, a, stream, ev_start, ev_stop);
+}
+
+zr_status zr_decode_attend(zr_plan_t plan, void* workspace, const void* q, const void* k_pool, const void* v_pool,
+                           const int32_t* block_tables, const void* sum_k, const void* sum_v, float* out,
+                           int32_t* sel_out, int32_t* ranges_out, int32_t* nranges_out, void* stream) {
+  return decode_common(plan, workspace, q, k_pool, v_pool, block_tables, sum_k, sum_v, out, sel_out, ranges_out,
+                       nranges_out, stream, nullptr, nullptr);
+}
+
+zr_status zr_decode_attend_timed(zr_plan_t plan, void* workspace, const void* q, const void* k_pool,
+                                 const void* v_pool, const int32_t* block_tables, const void* sum_k,
+                                 const void* sum_v, float* out, void* ev_start, void* ev_stop, void* stream) {
+  if (!ev_start || !ev_stop) return ZR_EINVAL;
+  return decode_common(plan, workspace, q, k_pool, v_pool, block_tables, sum_k, sum_v, out, nullptr, nullptr,
+                       nullptr, stream, ev_start, ev_stop);
+}
+
+zr_status zr_get_device_error(zr_plan_t plan, void* workspace, void* stream, int32_t* err_code) {
+  if (!plan || !workspace || !err_code) return ZR_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t* dev = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + plan->p.ws.err);
+  int32_t v = 0;
+  if (cudaStreamSynchronize(s) != cudaSuccess || cudaMemcpy(&v, dev, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) {
+    cudaGetLastError();
+    return ZR_ECUDA;
+  }
+  *err_code = v;
+  if (v != 0) {
+    if (cudaMemset(dev, 0, sizeof(v)) != cudaSuccess) {
+      cudaGetLastError();
+      return ZR_ECUDA;
+    }
+    return ZR_EDEVICE;
+  }
+  return ZR_OK;
+}
+
+void zr_free(zr_plan_t plan) {
+  if (!plan) return;
+  if (plan->p.d_meta_base) cudaFree(plan->p.d_meta_base);
+  delete plan;
+}
+
+const char* zr_status_string(zr_status s) {
+  switch (s) {
+    case ZR_OK: return "ZR_OK";
+    case ZR_EINVAL: return "ZR_EINVAL: invalid argument";
+    case ZR_ENOMEM: return "ZR_ENOMEM: allocation failed";
+    case ZR_ECUDA: return "ZR_ECUDA: CUDA runtime error";
+    case ZR_EUNSUPPORTED: return "ZR_EUNSUPPORTED: outside this build's limits";
+    case ZR_EDEVICE: return "ZR_EDEVICE: the device reported a bad index";
+  }
+  return "unknown zr_status";
+}
+
+}  // extern "C"

@@ -1,0 +1,234 @@
+"""Thin ctypes binding of ``libzoomr.so`` (declared in ``include/zoomr.h``).
+
+The functions carry the C names and only marshal arguments: torch tensors are
+passed as raw device pointers, host metadata as int32 arrays. Every step of the
+decode runs in the library's CUDA kernels; there is no Python or CPU fallback,
+and a missing library raises ``ZoomrLibraryMissing``.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence, Tuple
+
+import numpy as np
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libzoomr.so")
+
+ZR_OK, ZR_EINVAL, ZR_ENOMEM, ZR_ECUDA, ZR_EUNSUPPORTED, ZR_EDEVICE = range(6)
+ZR_F32, ZR_BF16 = 0, 1
+DTYPES = {"f32": ZR_F32, "bf16": ZR_BF16}
+TORCH_DTYPES = {ZR_F32: torch.float32, ZR_BF16: torch.bfloat16}
+
+
+class ZoomrLibraryMissing(RuntimeError):
+    pass
+
+
+class ZoomrError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {zr_status_string(status)}")
+
+
+class zr_config(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("block_size", ctypes.c_int32), ("num_blocks", ctypes.c_int32),
+                ("max_blocks_per_seq", ctypes.c_int32), ("window", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+
+
+_lib: Optional[ctypes.CDLL] = None
+_P = ctypes.c_void_p
+_I32P = ctypes.POINTER(ctypes.c_int32)
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load the library (once). Raises ZoomrLibraryMissing if it was not built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ZoomrLibraryMissing(f"{path} is missing: build it with `python -m hierarchical_sparse_kv_gb300.build`")
+    lib = ctypes.CDLL(path)
+    lib.zr_plan.argtypes = [ctypes.POINTER(zr_config), _I32P, _I32P, _I32P, _I32P, ctypes.POINTER(_P),
+                            ctypes.POINTER(ctypes.c_size_t)]
+    lib.zr_plan.restype = ctypes.c_int
+    lib.zr_plan_dims.argtypes = [_P, _I32P, _I32P]
+    lib.zr_plan_dims.restype = ctypes.c_int
+    lib.zr_decode_attend.argtypes = [_P] * 13
+    lib.zr_decode_attend.restype = ctypes.c_int
+    lib.zr_decode_attend_timed.argtypes = [_P] * 12
+    lib.zr_decode_attend_timed.restype = ctypes.c_int
+    lib.zr_get_device_error.argtypes = [_P, _P, _P, _I32P]
+    lib.zr_get_device_error.restype = ctypes.c_int
+    lib.zr_free.argtypes = [_P]
+    lib.zr_free.restype = None
+    lib.zr_status_string.argtypes = [ctypes.c_int]
+    lib.zr_status_string.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def zr_status_string(status: int) -> str:
+    return load().zr_status_string(int(status)).decode()
+
+
+def _i32(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+
+
+def _ptr32(a: np.ndarray):
+    return a.ctypes.data_as(_I32P)
+
+
+def _dev(t: Optional[torch.Tensor]) -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError("zoomr: tensors must be contiguous CUDA tensors")
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def zr_plan(cfg: zr_config, seq_lens, seg_ptr, seg_bounds, topk) -> Tuple[int, int]:
+    """Returns (plan handle, workspace bytes). Raises ZoomrError on a non-OK status."""
+    lib = load()
+    a = [_i32(x) for x in (seq_lens, seg_ptr, seg_bounds, topk)]
+    plan = _P()
+    ws = ctypes.c_size_t()
+    st = lib.zr_plan(ctypes.byref(cfg), *[_ptr32(x) for x in a], ctypes.byref(plan), ctypes.byref(ws))
+    if st != ZR_OK:
+        raise ZoomrError(st, "zr_plan")
+    return plan.value, ws.value
+
+
+def zr_plan_status(cfg: Optional[zr_config], seq_lens, seg_ptr, seg_bounds, topk) -> int:
+    """zr_plan's raw status (any plan created is freed): for error-path tests."""
+    lib = load()
+    a = [_i32(x) for x in (seq_lens, seg_ptr, seg_bounds, topk)]
+    plan = _P()
+    ws = ctypes.c_size_t()
+    st = lib.zr_plan(ctypes.byref(cfg) if cfg is not None else None, *[_ptr32(x) for x in a], ctypes.byref(plan),
+                     ctypes.byref(ws))
+    if st == ZR_OK:
+        lib.zr_free(plan)
+    return st
+
+
+def zr_plan_dims(plan: int) -> Tuple[int, int]:
+    k_max, n_max = ctypes.c_int32(), ctypes.c_int32()
+    st = load().zr_plan_dims(plan, ctypes.byref(k_max), ctypes.byref(n_max))
+    if st != ZR_OK:
+        raise ZoomrError(st, "zr_plan_dims")
+    return k_max.value, n_max.value
+
+
+def zr_decode_attend(plan: int, workspace: torch.Tensor, q: torch.Tensor, k_pool: torch.Tensor,
+                     v_pool: torch.Tensor, block_tables: torch.Tensor, sum_k: torch.Tensor, sum_v: torch.Tensor,
+                     out: torch.Tensor, sel_out: Optional[torch.Tensor] = None,
+                     ranges_out: Optional[torch.Tensor] = None, nranges_out: Optional[torch.Tensor] = None,
+                     stream=None) -> None:
+    st = load().zr_decode_attend(plan, _dev(workspace), _dev(q), _dev(k_pool), _dev(v_pool), _dev(block_tables),
+                                 _dev(sum_k), _dev(sum_v), _dev(out), _dev(sel_out), _dev(ranges_out),
+                                 _dev(nranges_out), _stream(stream))
+    if st != ZR_OK:
+        raise ZoomrError(st, "zr_decode_attend")
+
+
+def zr_decode_attend_timed(plan: int, workspace: torch.Tensor, q: torch.Tensor, k_pool: torch.Tensor,
+                           v_pool: torch.Tensor, block_tables: torch.Tensor, sum_k: torch.Tensor,
+                           sum_v: torch.Tensor, out: torch.Tensor, ev_start: torch.cuda.Event,
+                           ev_stop: torch.cuda.Event, stream=None) -> None:
+    st = load().zr_decode_attend_timed(plan, _dev(workspace), _dev(q), _dev(k_pool), _dev(v_pool),
+                                       _dev(block_tables), _dev(sum_k), _dev(sum_v), _dev(out),
+                                       ev_start.cuda_event, ev_stop.cuda_event, _stream(stream))
+    if st != ZR_OK:
+        raise ZoomrError(st, "zr_decode_attend_timed")
+
+
+def zr_get_device_error(plan: int, workspace: torch.Tensor, stream=None) -> int:
+    code = ctypes.c_int32()
+    st = load().zr_get_device_error(plan, _dev(workspace), _stream(stream), ctypes.byref(code))
+    if st not in (ZR_OK, ZR_EDEVICE):
+        raise ZoomrError(st, "zr_get_device_error")
+    return code.value
+
+
+def zr_free(plan: Optional[int]) -> None:
+    if plan:
+        load().zr_free(plan)
+
+
+class DecodePlan:
+    """A plan plus its workspace: one ZoomR decode step per call, on the current stream.
+
+    Host metadata follow the C ABI (``include/zoomr.h``): seq_lens [B], seg_ptr
+    [B+1] (CSR over segments), seg_bounds (sequence b's n_b + 1 bounds start at
+    seg_ptr[b] + b), topk [B]. Tensors passed to ``run`` are the caller's.
+    """
+
+    def __init__(self, *, batch: int, num_q_heads: int, num_kv_heads: int, head_dim: int, num_blocks: int,
+                 max_blocks_per_seq: int, window: int, dtype: str, seq_lens: Sequence[int], seg_ptr: Sequence[int],
+                 seg_bounds: Sequence[int], topk: Sequence[int], device=None):
+        self.cfg = zr_config(batch, num_q_heads, num_kv_heads, head_dim, 16, num_blocks, max_blocks_per_seq, window,
+                             DTYPES[dtype])
+        self.device = torch.device(device if device is not None else "cuda")
+        with torch.cuda.device(self.device):
+            self.handle, self.workspace_bytes = zr_plan(self.cfg, seq_lens, seg_ptr, seg_bounds, topk)
+            self.k_max, self.n_max = zr_plan_dims(self.handle)
+            self.workspace = torch.zeros(max(self.workspace_bytes, 256) // 4 + 64, dtype=torch.int32,
+                                         device=self.device)
+        # 256-byte aligned view of the workspace
+        off = (-self.workspace.data_ptr()) % 256
+        self.ws = self.workspace[off // 4:]
+        assert self.ws.data_ptr() % 256 == 0
+        self.batch, self.num_q_heads, self.num_kv_heads, self.head_dim = batch, num_q_heads, num_kv_heads, head_dim
+
+    @classmethod
+    def from_structure(cls, st, device=None) -> "DecodePlan":
+        """Plan for a ``workloads.Structure`` (any object with the same fields)."""
+        sp = st.spec
+        return cls(batch=st.batch, num_q_heads=sp.num_q_heads, num_kv_heads=sp.num_kv_heads, head_dim=sp.head_dim,
+                   num_blocks=st.num_blocks, max_blocks_per_seq=st.max_blocks_per_seq, window=st.window,
+                   dtype=sp.dtype, seq_lens=st.seq_lens, seg_ptr=st.seg_ptr, seg_bounds=st.seg_bounds, topk=st.topk,
+                   device=device)
+
+    def new_debug_outputs(self):
+        B, H = self.batch, self.num_kv_heads
+        sel = torch.full((B, H, self.k_max), -2, dtype=torch.int32, device=self.device)
+        rng = torch.full((B, H, self.k_max + 1, 2), -2, dtype=torch.int32, device=self.device)
+        nr = torch.full((B, H), -2, dtype=torch.int32, device=self.device)
+        return sel, rng, nr
+
+    def run(self, q, k_pool, v_pool, block_tables, sum_k, sum_v, out, debug=None, stream=None) -> None:
+        sel, rng, nr = debug if debug is not None else (None, None, None)
+        zr_decode_attend(self.handle, self.ws, q, k_pool, v_pool, block_tables, sum_k, sum_v, out, sel, rng, nr,
+                         stream)
+
+    def run_timed(self, q, k_pool, v_pool, block_tables, sum_k, sum_v, out, ev_start, ev_stop, stream=None):
+        zr_decode_attend_timed(self.handle, self.ws, q, k_pool, v_pool, block_tables, sum_k, sum_v, out, ev_start,
+                               ev_stop, stream)
+
+    def device_error(self, stream=None) -> int:
+        return zr_get_device_error(self.handle, self.ws, stream)
+
+    def close(self):
+        if getattr(self, "handle", None):
+            zr_free(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,170 @@
+/*
+ * zoomr.h -- C ABI of the GB300 (sm_103a) ZoomR decode step over a paged KV cache.
+ *
+ * One call computes, for every sequence b and every KV head g of a GQA layer
+ * (a "unit"), the four stages of ZoomR's decode-time retrieval:
+ *
+ *   1. score    ZoomR page, 3.3 "Per-Head Importance Scoring and Voting", the
+ *               equation alpha_i = q_t^T kbar_i: every segment's summary key is
+ *               scored against the query. Per KV head the score is the maximum
+ *               over the group's query heads. The ranking key is the fp32 dot
+ *               product with each product and each partial sum rounded to
+ *               nearest-even, summed in ascending component order (the 1/sqrt(d)
+ *               scale does not change the ranking and is not applied to it).
+ *   2. select   ZoomR 3.3, the equation I_top-k = argtop-k(alpha): the k_b
+ *               segments with the largest keys; ties go to the lower segment
+ *               index; k_b >= n_b selects every segment, k_b = 0 none.
+ *   3. gather   ZoomR 3.3, "Constructing the Final Multi-Granularity Context",
+ *               the equation for I_f: the token set is the union of the recent
+ *               window [max(0, L_b - w), L_b) and the token ranges of the selected
+ *               segments (deduplicated); every segment that is not selected
+ *               contributes its one summary key/value row. Token t of sequence b
+ *               is read through the block table as on the "KV-cache management"
+ *               page, "Paged KV cache (PagedAttention)": physical block
+ *               block_tables[b][t / 16], slot t % 16.
+ *   4. attend   ZoomR 2 "Background", A = softmax(q K^T / sqrt(d)) V over exactly
+ *               that set, for every query head of the group (GQA as on the
+ *               "KV-cache management" page, "Fewer key/value heads per token"):
+ *               query head h reads KV head h / (Hq / Hkv).
+ *
+ * Conventions
+ *   - Every function returns a zr_status; nothing is thrown, nothing exits.
+ *   - ZR_EINVAL from zr_plan means nothing was allocated or launched.
+ *   - zr_decode_attend is asynchronous on the caller's stream and allocates
+ *     nothing. Indices that are found bad on the device (a physical block id
+ *     outside [0, num_blocks)) set a sticky error word in the workspace; the
+ *     offending row is skipped (no trap, no fault). zr_get_device_error reads
+ *     and clears it.
+ *   - The plan is immutable after creation and may be reused for any number of
+ *     layers and calls. Calls that may overlap on the GPU need separate
+ *     workspaces.
+ *   - The library never allocates the big tensors: q, the K/V pools, the block
+ *     tables, the summaries, the output and the workspace belong to the caller.
+ */
+#ifndef ZOOMR_H
+#define ZOOMR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define ZR_API __attribute__((visibility("default")))
+#else
+#define ZR_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ZR_OK = 0,
+  ZR_EINVAL = 1,        /* bad argument: a null pointer, a shape or a metadata array out of its contract */
+  ZR_ENOMEM = 2,        /* a host or device allocation of the plan failed */
+  ZR_ECUDA = 3,         /* a CUDA runtime call failed (no device, bad stream, launch failure) */
+  ZR_EUNSUPPORTED = 4,  /* valid but outside this build's limits (head_dim, group size, segment count) */
+  ZR_EDEVICE = 5        /* the device reported a bad index (see zr_get_device_error) */
+} zr_status;
+
+typedef enum { ZR_F32 = 0, ZR_BF16 = 1 } zr_dtype;
+
+typedef struct zr_plan* zr_plan_t; /* opaque */
+
+typedef struct {
+  int32_t batch;              /* B >= 1 sequences */
+  int32_t num_q_heads;        /* Hq >= 1 */
+  int32_t num_kv_heads;       /* Hkv >= 1, Hq % Hkv == 0, group G = Hq / Hkv <= 16 */
+  int32_t head_dim;           /* d, 64 or 128 */
+  int32_t block_size;         /* tokens per KV block: must be 16 */
+  int32_t num_blocks;         /* physical blocks in each K (and V) pool */
+  int32_t max_blocks_per_seq; /* columns of block_tables */
+  int32_t window;             /* w >= 0 recent tokens always attended */
+  int32_t dtype;              /* zr_dtype of q, the K/V pools and the summaries */
+} zr_config;
+
+/*
+ * zr_plan -- validate the host metadata and build an immutable plan.
+ *
+ * Host metadata (copied; the caller keeps ownership):
+ *   seq_lens   [B]      L_b >= 1 cached tokens, L_b <= 16 * max_blocks_per_seq.
+ *   seg_ptr    [B+1]    CSR over segments: sequence b owns segments
+ *                       seg_ptr[b] .. seg_ptr[b+1]-1; n_b = seg_ptr[b+1]-seg_ptr[b],
+ *                       1 <= n_b <= 4096; seg_ptr[0] = 0.
+ *   seg_bounds [seg_ptr[B] + B]  sequence b's n_b + 1 strictly ascending token
+ *                       bounds start at index seg_ptr[b] + b; the first is 0 and
+ *                       the last is L_b (segments partition the cached tokens).
+ *   topk       [B]      k_b >= 0; values above n_b are clipped to n_b.
+ * Outputs: *out_plan, and *workspace_bytes = the device workspace one call needs.
+ * zr_plan copies a few small device arrays (the metadata) with cudaMalloc on
+ * the current device; that device must be current for every later call.
+ * Errors: ZR_EINVAL (nothing allocated), ZR_EUNSUPPORTED, ZR_ENOMEM, ZR_ECUDA.
+ */
+ZR_API zr_status zr_plan(const zr_config* cfg, const int32_t* seq_lens, const int32_t* seg_ptr,
+                  const int32_t* seg_bounds, const int32_t* topk, zr_plan_t* out_plan,
+                  size_t* workspace_bytes);
+
+/*
+ * zr_plan_dims -- sizes of the optional debug outputs of a plan.
+ *   *k_max = max_b min(topk[b], n_b) (at least 1), *n_max = max_b n_b.
+ */
+ZR_API zr_status zr_plan_dims(zr_plan_t plan, int32_t* k_max, int32_t* n_max);
+
+/*
+ * zr_decode_attend -- one decode step of one layer, every unit.
+ *
+ * All pointers are DEVICE pointers owned by the caller; the call is async on
+ * `stream` (a cudaStream_t; NULL is the legacy default stream).
+ *   workspace     >= workspace_bytes, 256-byte aligned; zero it once before its
+ *                 first use (it holds the sticky error word). Scratch between
+ *                 calls: one workspace per stream of concurrent calls.
+ *   q             [B, Hq, d]                       dtype
+ *   k_pool/v_pool [num_blocks, Hkv, 16, d]         dtype
+ *   block_tables  [B, max_blocks_per_seq]          int32 (entries past a sequence's last block are not read)
+ *   sum_k/sum_v   [seg_ptr[B], Hkv, d]             dtype, segment rows in CSR order
+ *   out           [B, Hq, d]                       float32 (written)
+ * Optional debug outputs (may be NULL), all int32:
+ *   sel_out       [B, Hkv, k_max]    selected segment indices, ascending, -1 padded
+ *   ranges_out    [B, Hkv, k_max+1, 2]  gathered token ranges [start, end), maximal
+ *                 runs in ascending order (unused entries are left unwritten)
+ *   nranges_out   [B, Hkv]           number of ranges
+ * Errors: ZR_EINVAL for a null plan or required pointer, a workspace that is not
+ * 256-byte aligned, or q/pool/summary pointers that are not 16-byte aligned;
+ * ZR_ECUDA if a launch fails.
+ */
+ZR_API zr_status zr_decode_attend(zr_plan_t plan, void* workspace, const void* q, const void* k_pool,
+                           const void* v_pool, const int32_t* block_tables, const void* sum_k,
+                           const void* sum_v, float* out, int32_t* sel_out, int32_t* ranges_out,
+                           int32_t* nranges_out, void* stream);
+
+/*
+ * zr_decode_attend_timed -- zr_decode_attend without debug outputs that also
+ * records two caller-owned CUDA events (cudaEvent_t, created with timing
+ * enabled) on `stream`: ev_start right before the gather-attention kernel and
+ * ev_stop right after it, so the caller can time that kernel alone. The events
+ * are recorded with the "external" flag, so inside a stream capture they become
+ * event-record nodes of the graph.
+ */
+ZR_API zr_status zr_decode_attend_timed(zr_plan_t plan, void* workspace, const void* q, const void* k_pool,
+                                 const void* v_pool, const int32_t* block_tables, const void* sum_k,
+                                 const void* sum_v, float* out, void* ev_start, void* ev_stop,
+                                 void* stream);
+
+/*
+ * zr_get_device_error -- synchronize `stream`, then read and clear the sticky
+ * device error word of `workspace` into *err_code (0 = none; bit 1 = a physical
+ * block id outside the pool; bit 2 = a unit needed more split slots than the
+ * plan bound). Returns ZR_EDEVICE if the word was non-zero, ZR_OK otherwise.
+ */
+ZR_API zr_status zr_get_device_error(zr_plan_t plan, void* workspace, void* stream, int32_t* err_code);
+
+/* zr_free -- release the plan and its small device metadata (NULL is a no-op). */
+ZR_API void zr_free(zr_plan_t plan);
+
+/* zr_status_string -- static, human-readable name of a status. */
+ZR_API const char* zr_status_string(zr_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ZOOMR_H */

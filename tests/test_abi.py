@@ -1,0 +1,89 @@
+"""The C-ABI library loads, exports every symbol ``include/zoomr.h`` declares,
+and rejects bad problem statements on the host (no GPU needed: validation
+happens before any CUDA call)."""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from hierarchical_sparse_kv_gb300 import build as B
+from hierarchical_sparse_kv_gb300 import zoomr as Z
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "zoomr.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return Z.load()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return re.findall(r"^ZR_API\s+[\w\s\*]+?\b(zr_\w+)\s*\(", text, flags=re.M)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_symbols()
+    assert set(names) >= {"zr_plan", "zr_decode_attend", "zr_free", "zr_get_device_error", "zr_status_string"}
+    for n in names:
+        assert hasattr(lib, n), n
+    # nothing else leaks out of the library
+    out = os.popen(f"nm -D --defined-only {B.LIB_PATH}").read().split("\n")
+    exported = sorted(l.split()[-1] for l in out if " T " in l)
+    assert exported == sorted(names)
+
+
+def test_status_strings(lib):
+    for s in range(6):
+        assert Z.zr_status_string(s).startswith("ZR_")
+    assert "unknown" in Z.zr_status_string(42)
+
+
+def _good():
+    # 2 sequences: L = 40 (segments 0,10,25,40) and L = 17 (segments 0,17)
+    cfg = Z.zr_config(2, 8, 2, 64, 16, 8, 3, 4, Z.ZR_F32)
+    return cfg, [40, 17], [0, 3, 4], [0, 10, 25, 40, 0, 17], [2, 5]
+
+
+@pytest.mark.parametrize("mutate,want", [
+    (lambda c, L, P, Bd, K: setattr(c, "batch", 0), Z.ZR_EINVAL),
+    (lambda c, L, P, Bd, K: setattr(c, "num_q_heads", 7), Z.ZR_EINVAL),       # not a multiple of Hkv
+    (lambda c, L, P, Bd, K: setattr(c, "block_size", 32), Z.ZR_EINVAL),
+    (lambda c, L, P, Bd, K: setattr(c, "window", -1), Z.ZR_EINVAL),
+    (lambda c, L, P, Bd, K: setattr(c, "dtype", 7), Z.ZR_EINVAL),
+    (lambda c, L, P, Bd, K: setattr(c, "head_dim", 96), Z.ZR_EUNSUPPORTED),
+    (lambda c, L, P, Bd, K: setattr(c, "num_q_heads", 34), Z.ZR_EUNSUPPORTED),  # group of 17
+    (lambda c, L, P, Bd, K: L.__setitem__(1, 0), Z.ZR_EINVAL),                 # empty sequence
+    (lambda c, L, P, Bd, K: L.__setitem__(0, 49), Z.ZR_EINVAL),                # longer than its table
+    (lambda c, L, P, Bd, K: K.__setitem__(0, -1), Z.ZR_EINVAL),
+    (lambda c, L, P, Bd, K: Bd.__setitem__(1, 25), Z.ZR_EINVAL),               # bounds not ascending
+    (lambda c, L, P, Bd, K: Bd.__setitem__(0, 1), Z.ZR_EINVAL),                # first bound not 0
+    (lambda c, L, P, Bd, K: Bd.__setitem__(3, 39), Z.ZR_EINVAL),               # last bound not L
+    (lambda c, L, P, Bd, K: P.__setitem__(0, 1), Z.ZR_EINVAL),
+    (lambda c, L, P, Bd, K: setattr(c, "num_blocks", 0), Z.ZR_EINVAL),
+])
+def test_plan_rejects_bad_metadata_on_the_host(lib, mutate, want):
+    cfg, L, P, Bd, K = _good()
+    mutate(cfg, L, P, Bd, K)
+    assert Z.zr_plan_status(cfg, L, P, Bd, K) == want
+
+
+def test_plan_rejects_null_arguments(lib):
+    cfg, L, P, Bd, K = _good()
+    assert Z.zr_plan_status(None, L, P, Bd, K) == Z.ZR_EINVAL
+    st = lib.zr_plan(ctypes.byref(cfg), None, None, None, None, None, None)
+    assert st == Z.ZR_EINVAL
+    assert lib.zr_decode_attend(*([None] * 13)) == Z.ZR_EINVAL
+    lib.zr_free(None)  # no-op
+
+
+def test_too_many_segments_is_unsupported(lib):
+    n = 4097
+    cfg = Z.zr_config(1, 4, 1, 64, 16, 300, 300, 0, Z.ZR_BF16)
+    assert Z.zr_plan_status(cfg, [n], [0, n], list(range(n + 1)), [1]) == Z.ZR_EUNSUPPORTED
