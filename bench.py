@@ -28,6 +28,10 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
+# The CPU oracle legs run single-threaded: cap numpy's BLAS threads before numpy loads.
+for _k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_k, "1")
+
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
@@ -148,11 +152,6 @@ def time_oracle(st, lt, budget_s: float, max_units=None):
     return done, time.perf_counter() - t0
 
 
-def oracle_threads_env():
-    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
-        os.environ.setdefault(k, "1")
-
-
 # ---------------------------------------------------------------------- distributed
 def dist_setup(n_gpus):
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -190,7 +189,6 @@ def run_reference(args):
     world, rank, local = dist_setup(args.gpus)
     if rank != 0:
         return 0
-    oracle_threads_env()
     spec = W.WORKLOADS[WORKLOAD_ID]
     st = W.make_structure(spec)
     device = "cuda" if torch.cuda.is_available() else "cpu"
@@ -273,6 +271,10 @@ def run_zoomr(args):
                 plan.run_timed(lt.q, lt.k_pool, lt.v_pool, bt, lt.sum_k, lt.sum_v, outs[l], ev_set[l][0],
                                ev_set[l][1], stream=s)
 
+    for ev_set in evs:  # torch creates CUDA events lazily: create them all before any capture
+        for a_, b_ in ev_set:
+            a_.record(stream)
+            b_.record(stream)
     stream.wait_stream(torch.cuda.current_stream())
     graphs = []
     with torch.cuda.stream(stream):
@@ -368,7 +370,6 @@ def run_zoomr(args):
         "tokens_gathered_per_step": tok_total,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        oracle_threads_env()
         n, t = time_oracle(st, lts[0], args.cpu_budget)
         units_per_step = L * st.batch * spec.num_kv_heads
         v = n / t / units_per_step
