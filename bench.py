@@ -143,7 +143,8 @@ def time_oracle(st, lt, budget_s: float, max_units=None):
     units = [(b, g) for b in range(st.batch) for g in range(st.spec.num_kv_heads)]
     done = 0
     t0 = time.perf_counter()
-    for (b, g) in units:
+    while True:  # cycle through the layer's units until the budget (or max_units) is reached
+        b, g = units[done % len(units)]
         O.decode_step(q, kp, vp, st.block_tables, st.seg_ptr, st.seg_bounds, sk, sv, st.topk, st.window,
                       units=[(b, g)])
         done += 1

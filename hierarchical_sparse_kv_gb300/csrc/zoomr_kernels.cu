@@ -24,6 +24,8 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstdio>
+#include <cstdlib>
 
 #include "zoomr_internal.h"
 
@@ -706,11 +708,25 @@ zr_status configure_for(Plan& p) {
   return ZR_OK;
 }
 
+// Inside a stream capture an event record must be "external" to become an event-record node
+// of the graph; outside a capture it is a plain record.
+cudaError_t record_event(cudaEvent_t ev, cudaStream_t s) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(s, &cs);
+  if (e != cudaSuccess) return e;
+  return cs == cudaStreamCaptureStatusActive ? cudaEventRecordWithFlags(ev, s, cudaEventRecordExternal)
+                                             : cudaEventRecord(ev, s);
+}
+
+void report(const char* what, cudaError_t e) {
+  if (std::getenv("ZOOMR_VERBOSE")) std::fprintf(stderr, "zoomr: %s: %s\n", what, cudaGetErrorString(e));
+}
+
 template <typename T, int D>
 cudaError_t launch_for(const Plan& p, const StepArgs& a, cudaStream_t s, cudaEvent_t ev0, cudaEvent_t ev1) {
   cudaError_t e = launch_pdl(zr_select_kernel<T, D>, dim3(p.Hkv, p.B), dim3(kSelectThreads), p.select_smem, s, a);
-  if (e != cudaSuccess) return e;
-  if (ev0 && (e = cudaEventRecordWithFlags(ev0, s, cudaEventRecordExternal)) != cudaSuccess) return e;
+  if (e != cudaSuccess) return report("select launch", e), e;
+  if (ev0 && (e = record_event(ev0, s)) != cudaSuccess) return report("start event record", e), e;
   const dim3 grid_attend((p.total_slots + kAttendWarps - 1) / kAttendWarps);
   bool use_mma = false;
   if constexpr (sizeof(T) == 2) use_mma = p.G <= kMmaMaxGroup;
@@ -719,10 +735,12 @@ cudaError_t launch_for(const Plan& p, const StepArgs& a, cudaStream_t s, cudaEve
   } else {
     e = launch_pdl(zr_attend_fma_kernel<T, D>, grid_attend, dim3(kAttendWarps * 32), 0, s, a);
   }
-  if (e != cudaSuccess) return e;
-  if (ev1 && (e = cudaEventRecordWithFlags(ev1, s, cudaEventRecordExternal)) != cudaSuccess) return e;
+  if (e != cudaSuccess) return report("attend launch", e), e;
+  if (ev1 && (e = record_event(ev1, s)) != cudaSuccess) return report("stop event record", e), e;
   const dim3 grid_merge((p.B * p.Hq + kAttendWarps - 1) / kAttendWarps);
-  return launch_pdl(zr_merge_kernel<D>, grid_merge, dim3(kAttendWarps * 32), 0, s, a);
+  e = launch_pdl(zr_merge_kernel<D>, grid_merge, dim3(kAttendWarps * 32), 0, s, a);
+  if (e != cudaSuccess) report("merge launch", e);
+  return e;
 }
 
 }  // namespace
