@@ -79,6 +79,12 @@ struct StepArgs {
   float scale_log2;  // log2(e) / sqrt(d)
 };
 
+// Implemented in zoomr_plan.cpp: argument checks, then one decode step on `workspace`.
+zr_status decode_into(zr_plan_t plan, void* workspace, const void* q, const void* k_pool, const void* v_pool,
+                      const int32_t* block_tables, const void* sum_k, const void* sum_v, float* out,
+                      int32_t* sel_out, int32_t* ranges_out, int32_t* nranges_out, void* stream, void* ev_start,
+                      void* ev_stop);
+
 // Implemented in zoomr_kernels.cu.
 zr_status configure_kernels(Plan& p);
 zr_status launch_step(const Plan& p, const StepArgs& a, void* stream, void* ev_start, void* ev_stop);

@@ -197,7 +197,11 @@ zr_status zr_plan_dims(zr_plan_t plan, int32_t* k_max, int32_t* n_max) {
   return ZR_OK;
 }
 
-static zr_status decode_common(zr_plan_t plan, void* workspace, const void* q, const void* k_pool, const void* v_pool,
+}  // extern "C"
+
+namespace zr {
+
+zr_status decode_into(zr_plan_t plan, void* workspace, const void* q, const void* k_pool, const void* v_pool,
                                const int32_t* block_tables, const void* sum_k, const void* sum_v, float* out,
                                int32_t* sel_out, int32_t* ranges_out, int32_t* nranges_out, void* stream,
                                void* ev_start, void* ev_stop) {
@@ -242,10 +246,14 @@ static zr_status decode_common(zr_plan_t plan, void* workspace, const void* q, c
   return zr::launch_step(p, a, stream, ev_start, ev_stop);
 }
 
+}  // namespace zr
+
+extern "C" {
+
 zr_status zr_decode_attend(zr_plan_t plan, void* workspace, const void* q, const void* k_pool, const void* v_pool,
                            const int32_t* block_tables, const void* sum_k, const void* sum_v, float* out,
                            int32_t* sel_out, int32_t* ranges_out, int32_t* nranges_out, void* stream) {
-  return decode_common(plan, workspace, q, k_pool, v_pool, block_tables, sum_k, sum_v, out, sel_out, ranges_out,
+  return zr::decode_into(plan, workspace, q, k_pool, v_pool, block_tables, sum_k, sum_v, out, sel_out, ranges_out,
                        nranges_out, stream, nullptr, nullptr);
 }
 
@@ -253,7 +261,7 @@ zr_status zr_decode_attend_timed(zr_plan_t plan, void* workspace, const void* q,
                                  const void* v_pool, const int32_t* block_tables, const void* sum_k,
                                  const void* sum_v, float* out, void* ev_start, void* ev_stop, void* stream) {
   if (!ev_start || !ev_stop) return ZR_EINVAL;
-  return decode_common(plan, workspace, q, k_pool, v_pool, block_tables, sum_k, sum_v, out, nullptr, nullptr,
+  return zr::decode_into(plan, workspace, q, k_pool, v_pool, block_tables, sum_k, sum_v, out, nullptr, nullptr,
                        nullptr, stream, ev_start, ev_stop);
 }
 

@@ -62,6 +62,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.zr_decode_attend.restype = ctypes.c_int
     lib.zr_decode_attend_timed.argtypes = [_P] * 12
     lib.zr_decode_attend_timed.restype = ctypes.c_int
+    lib.zr_decode_attend_static.argtypes = [_P] * 9
+    lib.zr_decode_attend_static.restype = ctypes.c_int
     lib.zr_get_device_error.argtypes = [_P, _P, _P, _I32P]
     lib.zr_get_device_error.restype = ctypes.c_int
     lib.zr_free.argtypes = [_P]
@@ -159,6 +161,17 @@ def zr_decode_attend_timed(plan: int, workspace: torch.Tensor, q: torch.Tensor, 
                                        ev_start.cuda_event, ev_stop.cuda_event, _stream(stream))
     if st != ZR_OK:
         raise ZoomrError(st, "zr_decode_attend_timed")
+
+
+def zr_decode_attend_static(plan: int, q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+                            block_tables: torch.Tensor, sum_k: torch.Tensor, sum_v: torch.Tensor,
+                            out: torch.Tensor, stream=None) -> None:
+    """The decode step with the library's static 16 MiB device scratch instead of a
+    caller workspace, for callers that cannot allocate device memory."""
+    st = load().zr_decode_attend_static(plan, _dev(q), _dev(k_pool), _dev(v_pool), _dev(block_tables), _dev(sum_k),
+                                        _dev(sum_v), _dev(out), _stream(stream))
+    if st != ZR_OK:
+        raise ZoomrError(st, "zr_decode_attend_static")
 
 
 def zr_get_device_error(plan: int, workspace: torch.Tensor, stream=None) -> int:

@@ -150,6 +150,33 @@ ZR_API zr_status zr_decode_attend_timed(zr_plan_t plan, void* workspace, const v
                                  void* stream);
 
 /*
+ * zr_decode_attend_static -- zr_decode_attend for callers that cannot allocate
+ * device memory. (The pages have no counterpart: this is a deployment variant.)
+ *
+ * Some callers are only handed their input and output buffers: a plugin inside
+ * a host engine that owns every device allocation and offers no scratch, or a
+ * loop that must never call cudaMalloc because it can synchronize the device.
+ * This entry point takes the same tensors as zr_decode_attend but no workspace
+ * and allocates nothing: its scratch is a 16 MiB static device array that every
+ * GPU loading this library holds until the process exits.
+ *   - The plan still comes from zr_plan (create it once, at start-up).
+ *   - The first call on a device looks up that array's device address with the
+ *     device current; make that first call before any stream capture.
+ *   - A plan whose workspace_bytes exceeds 16 MiB is rejected with
+ *     ZR_EUNSUPPORTED before anything is launched.
+ *   - All calls share the one array: calls that may overlap on the GPU (other
+ *     streams, other threads) race and corrupt each other's results; serialize
+ *     them on one stream.
+ *   - Out-of-pool block ids are masked as in zr_decode_attend, but not
+ *     reported: the error word is cleared at the start of every call.
+ * Errors: ZR_EINVAL (null plan or required pointer, misaligned pointer),
+ * ZR_EUNSUPPORTED (workspace over 16 MiB), ZR_ECUDA.
+ */
+ZR_API zr_status zr_decode_attend_static(zr_plan_t plan, const void* q, const void* k_pool, const void* v_pool,
+                                         const int32_t* block_tables, const void* sum_k, const void* sum_v,
+                                         float* out, void* stream);
+
+/*
  * zr_get_device_error -- synchronize `stream`, then read and clear the sticky
  * device error word of `workspace` into *err_code (0 = none; bit 1 = a physical
  * block id outside the pool; bit 2 = a unit needed more split slots than the

@@ -1,0 +1,70 @@
+"""The allocation-free entry point, zr_decode_attend_static.
+
+It serves callers that cannot allocate device memory: code handed only its
+input and output buffers by a host engine that owns all device allocations, or
+a loop that must not call cudaMalloc because it can synchronize the device. The
+test checks, through the C ABI, that two calls in a row give the same outputs as
+zr_decode_attend with a caller workspace, and that a plan too large for the
+16 MiB static scratch is refused before anything runs. This file is collected
+last on purpose.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+from hierarchical_sparse_kv_gb300 import build as B
+from hierarchical_sparse_kv_gb300 import workloads as W
+from hierarchical_sparse_kv_gb300 import zoomr as Z
+
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")]
+
+TOL = {"bf16": 2e-3, "f32": 1e-5}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    B.build()
+    Z.load()
+
+
+@pytest.mark.parametrize("cfg", [1, 0])
+def test_static_scratch_matches_the_workspace_entry_point_twice(cfg):
+    spec = W.WORKLOADS[cfg]
+    st = W.make_structure(spec)
+    lt = W.make_layer(st, 0, "cuda")
+    plan = Z.DecodePlan.from_structure(st)
+    assert plan.workspace_bytes <= 16 << 20
+    bt = torch.from_numpy(st.block_tables.astype(np.int32)).cuda()
+    ref = torch.full(lt.q.shape, float("nan"), dtype=torch.float32, device="cuda")
+    Z.zr_decode_attend(plan.handle, plan.ws, lt.q, lt.k_pool, lt.v_pool, bt, lt.sum_k, lt.sum_v, ref)
+    torch.cuda.synchronize()
+    assert plan.device_error() == 0
+    for _ in range(2):
+        out = torch.full(lt.q.shape, float("nan"), dtype=torch.float32, device="cuda")
+        Z.zr_decode_attend_static(plan.handle, lt.q, lt.k_pool, lt.v_pool, bt, lt.sum_k, lt.sum_v, out)
+        torch.cuda.synchronize()
+        assert torch.isfinite(out).all()
+        assert float((out - ref).abs().max()) <= TOL[spec.dtype]
+    plan.close()
+
+
+def test_plan_over_the_static_limit_is_refused():
+    # 6 sequences x 8 KV heads, every segment selected over 64K tokens: ~24 MiB of split partials
+    spec = W.small_spec(dtype="bf16", head_dim=128, batch=6, num_q_heads=32, num_kv_heads=8, seq_len=65536,
+                        seg_len_range=(512, 1024), topk=10_000, window=0)
+    st = W.make_structure(spec)
+    plan = Z.DecodePlan(batch=st.batch, num_q_heads=32, num_kv_heads=8, head_dim=128, num_blocks=st.num_blocks,
+                        max_blocks_per_seq=st.max_blocks_per_seq, window=0, dtype="bf16", seq_lens=st.seq_lens,
+                        seg_ptr=st.seg_ptr, seg_bounds=st.seg_bounds, topk=st.topk)
+    assert plan.workspace_bytes > 16 << 20
+    small = torch.zeros(64, dtype=torch.bfloat16, device="cuda")
+    bt = torch.zeros(64, dtype=torch.int32, device="cuda")
+    out = torch.zeros(64, dtype=torch.float32, device="cuda")
+    with pytest.raises(Z.ZoomrError) as e:
+        Z.zr_decode_attend_static(plan.handle, small, small, small, bt, small, small, out)
+    assert e.value.status == Z.ZR_EUNSUPPORTED
+    plan.close()
