@@ -13,7 +13,10 @@ constexpr int kMaxSegments = 4096;    // n_b limit of the select kernel's shared
 constexpr int kMaxGroup = 16;         // query heads per KV head
 constexpr int kMmaMaxGroup = 8;       // the tensor-core attend kernel packs the group into 8 MMA columns
 constexpr int kChunkRows = 256;       // gathered rows one warp reduces into one split partial
-constexpr int kAttendWarps = 4;       // warps per attend CTA
+#ifndef ZR_ATTEND_WARPS
+#define ZR_ATTEND_WARPS 4
+#endif
+constexpr int kAttendWarps = ZR_ATTEND_WARPS;  // warps per attend CTA
 constexpr int kSelectThreads = 256;   // threads per select CTA
 constexpr uint32_t kSummaryFlag = 0x80000000u;  // row id refers to the summary tensors
 constexpr uint32_t kInvalidRow = 0xFFFFFFFFu;   // masked row (past the chunk end, or a bad block id)

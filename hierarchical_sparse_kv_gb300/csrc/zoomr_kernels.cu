@@ -44,15 +44,6 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-// 16-byte streaming load that bypasses L1 (each byte is used once).
-__device__ __forceinline__ uint4 ld_stream16(const void* p) {
-  uint4 v;
-  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-      : "l"(p));
-  return v;
-}
-
 __device__ __forceinline__ float bf16_lo(uint32_t x) { return __uint_as_float(x << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t x) { return __uint_as_float(x & 0xFFFF0000u); }
 
@@ -144,16 +135,28 @@ __device__ int block_exclusive_scan(int v, int* total) {
 }
 
 // ------------------------------------------------------------------ select
-// Shared memory: q [kMaxGroup][D] f32 | keys [n_max] | flag [n_max+2] | bounds [n_max+1]
-//                | list [n_max] | runs_s [n_max] | runs_e [n_max]
+// Shared memory (32-bit words): q [kMaxGroup][D+4] f32 | staged summary keys [kKeyChunk][D+4] f32
+//   | pair values [kSelectThreads] | keys [n_max] | flag [n_max+2] | bounds [n_max+1] | list [n_max]
+//   | runs_s [n_max] | runs_e [n_max]
+// The +4 pad puts consecutive rows in different banks for the 16-byte reads of the key stage.
+constexpr int kKeyChunk = 64;
+
+template <int D>
+constexpr int select_fixed_words() {
+  return (kMaxGroup + kKeyChunk) * (D + 4) + kSelectThreads;
+}
+
 template <typename T, int D>
 __global__ void __launch_bounds__(kSelectThreads) zr_select_kernel(StepArgs a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
+  constexpr int DP = D + 4;
   const int g = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
   const int u = b * a.Hkv + g;
   const int G = a.G, nmax = a.n_max;
   float* qs = reinterpret_cast<float*>(smem_raw);
-  float* keys = qs + kMaxGroup * D;
+  float* ks = qs + kMaxGroup * DP;
+  float* pairv = ks + kKeyChunk * DP;
+  float* keys = pairv + kSelectThreads;
   int* flag = reinterpret_cast<int*>(keys + nmax);
   int* bnd = flag + nmax + 2;
   int* list = bnd + nmax + 1;
@@ -162,40 +165,72 @@ __global__ void __launch_bounds__(kSelectThreads) zr_select_kernel(StepArgs a) {
   __shared__ int s_rstar;
 
   pdl_trigger();
-  pdl_wait();
-
+  // Plan metadata is never written by a kernel: read it before waiting on the previous kernel.
   const int s0 = a.meta.seg_ptr[b];
   const int n = a.meta.seg_ptr[b + 1] - s0;
   const int L = a.meta.seq_lens[b];
   const int k = a.meta.topk[b];
-  const T* qg = static_cast<const T*>(a.q) + (static_cast<size_t>(b) * a.Hq + static_cast<size_t>(g) * G) * D;
-  for (int i = tid; i < G * D; i += blockDim.x) qs[i] = to_float(qg[i]);
   for (int i = tid; i <= n; i += blockDim.x) bnd[i] = a.meta.seg_bounds[s0 + b + i];
-  __syncthreads();
+  pdl_wait();
+
+  const T* qg = static_cast<const T*>(a.q) + (static_cast<size_t>(b) * a.Hq + static_cast<size_t>(g) * G) * D;
 
   // 1. ranking key: max over the group of the fp32 dot, products and sums rounded, ascending order.
+  //    Summary keys are staged kKeyChunk rows at a time with 16-byte loads (the first chunk together
+  //    with the queries, so both arrive in one memory round trip); then one thread runs the
+  //    sequential chain of one (segment, head) pair.
   const T* sk = static_cast<const T*>(a.sum_k);
-  for (int i = tid; i < n; i += blockDim.x) {
-    const T* row = sk + (static_cast<size_t>(s0 + i) * a.Hkv + g) * D;
-    float acc[kMaxGroup];
+  constexpr int kPer = kKeyChunk * (D / 8) / kSelectThreads;  // 16-byte pieces per thread per chunk
+  static_assert(kKeyChunk * (D / 8) % kSelectThreads == 0, "staging split");
+  for (int c0 = 0; c0 < n; c0 += kKeyChunk) {
+    const int rows = min(kKeyChunk, n - c0);
+    __syncthreads();  // the previous chunk's readers are done
+    float v[kPer][8];
+    float qv[8];
+    const bool q_here = c0 == 0 && tid < G * (D / 8);
+    if (q_here) load8<T>(qg + tid * 8, qv);
 #pragma unroll
-    for (int h = 0; h < kMaxGroup; ++h) acc[h] = 0.f;
-    for (int t0 = 0; t0 < D; t0 += 8) {
-      float sv[8];
-      load8<T>(row + t0, sv);
+    for (int j = 0; j < kPer; ++j) {
+      const int e = tid + j * kSelectThreads;
+      if (e < rows * (D / 8))
+        load8<T>(sk + (static_cast<size_t>(s0 + c0 + e / (D / 8)) * a.Hkv + g) * D + (e % (D / 8)) * 8, v[j]);
+    }
+    if (q_here) {
+      float4* dst = reinterpret_cast<float4*>(qs + (tid / (D / 8)) * DP + (tid % (D / 8)) * 8);
+      dst[0] = make_float4(qv[0], qv[1], qv[2], qv[3]);
+      dst[1] = make_float4(qv[4], qv[5], qv[6], qv[7]);
+    }
 #pragma unroll
-      for (int h = 0; h < kMaxGroup; ++h) {
-        if (h < G) {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) acc[h] = __fadd_rn(acc[h], __fmul_rn(qs[h * D + t0 + e], sv[e]));
-        }
+    for (int j = 0; j < kPer; ++j) {
+      const int e = tid + j * kSelectThreads;
+      if (e < rows * (D / 8)) {
+        float4* dst = reinterpret_cast<float4*>(ks + (e / (D / 8)) * DP + (e % (D / 8)) * 8);
+        dst[0] = make_float4(v[j][0], v[j][1], v[j][2], v[j][3]);
+        dst[1] = make_float4(v[j][4], v[j][5], v[j][6], v[j][7]);
       }
     }
-    float key = acc[0];
-#pragma unroll
-    for (int h = 1; h < kMaxGroup; ++h)
-      if (h < G) key = fmaxf(key, acc[h]);
-    keys[i] = key;
+    __syncthreads();
+    for (int pi = tid; pi < rows * G; pi += blockDim.x) {
+      const int i = pi / G, h = pi - i * G;
+      const float4* sr = reinterpret_cast<const float4*>(ks + i * DP);
+      const float4* qr = reinterpret_cast<const float4*>(qs + h * DP);
+      float acc = 0.f;
+#pragma unroll 8
+      for (int t4 = 0; t4 < D / 4; ++t4) {
+        const float4 x = sr[t4], y = qr[t4];
+        acc = __fadd_rn(acc, __fmul_rn(y.x, x.x));
+        acc = __fadd_rn(acc, __fmul_rn(y.y, x.y));
+        acc = __fadd_rn(acc, __fmul_rn(y.z, x.z));
+        acc = __fadd_rn(acc, __fmul_rn(y.w, x.w));
+      }
+      pairv[pi] = acc;
+    }
+    __syncthreads();
+    for (int i = tid; i < rows; i += blockDim.x) {
+      float key = pairv[i * G];
+      for (int h = 1; h < G; ++h) key = fmaxf(key, pairv[i * G + h]);
+      keys[c0 + i] = key;
+    }
   }
   __syncthreads();
 
@@ -378,89 +413,122 @@ __device__ __forceinline__ const T* row_ptr(uint32_t id, const T* pool, const T*
 
 // ------------------------------------------------------------------ attend: tensor cores (bf16, G <= 8)
 //
-// Per 16-row tile, with r = lane / 4 and c = lane % 4:
-//   S = Q K^T  as m16n8k16 with M = query heads (G valid of 16), N = 8 tokens (two tiles),
-//              K = d. Thread (r, c) feeds K rows r and r+8 (B operand), reading the d
-//              components 32q + 8c .. +7 with one 16-byte load per q; Q's A fragments use
-//              the same d order (a permutation of the contraction index).
-//   P          thread (r, c) then holds S[head r][tokens 2c, 2c+1, 2c+8, 2c+9], which is
-//              exactly the B fragment of P^T for the next product: no data movement.
-//              P is split into bf16 hi + lo parts (two MMAs) so it keeps ~16 bits.
-//   O^T += V^T P^T  with M = d (D/16 tiles), N = heads, K = 16 tokens. Thread (r, c) loads
-//              V rows 2c, 2c+1, 2c+8, 2c+9 at d = r*D/8 .. +D/8-1 and pairs tokens with
-//              byte permutes; M row r of tile i is d = r*D/8 + 2i, row r+8 is d + 1.
-template <int D>
-struct MmaTile {
-  uint32_t k[2][D / 32][4];  // K rows r, r+8
-  uint32_t v[4][D / 16];     // V rows 2c, 2c+1, 2c+8, 2c+9
-  uint32_t vmask;            // bit j: V row j of this thread is a real row
-};
+// A warp owns one split (up to kChunkRows gathered rows of one unit) and walks it in 16-row
+// tiles through a ring of kStages shared-memory stages filled by cp.async:
+//   staging   each warp-wide cp.async moves whole rows (D/8 consecutive lanes per row), so
+//             every request reads full 128-byte lines; rows sit row-major with a 16-byte pad,
+//             which makes every ldmatrix below conflict-free. Masked rows use the zero-fill
+//             form (source size 0) and read nothing.
+//   S = Q K^T  mma.sync m16n8k16 bf16 with M = query heads (G valid of 16), N = 8 tokens
+//             (two n-tiles), K = d; K^T's B fragments come from ldmatrix.x4.
+//   P         thread (r = lane/4, c = lane%4) holds S[head r][tokens 2c, 2c+1, 2c+8, 2c+9],
+//             which is exactly the B fragment of P^T for the next product. P is split into
+//             bf16 hi + lo parts (two MMAs) so it keeps ~16 bits.
+//   O^T += V^T P^T  with M = d (D/16 m-tiles), N = heads, K = 16 tokens; V^T's A fragments
+//             come from ldmatrix.x4.trans of the V rows.
+// The online softmax runs in log2 units (scale log2(e)/sqrt(d)); O is rescaled only when some
+// head's running maximum moved in this tile.
+#ifndef ZR_ATTEND_STAGES
+#define ZR_ATTEND_STAGES 2
+#endif
+constexpr int kStages = ZR_ATTEND_STAGES;  // 2: one tile in flight while one is computed, 3 CTAs / SM
 
 template <int D>
-__device__ __forceinline__ void mma_load_tile(MmaTile<D>& t, const uint32_t* tab, int t0, int r, int c,
-                                              const __nv_bfloat16* kp, const __nv_bfloat16* vp,
-                                              const __nv_bfloat16* skp, const __nv_bfloat16* svp) {
+__host__ __device__ constexpr int ring_row_bytes() {
+  return D * 2 + 16;
+}
+template <int D>
+constexpr size_t attend_ring_bytes() {
+  return static_cast<size_t>(kAttendWarps) * kStages * 32 * ring_row_bytes<D>();
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t smem_dst, const void* gsrc, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_dst), "l"(gsrc), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr)
+               : "memory");
+}
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr)
+               : "memory");
+}
+
+// Per-lane source bases: the K/V pools and summary tensors, offset by this lane's 16-byte chunk.
+struct LoadBases {
+  const char* kp;
+  const char* vp;
+  const char* sk;
+  const char* sv;
+};
+
+// Stage the 16 K rows and 16 V rows of tile t0. Every cp.async instruction moves whole rows
+// (D/8 consecutive lanes per row, 16 bytes each), so each warp-wide copy reads full 128-byte
+// lines: one row id serves both the K and the V copy of a row.
+template <int D>
+__device__ __forceinline__ void mma_issue_tile(uint32_t stage, const uint32_t* tab, int t0, int lane,
+                                               const LoadBases& lb) {
+  constexpr int RB = ring_row_bytes<D>();
+  constexpr int CPR = D / 8;     // 16-byte chunks per row
+  constexpr int RPI = 32 / CPR;  // rows per warp instruction
+  const int sub = lane / CPR, ch = lane % CPR;
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const uint32_t id = tab[t0 + r + 8 * h];
-    if (id != kInvalidRow) {
-      const __nv_bfloat16* p = row_ptr<__nv_bfloat16, D>(id, kp, skp) + 8 * c;
-#pragma unroll
-      for (int q = 0; q < D / 32; ++q) {
-        const uint4 w = ld_stream16(p + 32 * q);
-        t.k[h][q][0] = w.x; t.k[h][q][1] = w.y; t.k[h][q][2] = w.z; t.k[h][q][3] = w.w;
-      }
-    } else {
-#pragma unroll
-      for (int q = 0; q < D / 32; ++q) t.k[h][q][0] = t.k[h][q][1] = t.k[h][q][2] = t.k[h][q][3] = 0u;
-    }
-  }
-  t.vmask = 0;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int row = 2 * c + (j & 1) + 8 * (j >> 1);
+  for (int j = 0; j < 16 / RPI; ++j) {
+    const int row = RPI * j + sub;
     const uint32_t id = tab[t0 + row];
-    if (id != kInvalidRow) {
-      t.vmask |= 1u << j;
-      const __nv_bfloat16* p = row_ptr<__nv_bfloat16, D>(id, vp, svp) + (D / 8) * r;
-#pragma unroll
-      for (int q = 0; q < D / 64; ++q) {
-        const uint4 w = ld_stream16(p + 8 * q);
-        t.v[j][4 * q + 0] = w.x; t.v[j][4 * q + 1] = w.y; t.v[j][4 * q + 2] = w.z; t.v[j][4 * q + 3] = w.w;
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < D / 16; ++i) t.v[j][i] = 0u;
-    }
+    const bool ok = id != kInvalidRow;
+    const bool is_sum = (id & kSummaryFlag) != 0;
+    const size_t off = static_cast<size_t>(ok ? (id & ~kSummaryFlag) : 0u) * (D * 2);
+    const uint32_t bytes = ok ? 16u : 0u;
+    const uint32_t dst = stage + row * RB + ch * 16;
+    cp_async16(dst, (is_sum ? lb.sk : lb.kp) + off, bytes);
+    cp_async16(dst + 16 * RB, (is_sum ? lb.sv : lb.vp) + off, bytes);
   }
 }
 
 template <int D>
 struct MmaState {
-  uint32_t qa0[D / 16], qa2[D / 16];  // Q A-fragments (rows r < G), rows r+8 are zero
+  uint32_t qa0[D / 16], qa2[D / 16];  // Q A-fragments (rows r < G); rows r+8 are zero
   float o[D / 16][4];                  // O^T accumulators
   float m;                             // running max (log2 units) of head r
   float l;                             // this thread's part of head r's running sum
 };
 
 template <int D>
-__device__ __forceinline__ void mma_compute_tile(MmaState<D>& st, const MmaTile<D>& t, float scale_log2, int c) {
+__device__ __forceinline__ void mma_compute_tile(MmaState<D>& st, uint32_t stage, uint32_t vmask16, float scale_log2,
+                                                 int lane) {
+  constexpr int RB = ring_row_bytes<D>();
+  const int c = lane & 3;
+  const int mi = lane >> 3, mr = lane & 7;  // ldmatrix: this lane addresses row mr of matrix mi
+  const uint32_t krow = stage + (8 * (mi >> 1) + mr) * RB + 16 * (mi & 1);
+  const uint32_t vrow = krow + 16 * RB;
   float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int s = 0; s < D / 16; ++s) {
-    const int q = s >> 1, hh = (s & 1) * 2;
-    mma_bf16(s0, st.qa0[s], 0u, st.qa2[s], 0u, t.k[0][q][hh], t.k[0][q][hh + 1]);
-    mma_bf16(s1, st.qa0[s], 0u, st.qa2[s], 0u, t.k[1][q][hh], t.k[1][q][hh + 1]);
+    uint32_t b00, b01, b10, b11;
+    ldsm_x4(krow + 32 * s, b00, b01, b10, b11);
+    mma_bf16(s0, st.qa0[s], 0u, st.qa2[s], 0u, b00, b01);
+    mma_bf16(s1, st.qa0[s], 0u, st.qa2[s], 0u, b10, b11);
   }
   const float ninf = -INFINITY;
-  const float x0 = (t.vmask & 1u) ? s0[0] * scale_log2 : ninf;
-  const float x1 = (t.vmask & 2u) ? s0[1] * scale_log2 : ninf;
-  const float x2 = (t.vmask & 4u) ? s1[0] * scale_log2 : ninf;
-  const float x3 = (t.vmask & 8u) ? s1[1] * scale_log2 : ninf;
+  const float x0 = (vmask16 >> (2 * c)) & 1u ? s0[0] * scale_log2 : ninf;
+  const float x1 = (vmask16 >> (2 * c + 1)) & 1u ? s0[1] * scale_log2 : ninf;
+  const float x2 = (vmask16 >> (2 * c + 8)) & 1u ? s1[0] * scale_log2 : ninf;
+  const float x3 = (vmask16 >> (2 * c + 9)) & 1u ? s1[1] * scale_log2 : ninf;
   float mt = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
   mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 1));
   mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 2));
   const float m_new = fmaxf(st.m, mt);
+  const bool moved = m_new != st.m;
   const float alpha = fast_exp2(st.m - m_new);
   const float p0 = fast_exp2(x0 - m_new), p1 = fast_exp2(x1 - m_new);
   const float p2 = fast_exp2(x2 - m_new), p3 = fast_exp2(x3 - m_new);
@@ -469,19 +537,22 @@ __device__ __forceinline__ void mma_compute_tile(MmaState<D>& st, const MmaTile<
   const uint32_t bh0 = pack_bf16(p0, p1), bh1 = pack_bf16(p2, p3);
   const uint32_t bl0 = pack_bf16(p0 - bf16_lo(bh0), p1 - bf16_hi(bh0));
   const uint32_t bl1 = pack_bf16(p2 - bf16_lo(bh1), p3 - bf16_hi(bh1));
-  // O^T columns of this thread are heads 2c and 2c+1, whose alphas live in lanes 8c and 8c+4.
-  const float a_e = __shfl_sync(kFull, alpha, 8 * c);
-  const float a_o = __shfl_sync(kFull, alpha, 8 * c + 4);
+  if (__any_sync(kFull, moved)) {
+    // O^T columns of this thread are heads 2c and 2c+1, whose alphas live in lanes 8c and 8c+4.
+    const float a_e = __shfl_sync(kFull, alpha, 8 * c);
+    const float a_o = __shfl_sync(kFull, alpha, 8 * c + 4);
+#pragma unroll
+    for (int i = 0; i < D / 16; ++i) {
+      st.o[i][0] *= a_e;
+      st.o[i][1] *= a_o;
+      st.o[i][2] *= a_e;
+      st.o[i][3] *= a_o;
+    }
+  }
 #pragma unroll
   for (int i = 0; i < D / 16; ++i) {
-    st.o[i][0] *= a_e;
-    st.o[i][1] *= a_o;
-    st.o[i][2] *= a_e;
-    st.o[i][3] *= a_o;
-    const uint32_t a0 = __byte_perm(t.v[0][i], t.v[1][i], 0x5410);
-    const uint32_t a1 = __byte_perm(t.v[0][i], t.v[1][i], 0x7632);
-    const uint32_t a2 = __byte_perm(t.v[2][i], t.v[3][i], 0x5410);
-    const uint32_t a3 = __byte_perm(t.v[2][i], t.v[3][i], 0x7632);
+    uint32_t a0, a1, a2, a3;
+    ldsm_x4_trans(vrow + 32 * i, a0, a1, a2, a3);
     mma_bf16(st.o[i], a0, a1, a2, a3, bh0, bh1);
     mma_bf16(st.o[i], a0, a1, a2, a3, bl0, bl1);
   }
@@ -489,6 +560,9 @@ __device__ __forceinline__ void mma_compute_tile(MmaState<D>& st, const MmaTile<
 
 template <int D>
 __global__ void __launch_bounds__(kAttendWarps * 32) zr_attend_mma_kernel(StepArgs a) {
+  constexpr int RB = ring_row_bytes<D>();
+  constexpr uint32_t kStageBytes = 32 * RB;
+  extern __shared__ __align__(16) unsigned char attend_smem[];
   __shared__ uint32_t rowtab[kAttendWarps][kChunkRows];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int slot = blockIdx.x * kAttendWarps + warp;
@@ -511,10 +585,9 @@ __global__ void __launch_bounds__(kAttendWarps * 32) zr_attend_mma_kernel(StepAr
       static_cast<const __nv_bfloat16*>(a.q) + (static_cast<size_t>(s.b) * a.Hq + static_cast<size_t>(s.g) * G) * D;
 #pragma unroll
   for (int k = 0; k < D / 16; ++k) {
-    const int d0 = 32 * (k >> 1) + 8 * c + 4 * (k & 1);
     if (r < G) {
-      st.qa0[k] = *reinterpret_cast<const uint32_t*>(qg + r * D + d0);
-      st.qa2[k] = *reinterpret_cast<const uint32_t*>(qg + r * D + d0 + 2);
+      st.qa0[k] = *reinterpret_cast<const uint32_t*>(qg + r * D + 16 * k + 2 * c);
+      st.qa2[k] = *reinterpret_cast<const uint32_t*>(qg + r * D + 16 * k + 2 * c + 8);
     } else {
       st.qa0[k] = 0u;
       st.qa2[k] = 0u;
@@ -525,22 +598,25 @@ __global__ void __launch_bounds__(kAttendWarps * 32) zr_attend_mma_kernel(StepAr
   st.m = -1e30f;
   st.l = 0.f;
 
-  const __nv_bfloat16* kp = static_cast<const __nv_bfloat16*>(a.k_pool);
-  const __nv_bfloat16* vp = static_cast<const __nv_bfloat16*>(a.v_pool);
-  const __nv_bfloat16* skp = static_cast<const __nv_bfloat16*>(a.sum_k);
-  const __nv_bfloat16* svp = static_cast<const __nv_bfloat16*>(a.sum_v);
-  MmaTile<D> ta, tb;
-  mma_load_tile<D>(ta, tab, 0, r, c, kp, vp, skp, svp);
-  int t0 = 0;
-  while (true) {
-    if (t0 + 16 < nrows) mma_load_tile<D>(tb, tab, t0 + 16, r, c, kp, vp, skp, svp);
-    mma_compute_tile<D>(st, ta, a.scale_log2, c);
-    t0 += 16;
-    if (t0 >= nrows) break;
-    if (t0 + 16 < nrows) mma_load_tile<D>(ta, tab, t0 + 16, r, c, kp, vp, skp, svp);
-    mma_compute_tile<D>(st, tb, a.scale_log2, c);
-    t0 += 16;
-    if (t0 >= nrows) break;
+  const int chunk_off = (lane % (D / 8)) * 16;
+  const LoadBases lb{static_cast<const char*>(a.k_pool) + chunk_off, static_cast<const char*>(a.v_pool) + chunk_off,
+                     static_cast<const char*>(a.sum_k) + chunk_off, static_cast<const char*>(a.sum_v) + chunk_off};
+  const uint32_t ring = static_cast<uint32_t>(__cvta_generic_to_shared(attend_smem)) + warp * kStages * kStageBytes;
+  const int ntiles = (nrows + 15) >> 4;
+#pragma unroll
+  for (int i = 0; i < kStages - 1; ++i) {
+    if (i < ntiles) mma_issue_tile<D>(ring + i * kStageBytes, tab, 16 * i, lane, lb);
+    cp_async_commit();
+  }
+  for (int i = 0; i < ntiles; ++i) {
+    const int nx = i + kStages - 1;
+    __syncwarp();  // every lane is done reading the stage that is refilled next
+    if (nx < ntiles) mma_issue_tile<D>(ring + (nx % kStages) * kStageBytes, tab, 16 * nx, lane, lb);
+    cp_async_commit();
+    cp_async_wait<kStages - 1>();
+    __syncwarp();  // tile i's rows, staged by all lanes, are visible to every lane
+    const uint32_t vmask16 = __ballot_sync(kFull, lane < 16 && tab[16 * i + lane] != kInvalidRow) & 0xFFFFu;
+    mma_compute_tile<D>(st, ring + (i % kStages) * kStageBytes, vmask16, a.scale_log2, lane);
   }
 
   // head r's sum: add the parts of the four lanes that share r.
@@ -552,11 +628,11 @@ __global__ void __launch_bounds__(kAttendWarps * 32) zr_attend_mma_kernel(StepAr
   for (int e = 0; e < 2; ++e) {
     const int h = 2 * c + e;
     if (h < G) {
-      float* dst = a.part_o + (static_cast<size_t>(slot) * G + h) * D + (D / 8) * r;
+      float* dst = a.part_o + (static_cast<size_t>(slot) * G + h) * D + r;
 #pragma unroll
-      for (int i = 0; i < D / 16; i += 2) {
-        const float4 v = make_float4(st.o[i][e], st.o[i][e + 2], st.o[i + 1][e], st.o[i + 1][e + 2]);
-        *reinterpret_cast<float4*>(dst + 2 * i) = v;
+      for (int i = 0; i < D / 16; ++i) {
+        dst[16 * i] = st.o[i][e];
+        dst[16 * i + 8] = st.o[i][e + 2];
       }
     }
   }
@@ -638,6 +714,8 @@ __global__ void __launch_bounds__(kAttendWarps * 32) zr_attend_fma_kernel(StepAr
 }
 
 // ------------------------------------------------------------------ merge
+// Lanes first own chunks (max, weights, weighted sums of l), then own d components while
+// the chunk loop is unrolled so that several partial rows are in flight at once.
 template <int D>
 __global__ void __launch_bounds__(kAttendWarps * 32) zr_merge_kernel(StepArgs a) {
   constexpr int E = D / 32;
@@ -651,24 +729,35 @@ __global__ void __launch_bounds__(kAttendWarps * 32) zr_merge_kernel(StepArgs a)
   const int base = a.meta.slot_base[b] + g * a.meta.slots[b];
   pdl_wait();
   const int nch = a.unit_info[u].w;
+  const float2* ml = a.part_ml + static_cast<size_t>(base) * G + hh;
   float M = -INFINITY;
-  for (int c = lane; c < nch; c += 32) M = fmaxf(M, a.part_ml[static_cast<size_t>(base + c) * G + hh].x);
+  for (int c = lane; c < nch; c += 32) M = fmaxf(M, ml[static_cast<size_t>(c) * G].x);
 #pragma unroll
   for (int o2 = 16; o2 > 0; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o2));
   float acc[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
   float Ls = 0.f;
-  for (int c = 0; c < nch; ++c) {
-    const float2 ml = a.part_ml[static_cast<size_t>(base + c) * G + hh];
-    const float wgt = fast_exp2(ml.x - M);
-    Ls = fmaf(ml.y, wgt, Ls);
-    const float* src = a.part_o + (static_cast<size_t>(base + c) * G + hh) * D + lane * E;
-    float v[E];
-    load_e<float, E>(src, v);
+  const float* po = a.part_o + (static_cast<size_t>(base) * G + hh) * D + lane * E;
+  for (int c0 = 0; c0 < nch; c0 += 32) {
+    float wgt = 0.f;
+    if (c0 + lane < nch) {
+      const float2 v = ml[static_cast<size_t>(c0 + lane) * G];
+      wgt = fast_exp2(v.x - M);
+      Ls = fmaf(v.y, wgt, Ls);
+    }
+    const int cnt = min(32, nch - c0);
+#pragma unroll 8
+    for (int j = 0; j < cnt; ++j) {
+      const float wj = __shfl_sync(kFull, wgt, j);
+      float v[E];
+      load_e<float, E>(po + static_cast<size_t>(c0 + j) * G * D, v);
 #pragma unroll
-    for (int e = 0; e < E; ++e) acc[e] = fmaf(wgt, v[e], acc[e]);
+      for (int e = 0; e < E; ++e) acc[e] = fmaf(wj, v[e], acc[e]);
+    }
   }
+#pragma unroll
+  for (int o2 = 16; o2 > 0; o2 >>= 1) Ls += __shfl_xor_sync(kFull, Ls, o2);
   const float inv = 1.f / Ls;
   float* dst = a.out + (static_cast<size_t>(b) * a.Hq + h) * D + lane * E;
 #pragma unroll
@@ -692,11 +781,19 @@ cudaError_t launch_pdl(Kern kernel, dim3 grid, dim3 block, size_t smem, cudaStre
 }
 
 size_t select_smem_bytes(int d, int n_max) {
-  return static_cast<size_t>(kMaxGroup) * d * 4 + static_cast<size_t>(n_max) * 4 * 6 + 16;
+  const size_t fixed = d == 64 ? select_fixed_words<64>() : select_fixed_words<128>();
+  return (fixed + static_cast<size_t>(n_max) * 6 + 3) * 4;
 }
 
 template <typename T, int D>
 zr_status configure_for(Plan& p) {
+  if constexpr (sizeof(T) == 2) {
+    if (cudaFuncSetAttribute(zr_attend_mma_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(attend_ring_bytes<D>())) != cudaSuccess) {
+      cudaGetLastError();
+      return ZR_ECUDA;
+    }
+  }
   p.select_smem = select_smem_bytes(D, p.n_max);
   if (p.select_smem > 48 * 1024) {
     if (cudaFuncSetAttribute(zr_select_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -731,7 +828,8 @@ cudaError_t launch_for(const Plan& p, const StepArgs& a, cudaStream_t s, cudaEve
   bool use_mma = false;
   if constexpr (sizeof(T) == 2) use_mma = p.G <= kMmaMaxGroup;
   if (use_mma) {
-    if constexpr (sizeof(T) == 2) e = launch_pdl(zr_attend_mma_kernel<D>, grid_attend, dim3(kAttendWarps * 32), 0, s, a);
+    if constexpr (sizeof(T) == 2)
+      e = launch_pdl(zr_attend_mma_kernel<D>, grid_attend, dim3(kAttendWarps * 32), attend_ring_bytes<D>(), s, a);
   } else {
     e = launch_pdl(zr_attend_fma_kernel<T, D>, grid_attend, dim3(kAttendWarps * 32), 0, s, a);
   }
