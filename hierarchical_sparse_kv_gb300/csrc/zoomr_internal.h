@@ -12,7 +12,7 @@ constexpr int kBlockTokens = 16;      // tokens per paged KV block
 constexpr int kMaxSegments = 4096;    // n_b limit of the select kernel's shared memory
 constexpr int kMaxGroup = 16;         // query heads per KV head
 constexpr int kMmaMaxGroup = 8;       // the tensor-core attend kernel packs the group into 8 MMA columns
-constexpr int kChunkRows = 256;       // gathered rows one warp reduces into one split partial
+constexpr int kChunkRows = 256;       // rows of one attend warp's row table (a range is walked in such pieces)
 #ifndef ZR_ATTEND_WARPS
 #define ZR_ATTEND_WARPS 4
 #endif
@@ -21,7 +21,7 @@ constexpr int kSelectThreads = 256;   // threads per select CTA
 constexpr uint32_t kSummaryFlag = 0x80000000u;  // row id refers to the summary tensors
 constexpr uint32_t kInvalidRow = 0xFFFFFFFFu;   // masked row (past the chunk end, or a bad block id)
 
-enum : int32_t { kErrBadBlock = 1, kErrSlots = 2 };
+enum : int32_t { kErrBadBlock = 1 };
 
 // Small device metadata copied from the host at plan time (one allocation).
 struct DeviceMeta {
@@ -29,32 +29,34 @@ struct DeviceMeta {
   int32_t* seg_ptr;     // [B+1]
   int32_t* seg_bounds;  // [total_segments + B]
   int32_t* topk;        // [B], already clipped to n_b
-  int32_t* slot_base;   // [B+1] first split slot of sequence b
-  int32_t* slots;       // [B] split slots of each unit of sequence b
 };
 
 // Byte offsets into the caller's workspace.
 struct WsLayout {
-  size_t err;        // int32 sticky error word
-  size_t unit_info;  // int32 [U][4]: n_ranges, n_tok, n_sum, n_chunks
-  size_t ranges;     // int32 [U][k_max+1][2]
-  size_t cum;        // int32 [U][k_max+2] prefix sums of range lengths
-  size_t sumlist;    // int32 [U][n_max] non-selected segments, ascending
-  size_t sel;        // int32 [U][k_max] selected segments, ascending
-  size_t part_o;     // float [total_slots][G][d] unnormalised split outputs
-  size_t part_ml;    // float [total_slots][G][2] split (max, sum) in log2 units
+  size_t err;         // int32 sticky error word
+  size_t unit_info;   // int32 [U][4]: n_ranges, n_tok, n_sum, 0
+  size_t ranges;      // int32 [U][k_max+1][2]
+  size_t cum;         // int32 [U][k_max+2] prefix sums of range lengths
+  size_t sumlist;     // int32 [U][n_max] non-selected segments, ascending
+  size_t sel;         // int32 [U][k_max] selected segments, ascending
+  size_t merge_info;  // int32 [U][2]: first attend warp of the unit, number of its warps
+  size_t part_o;      // float [U + attend_warps][G][d] unnormalised split outputs
+  size_t part_ml;     // float [U + attend_warps][G][2] split (max, sum) in log2 units
   size_t total;
 };
 
 struct Plan {
   zr_config cfg;
   int B, Hq, Hkv, G, d, window, num_blocks, max_blocks;
-  int k_max, n_max, total_segments, total_slots, chunk_rows;
+  int k_max, n_max, total_segments;
+  int attend_ctas;   // persistent attend grid (one resident wave)
+  int attend_warps;  // attend_ctas * kAttendWarps
   int device;
   void* d_meta_base;
   DeviceMeta meta;
   WsLayout ws;
   size_t select_smem;  // dynamic shared memory of the select kernel
+  size_t attend_smem;  // dynamic shared memory of the attend kernel
 };
 
 // Everything one launch needs, passed by value.
@@ -76,9 +78,10 @@ struct StepArgs {
   int32_t* cum;
   int32_t* sumlist;
   int32_t* sel;
+  int2* merge_info;
   float* part_o;
   float2* part_ml;
-  int B, Hq, Hkv, G, window, num_blocks, max_blocks, k_max, n_max, total_slots, chunk_rows;
+  int B, Hq, Hkv, G, window, num_blocks, max_blocks, k_max, n_max, attend_warps;
   float scale_log2;  // log2(e) / sqrt(d)
 };
 
@@ -89,7 +92,9 @@ zr_status decode_into(zr_plan_t plan, void* workspace, const void* q, const void
                       void* ev_stop);
 
 // Implemented in zoomr_kernels.cu.
-zr_status configure_kernels(Plan& p);
+// Sets kernel attributes and sizes the persistent attend grid (p.attend_ctas, p.attend_warps)
+// for at most `useful_warps` warps.
+zr_status configure_kernels(Plan& p, int64_t useful_warps);
 zr_status launch_step(const Plan& p, const StepArgs& a, void* stream, void* ev_start, void* ev_stop);
 
 }  // namespace zr

@@ -23,6 +23,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 #include <cstdio>
 #include <cstdlib>
@@ -106,6 +107,15 @@ __device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+__device__ __forceinline__ int warp_incl_scan(int x, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(kFull, x, o);
+    if (lane >= o) x += y;
+  }
+  return x;
+}
+
 // Exclusive prefix sum of one int per thread over the CTA; *total receives the sum.
 __device__ int block_exclusive_scan(int v, int* total) {
   __shared__ int wsum[32];
@@ -135,29 +145,33 @@ __device__ int block_exclusive_scan(int v, int* total) {
 }
 
 // ------------------------------------------------------------------ select
-// Shared memory (32-bit words): q [kMaxGroup][D+4] f32 | staged summary keys [kKeyChunk][D+4] f32
-//   | pair values [kSelectThreads] | keys [n_max] | flag [n_max+2] | bounds [n_max+1] | list [n_max]
-//   | runs_s [n_max] | runs_e [n_max]
-// The +4 pad puts consecutive rows in different banks for the 16-byte reads of the key stage.
-constexpr int kKeyChunk = 64;
-
-template <int D>
-constexpr int select_fixed_words() {
-  return (kMaxGroup + kKeyChunk) * (D + 4) + kSelectThreads;
-}
+// Shared memory: q [kMaxGroup][D+4] f32 | staged summary-key rows, raw, kStageRows x (D*sizeof(T)+16)
+//   | pair values [kStageRows][kMaxGroup] | keys [n_max+4] | flag [n_max+2] | bounds [n_max+1] | list [n_max] | runs_s [n_max] | runs_e [n_max]
+// The 16-byte row pad keeps the threads' row reads in different banks.
+template <typename T, int D>
+struct SelectLayout {
+  static constexpr int DP = D + 4;
+  static constexpr int kRowBytes = D * static_cast<int>(sizeof(T)) + 16;
+  static constexpr int kStageRows = D * sizeof(T) >= 512 ? 128 : 256;
+  static constexpr int kPieces = D * static_cast<int>(sizeof(T)) / 16;  // 16-byte pieces per row
+  static constexpr size_t kPairBytes = static_cast<size_t>(kStageRows) * kMaxGroup * 4;
+  static constexpr size_t kFixedBytes =
+      static_cast<size_t>(kMaxGroup) * DP * 4 + static_cast<size_t>(kStageRows) * kRowBytes + kPairBytes;
+};
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kSelectThreads) zr_select_kernel(StepArgs a) {
+  using LY = SelectLayout<T, D>;
+  constexpr int DP = LY::DP;
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  constexpr int DP = D + 4;
   const int g = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
   const int u = b * a.Hkv + g;
   const int G = a.G, nmax = a.n_max;
   float* qs = reinterpret_cast<float*>(smem_raw);
-  float* ks = qs + kMaxGroup * DP;
-  float* pairv = ks + kKeyChunk * DP;
-  float* keys = pairv + kSelectThreads;
-  int* flag = reinterpret_cast<int*>(keys + nmax);
+  unsigned char* stage = smem_raw + static_cast<size_t>(kMaxGroup) * DP * 4;
+  float* pairv = reinterpret_cast<float*>(stage + static_cast<size_t>(LY::kStageRows) * LY::kRowBytes);
+  float* keys = reinterpret_cast<float*>(smem_raw + LY::kFixedBytes);
+  int* flag = reinterpret_cast<int*>(keys + nmax + 4);
   int* bnd = flag + nmax + 2;
   int* list = bnd + nmax + 1;
   int* runs_s = list + nmax;
@@ -176,24 +190,26 @@ __global__ void __launch_bounds__(kSelectThreads) zr_select_kernel(StepArgs a) {
   const T* qg = static_cast<const T*>(a.q) + (static_cast<size_t>(b) * a.Hq + static_cast<size_t>(g) * G) * D;
 
   // 1. ranking key: max over the group of the fp32 dot, products and sums rounded, ascending order.
-  //    Summary keys are staged kKeyChunk rows at a time with 16-byte loads (the first chunk together
-  //    with the queries, so both arrive in one memory round trip); then one thread runs the
-  //    sequential chain of one (segment, head) pair.
-  const T* sk = static_cast<const T*>(a.sum_k);
-  constexpr int kPer = kKeyChunk * (D / 8) / kSelectThreads;  // 16-byte pieces per thread per chunk
-  static_assert(kKeyChunk * (D / 8) % kSelectThreads == 0, "staging split");
-  for (int c0 = 0; c0 < n; c0 += kKeyChunk) {
-    const int rows = min(kKeyChunk, n - c0);
-    __syncthreads();  // the previous chunk's readers are done
-    float v[kPer][8];
+  //    Up to kStageRows summary-key rows are staged raw in one memory round trip (the first batch
+  //    together with the queries); then every (segment, head) pair runs its own sequential chain.
+  const char* sk = static_cast<const char*>(a.sum_k);
+  constexpr int PER = LY::kStageRows * LY::kPieces / kSelectThreads;
+  static_assert(LY::kStageRows * LY::kPieces % kSelectThreads == 0, "staging split");
+  constexpr int EPP = 16 / static_cast<int>(sizeof(T));  // elements per 16-byte piece
+  for (int c0 = 0; c0 < n; c0 += LY::kStageRows) {
+    const int rows = min(LY::kStageRows, n - c0);
+    __syncthreads();  // the previous batch's readers are done
+    uint4 v[PER];
     float qv[8];
     const bool q_here = c0 == 0 && tid < G * (D / 8);
     if (q_here) load8<T>(qg + tid * 8, qv);
 #pragma unroll
-    for (int j = 0; j < kPer; ++j) {
+    for (int j = 0; j < PER; ++j) {
       const int e = tid + j * kSelectThreads;
-      if (e < rows * (D / 8))
-        load8<T>(sk + (static_cast<size_t>(s0 + c0 + e / (D / 8)) * a.Hkv + g) * D + (e % (D / 8)) * 8, v[j]);
+      if (e < rows * LY::kPieces)
+        v[j] = *reinterpret_cast<const uint4*>(
+            sk + ((static_cast<size_t>(s0 + c0 + e / LY::kPieces) * a.Hkv + g) * D) * sizeof(T) +
+            (e % LY::kPieces) * 16);
     }
     if (q_here) {
       float4* dst = reinterpret_cast<float4*>(qs + (tid / (D / 8)) * DP + (tid % (D / 8)) * 8);
@@ -201,27 +217,35 @@ __global__ void __launch_bounds__(kSelectThreads) zr_select_kernel(StepArgs a) {
       dst[1] = make_float4(qv[4], qv[5], qv[6], qv[7]);
     }
 #pragma unroll
-    for (int j = 0; j < kPer; ++j) {
+    for (int j = 0; j < PER; ++j) {
       const int e = tid + j * kSelectThreads;
-      if (e < rows * (D / 8)) {
-        float4* dst = reinterpret_cast<float4*>(ks + (e / (D / 8)) * DP + (e % (D / 8)) * 8);
-        dst[0] = make_float4(v[j][0], v[j][1], v[j][2], v[j][3]);
-        dst[1] = make_float4(v[j][4], v[j][5], v[j][6], v[j][7]);
-      }
+      if (e < rows * LY::kPieces)
+        *reinterpret_cast<uint4*>(stage + (e / LY::kPieces) * LY::kRowBytes + (e % LY::kPieces) * 16) = v[j];
     }
     __syncthreads();
-    for (int pi = tid; pi < rows * G; pi += blockDim.x) {
-      const int i = pi / G, h = pi - i * G;
-      const float4* sr = reinterpret_cast<const float4*>(ks + i * DP);
-      const float4* qr = reinterpret_cast<const float4*>(qs + h * DP);
+    // One sequential chain per (segment, head) pair, 16-byte shared-memory reads of both operands.
+    const int npairs = rows * G;
+    for (int pi = tid; pi < npairs; pi += blockDim.x) {
+      const unsigned char* srow = stage + (pi / G) * LY::kRowBytes;
+      const float4* q4 = reinterpret_cast<const float4*>(qs + (pi % G) * DP);
       float acc = 0.f;
-#pragma unroll 8
-      for (int t4 = 0; t4 < D / 4; ++t4) {
-        const float4 x = sr[t4], y = qr[t4];
-        acc = __fadd_rn(acc, __fmul_rn(y.x, x.x));
-        acc = __fadd_rn(acc, __fmul_rn(y.y, x.y));
-        acc = __fadd_rn(acc, __fmul_rn(y.z, x.z));
-        acc = __fadd_rn(acc, __fmul_rn(y.w, x.w));
+#pragma unroll 4
+      for (int pc = 0; pc < LY::kPieces; ++pc) {
+        const uint4 w = *reinterpret_cast<const uint4*>(srow + 16 * pc);
+        float sv[EPP], qv[EPP];
+        if constexpr (sizeof(T) == 2) {
+          sv[0] = bf16_lo(w.x); sv[1] = bf16_hi(w.x); sv[2] = bf16_lo(w.y); sv[3] = bf16_hi(w.y);
+          sv[4] = bf16_lo(w.z); sv[5] = bf16_hi(w.z); sv[6] = bf16_lo(w.w); sv[7] = bf16_hi(w.w);
+          const float4 qa = q4[2 * pc], qb = q4[2 * pc + 1];
+          qv[0] = qa.x; qv[1] = qa.y; qv[2] = qa.z; qv[3] = qa.w; qv[4] = qb.x; qv[5] = qb.y; qv[6] = qb.z; qv[7] = qb.w;
+        } else {
+          sv[0] = __uint_as_float(w.x); sv[1] = __uint_as_float(w.y);
+          sv[2] = __uint_as_float(w.z); sv[3] = __uint_as_float(w.w);
+          const float4 qa = q4[pc];
+          qv[0] = qa.x; qv[1] = qa.y; qv[2] = qa.z; qv[3] = qa.w;
+        }
+#pragma unroll
+        for (int e = 0; e < EPP; ++e) acc = __fadd_rn(acc, __fmul_rn(qv[e], sv[e]));
       }
       pairv[pi] = acc;
     }
@@ -232,113 +256,189 @@ __global__ void __launch_bounds__(kSelectThreads) zr_select_kernel(StepArgs a) {
       keys[c0 + i] = key;
     }
   }
+  if (tid < 4) keys[n + tid] = -INFINITY;  // pad for the 4-wide reads below
   __syncthreads();
 
-  // 2. top-k: segment i is selected iff fewer than k segments beat it (greater key, or equal key and lower index).
+  // 2. top-k: segment i is selected iff fewer than k segments beat it (a greater key, or an equal
+  //    key and a lower index). Branch-free count over 4-wide reads; the pad never beats a key.
+  const float4* keys4 = reinterpret_cast<const float4*>(keys);
   for (int i = tid; i < n; i += blockDim.x) {
     const float ki = keys[i];
     int cnt = 0;
-    for (int j = 0; j < n && cnt < k; ++j) {
-      const float kj = keys[j];
-      cnt += (kj > ki) || (kj == ki && j < i);
+#pragma unroll 4
+    for (int j4 = 0; j4 < (n + 3) >> 2; ++j4) {
+      const float4 kv = keys4[j4];
+      const int j = 4 * j4;
+      cnt += (kv.x > ki) | ((kv.x == ki) & (j < i));
+      cnt += (kv.y > ki) | ((kv.y == ki) & (j + 1 < i));
+      cnt += (kv.z > ki) | ((kv.z == ki) & (j + 2 < i));
+      cnt += (kv.w > ki) | ((kv.w == ki) & (j + 3 < i));
     }
     flag[i] = cnt < k ? 1 : 0;
   }
   __syncthreads();
 
-  // Compact the selected segments (ascending) and the summary list (the rest, ascending).
+  // 3. the selected list (ascending), the summary list (the rest, ascending), the maximal runs of
+  //    selected segments (consecutive segments touch), and the token ranges: the runs merged with
+  //    the window [W0, L) -- the first run reaching W0 absorbs it, later runs lie inside it.
   int* sel_ws = a.sel + static_cast<size_t>(u) * a.k_max;
   int* sum_ws = a.sumlist + static_cast<size_t>(u) * a.n_max;
-  {
-    const int per = (n + blockDim.x - 1) / blockDim.x;
-    const int i0 = min(n, tid * per), i1 = min(n, i0 + per);
-    int local = 0;
-    for (int i = i0; i < i1; ++i) local += flag[i];
-    int total;
-    int pos = block_exclusive_scan(local, &total);
-    for (int i = i0; i < i1; ++i) {
-      if (flag[i]) {
-        list[pos] = i;
-        sel_ws[pos] = i;
-        ++pos;
+  int* rg = a.ranges + static_cast<size_t>(u) * (a.k_max + 1) * 2;
+  int* cum = a.cum + static_cast<size_t>(u) * (a.k_max + 2);
+  int* rout = a.ranges_out ? a.ranges_out + static_cast<size_t>(u) * (a.k_max + 1) * 2 : nullptr;
+  const int W0 = max(0, L - a.window);
+  if (n <= kSelectThreads) {
+    // One thread per segment: compaction and run numbering from warp ballots.
+    __shared__ int s_cnt[3][kSelectThreads / 32];
+    const int lane = tid & 31, wi = tid >> 5, nwarps = blockDim.x >> 5;
+    const bool in = tid < n;
+    const bool sel = in && flag[tid];
+    const bool rstart = sel && !(tid > 0 && flag[tid - 1]);
+    const bool rend = sel && !(tid + 1 < n && flag[tid + 1]);
+    const int e_i = in ? bnd[tid + 1] : 0;
+    const unsigned bs = __ballot_sync(kFull, sel), bst = __ballot_sync(kFull, rstart);
+    const unsigned bbe = __ballot_sync(kFull, rend && e_i < W0);
+    if (lane == 0) {
+      s_cnt[0][wi] = __popc(bs);
+      s_cnt[1][wi] = __popc(bst);
+      s_cnt[2][wi] = __popc(bbe);
+    }
+    __syncthreads();
+    int off_s = 0, off_r = 0, m = 0, rstar = 0;
+    for (int w = 0; w < nwarps; ++w) {
+      if (w < wi) {
+        off_s += s_cnt[0][w];
+        off_r += s_cnt[1][w];
+      }
+      m += s_cnt[1][w];
+      rstar += s_cnt[2][w];  // runs that end before the window starts
+    }
+    const unsigned lt = (1u << lane) - 1u;
+    const int pos = off_s + __popc(bs & lt);
+    if (in) {
+      if (sel) {
+        list[pos] = tid;
+        sel_ws[pos] = tid;
       } else {
-        sum_ws[i - pos] = i;
+        sum_ws[tid - pos] = tid;
       }
     }
-  }
-  __syncthreads();
-
-  // 3. maximal runs of selected segments (adjacent segments touch: bound[i+1] == bound[i+1]).
-  int m;
-  {
-    const int per = (k + blockDim.x - 1) / blockDim.x;
-    const int j0 = min(k, tid * per), j1 = min(k, j0 + per);
-    int starts = 0;
-    for (int j = j0; j < j1; ++j) starts += (j == 0) || (bnd[list[j - 1] + 1] != bnd[list[j]]);
-    int ridx = block_exclusive_scan(starts, &m) - 1;
-    for (int j = j0; j < j1; ++j) {
-      const int seg = list[j];
-      if ((j == 0) || (bnd[list[j - 1] + 1] != bnd[seg])) runs_s[++ridx] = bnd[seg];
-      if ((j == k - 1) || (bnd[list[j + 1]] != bnd[seg + 1])) runs_e[ridx] = bnd[seg + 1];
+    if (rstart) runs_s[off_r + __popc(bst & lt)] = bnd[tid];
+    if (rend) runs_e[off_r + __popc(bst & (lt | (1u << lane))) - 1] = e_i;
+    __syncthreads();
+    const int nr = rstar < m ? rstar + 1 : m + (W0 < L ? 1 : 0);
+    if (wi == 0) {
+      int carry = 0;
+      for (int r0 = 0; r0 < nr; r0 += 32) {
+        const int r = r0 + lane;
+        int s_ = 0, e_ = 0;
+        if (r < nr) {
+          if (r < rstar) {
+            s_ = runs_s[r];
+            e_ = runs_e[r];
+          } else {
+            s_ = rstar < m ? min(W0, runs_s[rstar]) : W0;
+            e_ = L;
+          }
+        }
+        const int len = e_ - s_;
+        const int incl = warp_incl_scan(len, lane);
+        if (r < nr) {
+          rg[2 * r] = s_;
+          rg[2 * r + 1] = e_;
+          cum[r] = carry + incl - len;
+          if (rout) {
+            rout[2 * r] = s_;
+            rout[2 * r + 1] = e_;
+          }
+        }
+        carry += __shfl_sync(kFull, incl, 31);
+      }
+      if (lane == 0) {
+        cum[nr] = carry;
+        a.unit_info[u] = make_int4(nr, carry, n - k, 0);
+        if (a.nranges_out) a.nranges_out[u] = nr;
+      }
     }
-  }
-  if (tid == 0) s_rstar = m;
-  __syncthreads();
-  // Merge with the window [W0, L): the first run reaching W0 absorbs it; later runs lie inside it.
-  const int W0 = max(0, L - a.window);
-  for (int r = tid; r < m; r += blockDim.x)
-    if (runs_e[r] >= W0 && (r == 0 || runs_e[r - 1] < W0)) s_rstar = r;
-  __syncthreads();
-  const int rstar = s_rstar;
-  const int nr = rstar < m ? rstar + 1 : m + (W0 < L ? 1 : 0);
-  int* rg = a.ranges + static_cast<size_t>(u) * (a.k_max + 1) * 2;
-  int* lens = flag;  // flags are no longer needed
-  for (int r = tid; r < nr; r += blockDim.x) {
-    int s, e;
-    if (r < rstar) {
-      s = runs_s[r];
-      e = runs_e[r];
-    } else if (rstar < m) {
-      s = min(W0, runs_s[rstar]);
-      e = L;
-    } else {
-      s = W0;
-      e = L;
+  } else {
+    // Any n: block-wide scans over contiguous per-thread slices.
+    {
+      const int per = (n + blockDim.x - 1) / blockDim.x;
+      const int i0 = min(n, tid * per), i1 = min(n, i0 + per);
+      int local = 0;
+      for (int i = i0; i < i1; ++i) local += flag[i];
+      int total;
+      int pos = block_exclusive_scan(local, &total);
+      for (int i = i0; i < i1; ++i) {
+        if (flag[i]) {
+          list[pos] = i;
+          sel_ws[pos] = i;
+          ++pos;
+        } else {
+          sum_ws[i - pos] = i;
+        }
+      }
     }
-    rg[2 * r] = s;
-    rg[2 * r + 1] = e;
-    lens[r] = e - s;
-    if (a.ranges_out) {
-      int* ro = a.ranges_out + static_cast<size_t>(u) * (a.k_max + 1) * 2;
-      ro[2 * r] = s;
-      ro[2 * r + 1] = e;
+    __syncthreads();
+    int m;
+    {
+      const int per = (k + blockDim.x - 1) / blockDim.x;
+      const int j0 = min(k, tid * per), j1 = min(k, j0 + per);
+      int starts = 0;
+      for (int j = j0; j < j1; ++j) starts += (j == 0) || (bnd[list[j - 1] + 1] != bnd[list[j]]);
+      int ridx = block_exclusive_scan(starts, &m) - 1;
+      for (int j = j0; j < j1; ++j) {
+        const int seg = list[j];
+        if ((j == 0) || (bnd[list[j - 1] + 1] != bnd[seg])) runs_s[++ridx] = bnd[seg];
+        if ((j == k - 1) || (bnd[list[j + 1]] != bnd[seg + 1])) runs_e[ridx] = bnd[seg + 1];
+      }
     }
-  }
-  __syncthreads();
-  int* cum = a.cum + static_cast<size_t>(u) * (a.k_max + 2);
-  int n_tok;
-  {
-    const int per = (nr + blockDim.x - 1) / blockDim.x;
-    const int r0 = min(nr, tid * per), r1 = min(nr, r0 + per);
-    int local = 0;
-    for (int r = r0; r < r1; ++r) local += lens[r];
-    int run = block_exclusive_scan(local, &n_tok);
-    for (int r = r0; r < r1; ++r) {
-      cum[r] = run;
-      run += lens[r];
+    if (tid == 0) s_rstar = m;
+    __syncthreads();
+    for (int r = tid; r < m; r += blockDim.x)
+      if (runs_e[r] >= W0 && (r == 0 || runs_e[r - 1] < W0)) s_rstar = r;
+    __syncthreads();
+    const int rstar = s_rstar;
+    const int nr = rstar < m ? rstar + 1 : m + (W0 < L ? 1 : 0);
+    int* lens = flag;  // flags are no longer needed
+    for (int r = tid; r < nr; r += blockDim.x) {
+      int s_, e_;
+      if (r < rstar) {
+        s_ = runs_s[r];
+        e_ = runs_e[r];
+      } else if (rstar < m) {
+        s_ = min(W0, runs_s[rstar]);
+        e_ = L;
+      } else {
+        s_ = W0;
+        e_ = L;
+      }
+      rg[2 * r] = s_;
+      rg[2 * r + 1] = e_;
+      lens[r] = e_ - s_;
+      if (rout) {
+        rout[2 * r] = s_;
+        rout[2 * r + 1] = e_;
+      }
     }
-  }
-  if (tid == 0) {
-    cum[nr] = n_tok;
-    const int n_sum = n - k;
-    const int rows = n_tok + n_sum;
-    int n_chunks = (rows + a.chunk_rows - 1) / a.chunk_rows;
-    if (n_chunks > a.meta.slots[b]) {
-      atomicOr(a.err, kErrSlots);
-      n_chunks = a.meta.slots[b];
+    __syncthreads();
+    int n_tok;
+    {
+      const int per = (nr + blockDim.x - 1) / blockDim.x;
+      const int r0 = min(nr, tid * per), r1 = min(nr, r0 + per);
+      int local = 0;
+      for (int r = r0; r < r1; ++r) local += lens[r];
+      int run = block_exclusive_scan(local, &n_tok);
+      for (int r = r0; r < r1; ++r) {
+        cum[r] = run;
+        run += lens[r];
+      }
     }
-    a.unit_info[u] = make_int4(nr, n_tok, n_sum, n_chunks);
-    if (a.nranges_out) a.nranges_out[u] = nr;
+    if (tid == 0) {
+      cum[nr] = n_tok;
+      a.unit_info[u] = make_int4(nr, n_tok, n - k, 0);
+      if (a.nranges_out) a.nranges_out[u] = nr;
+    }
   }
   if (a.sel_out) {
     int* so = a.sel_out + static_cast<size_t>(u) * a.k_max;
@@ -347,63 +447,166 @@ __global__ void __launch_bounds__(kSelectThreads) zr_select_kernel(StepArgs a) {
 }
 
 // ------------------------------------------------------------------ attend: shared pieces
-struct SlotInfo {
-  int b, g, c, u;
-};
+// The rows every unit gathers (its tokens through the block table, then its summary rows) are
+// laid end to end in unit order, R rows in all, and the attend grid's warps split them evenly:
+// warp w takes global rows [w*R/N, (w+1)*R/N) with N = min(warps, R), so every warp streams
+// the same number of bytes whatever the units' sizes. A warp writes one partial per unit its
+// range touches, into slot u + w: the (unit, warp) pairs that intersect form a monotone
+// staircase, so u + w is unique and the slots never exceed U + N.
 
-// Which (sequence, KV head, chunk) a split slot belongs to. slot_base is strictly increasing.
-__device__ __forceinline__ SlotInfo decode_slot(const StepArgs& a, int slot, int lane) {
-  int b = 0;
-  for (int base = 0; base < a.B; base += 32) {
-    const int cand = base + lane;
-    const bool le = cand < a.B && a.meta.slot_base[cand] <= slot;
-    const unsigned m = __ballot_sync(kFull, le);
-    if (m) b = base + 31 - __clz(m);
-    if (m != kFull) break;
-  }
-  const int rel = slot - a.meta.slot_base[b];
-  const int S = a.meta.slots[b];
-  SlotInfo s;
-  s.b = b;
-  s.g = rel / S;
-  s.c = rel - s.g * S;
-  s.u = b * a.Hkv + s.g;
-  return s;
+__device__ __forceinline__ int unit_rows(const StepArgs& a, int u) {
+  const int4 i = a.unit_info[u];
+  return i.y + i.z;
 }
 
-// Fill one warp's row table for rows [row0, row0 + nrows) of unit u: pool row id
-// ((block * Hkv + g) * 16 + slot) for gathered tokens, summary row id | flag after
-// them, kInvalidRow past the end or for a block id outside the pool.
-__device__ __forceinline__ void build_row_table(const StepArgs& a, const SlotInfo& s, int4 info, int row0,
-                                                int nrows, uint32_t* tab, int lane) {
-  const int n_tok = info.y;
-  const int32_t* rg = a.ranges + static_cast<size_t>(s.u) * (a.k_max + 1) * 2;
-  const int32_t* cum = a.cum + static_cast<size_t>(s.u) * (a.k_max + 2);
-  const int32_t* sl = a.sumlist + static_cast<size_t>(s.u) * a.n_max;
-  const int32_t* bt = a.block_tables + static_cast<size_t>(s.b) * a.max_blocks;
-  const int seg0 = a.meta.seg_ptr[s.b];
-  int r = 0;
-  for (int e = lane; e < a.chunk_rows; e += 32) {
-    uint32_t id = kInvalidRow;
-    if (e < nrows) {
-      const int j = row0 + e;
-      if (j < n_tok) {
-        while (r + 1 < info.x && cum[r + 1] <= j) ++r;
-        const int t = rg[2 * r] + (j - cum[r]);
+struct WarpRange {
+  long long s, e;  // this warp's global rows [s, e)
+  long long R;     // rows of all units
+  long long N;     // warps that get rows
+  int u;           // unit containing row s
+  long long P;     // first global row of unit u
+  int Ru;          // rows of unit u
+};
+
+// This warp's share of the rows and the unit where it starts; false when it gets no rows.
+__device__ bool locate_range(const StepArgs& a, int w, int nwarps, int lane, WarpRange& wr) {
+  const int U = a.B * a.Hkv;
+  constexpr int K = 8;  // units kept in registers per lane: one memory round trip when U <= 256
+  const bool fast = U <= 32 * K;
+  int v[K];
+  long long tot = 0;
+  if (fast) {
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      const int u = 32 * k + lane;
+      v[k] = u < U ? unit_rows(a, u) : 0;
+      tot += v[k];
+    }
+  } else {
+    for (int u = lane; u < U; u += 32) tot += unit_rows(a, u);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(kFull, tot, o);
+  wr.R = tot;
+  wr.N = min(static_cast<long long>(nwarps), tot);
+  if (w >= wr.N) return false;
+  wr.s = static_cast<long long>(w) * tot / wr.N;
+  wr.e = static_cast<long long>(w + 1) * tot / wr.N;
+  long long carry = 0;
+  auto found = [&](int base, int r, int incl) {
+    const unsigned m = __ballot_sync(kFull, carry + incl > wr.s);
+    const int l = __ffs(m) - 1;
+    wr.u = base + l;
+    wr.Ru = __shfl_sync(kFull, r, l);
+    wr.P = carry + __shfl_sync(kFull, incl, l) - wr.Ru;
+  };
+  if (fast) {
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      if (32 * k < U) {
+        const int incl = warp_incl_scan(v[k], lane);
+        const int ctot = __shfl_sync(kFull, incl, 31);
+        if (carry + ctot > wr.s) {
+          found(32 * k, v[k], incl);
+          return true;
+        }
+        carry += ctot;
+      }
+    }
+  } else {
+    for (int base = 0; base < U; base += 32) {
+      const int r = base + lane < U ? unit_rows(a, base + lane) : 0;
+      const int incl = warp_incl_scan(r, lane);
+      const int ctot = __shfl_sync(kFull, incl, 31);
+      if (carry + ctot > wr.s) {
+        found(base, r, incl);
+        return true;
+      }
+      carry += ctot;
+    }
+  }
+  return false;  // not reached: row s < R lies in some unit
+}
+
+// Fill tab[0, kChunkRows) for the unit-local rows [r0, r0 + n) of unit u: the pool row id
+// ((block * Hkv + g) * 16 + slot) of each gathered token, then (summary row id | flag) for the
+// summary rows, kInvalidRow past n or for a block id outside the pool. Lane l owns entries
+// l, l + 32, ...; the token ranges are walked 32 at a time, each lane holding one.
+__device__ void build_row_table(const StepArgs& a, int b, int g, int u, int4 info, int r0, int n, uint32_t* tab,
+                                int lane) {
+  const int nr = info.x, n_tok = info.y;
+  const int32_t* rg = a.ranges + static_cast<size_t>(u) * (a.k_max + 1) * 2;
+  const int32_t* cum = a.cum + static_cast<size_t>(u) * (a.k_max + 2);
+  const int32_t* sl = a.sumlist + static_cast<size_t>(u) * a.n_max;
+  const int32_t* bt = a.block_tables + static_cast<size_t>(b) * a.max_blocks;
+  const int seg0 = a.meta.seg_ptr[b];
+  __syncwarp();  // the previous table's readers are done
+  for (int e = lane; e < kChunkRows; e += 32) tab[e] = kInvalidRow;
+  const int tok_end = min(r0 + n, n_tok);
+  for (int base = 0; base < nr && r0 < tok_end; base += 32) {
+    const int i = base + lane;
+    const int cs = i < nr ? cum[i] : 0x7fffffff;
+    const int ce = i < nr ? cum[i + 1] : 0x7fffffff;
+    const int st = i < nr ? rg[2 * i] : 0;
+    unsigned m = __ballot_sync(kFull, i < nr && ce > r0 && cs < tok_end);
+    while (m) {
+      const int l = __ffs(m) - 1;
+      m &= m - 1;
+      const int rcs = __shfl_sync(kFull, cs, l), rce = __shfl_sync(kFull, ce, l), rst = __shfl_sync(kFull, st, l);
+      const int e0 = max(rcs, r0) - r0, e1 = min(rce, tok_end) - r0;
+      for (int e = e0 + ((lane - e0) & 31); e < e1; e += 32) {
+        const int t = rst + (r0 + e - rcs);
         const int phys = bt[t >> 4];
         if (static_cast<unsigned>(phys) < static_cast<unsigned>(a.num_blocks)) {
-          id = ((static_cast<uint32_t>(phys) * a.Hkv + s.g) << 4) | static_cast<uint32_t>(t & 15);
+          tab[e] = ((static_cast<uint32_t>(phys) * a.Hkv + g) << 4) | static_cast<uint32_t>(t & 15);
         } else {
           atomicOr(a.err, kErrBadBlock);
         }
-      } else {
-        const int seg = sl[j - n_tok];
-        id = (static_cast<uint32_t>(seg0 + seg) * a.Hkv + s.g) | kSummaryFlag;
       }
     }
-    tab[e] = id;
+    if (__shfl_sync(kFull, ce, 31) >= tok_end) break;  // the last range of this window reaches the end
+  }
+  for (int e = max(n_tok - r0, 0) + ((lane - max(n_tok - r0, 0)) & 31); e < n; e += 32) {
+    const int seg = sl[r0 + e - n_tok];
+    tab[e] = (static_cast<uint32_t>(seg0 + seg) * a.Hkv + g) | kSummaryFlag;
   }
   __syncwarp();
+}
+
+// One warp's walk over its rows: for every unit its range touches, begin_unit, run over row
+// tables of up to kChunkRows rows, and end_unit into slot u + w. The warp holding a unit's first
+// row records which warps hold the unit, for the merge.
+template <class Worker>
+__device__ void attend_balanced(const StepArgs& a, Worker& wk, uint32_t* tab, int warp, int lane) {
+  const int w = blockIdx.x * kAttendWarps + warp;
+  WarpRange wr;
+  if (!locate_range(a, w, a.attend_warps, lane, wr)) return;
+  int u = wr.u;
+  long long P = wr.P;
+  int Ru = wr.Ru;
+  long long pos = wr.s;
+  while (true) {
+    const int b = u / a.Hkv, g = u - b * a.Hkv;
+    const int4 info = a.unit_info[u];
+    const long long end = min(wr.e, P + Ru);
+    const int lo = static_cast<int>(pos - P), hi = static_cast<int>(end - P);
+    if (lo == 0 && lane == 0) {
+      const long long w_last = ((P + Ru) * wr.N + wr.R - 1) / wr.R - 1;  // warp holding the unit's last row
+      a.merge_info[u] = make_int2(w, static_cast<int>(w_last - w + 1));
+    }
+    wk.begin_unit(a, b, g, lane);
+    for (int r0 = lo; r0 < hi; r0 += kChunkRows) {
+      const int nrow = min(kChunkRows, hi - r0);
+      build_row_table(a, b, g, u, info, r0, nrow, tab, lane);
+      wk.run(a, tab, nrow, lane);
+    }
+    wk.end_unit(a, u + w, lane);
+    pos = end;
+    if (pos >= wr.e) break;
+    P += Ru;
+    ++u;
+    Ru = unit_rows(a, u);
+  }
 }
 
 template <typename T, int D>
@@ -559,209 +762,226 @@ __device__ __forceinline__ void mma_compute_tile(MmaState<D>& st, uint32_t stage
 }
 
 template <int D>
-__global__ void __launch_bounds__(kAttendWarps * 32) zr_attend_mma_kernel(StepArgs a) {
-  constexpr int RB = ring_row_bytes<D>();
-  constexpr uint32_t kStageBytes = 32 * RB;
+struct MmaWorker {
+  static constexpr uint32_t kStageBytes = 32 * ring_row_bytes<D>();
+  MmaState<D> st;
+  uint32_t ring;  // this warp's ring (shared-space address)
+  LoadBases lb;
+
+  __device__ void begin_unit(const StepArgs& a, int b, int g, int lane) {
+    const int r = lane >> 2, c = lane & 3, G = a.G;
+    const __nv_bfloat16* qg =
+        static_cast<const __nv_bfloat16*>(a.q) + (static_cast<size_t>(b) * a.Hq + static_cast<size_t>(g) * G) * D;
+#pragma unroll
+    for (int k = 0; k < D / 16; ++k) {
+      if (r < G) {
+        st.qa0[k] = *reinterpret_cast<const uint32_t*>(qg + r * D + 16 * k + 2 * c);
+        st.qa2[k] = *reinterpret_cast<const uint32_t*>(qg + r * D + 16 * k + 2 * c + 8);
+      } else {
+        st.qa0[k] = 0u;
+        st.qa2[k] = 0u;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < D / 16; ++i) st.o[i][0] = st.o[i][1] = st.o[i][2] = st.o[i][3] = 0.f;
+    st.m = -1e30f;
+    st.l = 0.f;
+  }
+
+  __device__ void run(const StepArgs& a, const uint32_t* tab, int nrows, int lane) {
+    const int ntiles = (nrows + 15) >> 4;
+    __syncwarp();  // no lane still reads a stage that the prologue refills
+#pragma unroll
+    for (int i = 0; i < kStages - 1; ++i) {
+      if (i < ntiles) mma_issue_tile<D>(ring + i * kStageBytes, tab, 16 * i, lane, lb);
+      cp_async_commit();
+    }
+    for (int i = 0; i < ntiles; ++i) {
+      const int nx = i + kStages - 1;
+      __syncwarp();  // every lane is done reading the stage that is refilled next
+      if (nx < ntiles) mma_issue_tile<D>(ring + (nx % kStages) * kStageBytes, tab, 16 * nx, lane, lb);
+      cp_async_commit();
+      cp_async_wait<kStages - 1>();
+      __syncwarp();  // tile i's rows, staged by all lanes, are visible to every lane
+      const uint32_t vmask16 = __ballot_sync(kFull, lane < 16 && tab[16 * i + lane] != kInvalidRow) & 0xFFFFu;
+      mma_compute_tile<D>(st, ring + (i % kStages) * kStageBytes, vmask16, a.scale_log2, lane);
+    }
+  }
+
+  __device__ void end_unit(const StepArgs& a, int slot, int lane) {
+    const int r = lane >> 2, c = lane & 3, G = a.G;
+    // head r's sum: add the parts of the four lanes that share r.
+    float l = st.l;
+    l += __shfl_xor_sync(kFull, l, 1);
+    l += __shfl_xor_sync(kFull, l, 2);
+    if (c == 0 && r < G) a.part_ml[static_cast<size_t>(slot) * G + r] = make_float2(st.m, l);
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int h = 2 * c + e;
+      if (h < G) {
+        float* dst = a.part_o + (static_cast<size_t>(slot) * G + h) * D + r;
+#pragma unroll
+        for (int i = 0; i < D / 16; ++i) {
+          dst[16 * i] = st.o[i][e];
+          dst[16 * i + 8] = st.o[i][e + 2];
+        }
+      }
+    }
+  }
+};
+
+template <int D>
+__global__ void __launch_bounds__(kAttendWarps * 32, 3) zr_attend_mma_kernel(StepArgs a) {
   extern __shared__ __align__(16) unsigned char attend_smem[];
   __shared__ uint32_t rowtab[kAttendWarps][kChunkRows];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int slot = blockIdx.x * kAttendWarps + warp;
   pdl_trigger();
-  if (slot >= a.total_slots) return;
-  const SlotInfo s = decode_slot(a, slot, lane);
   pdl_wait();
-  const int4 info = a.unit_info[s.u];
-  if (s.c >= info.w) return;
-  const int rows = info.y + info.z;
-  const int row0 = s.c * a.chunk_rows;
-  const int nrows = min(a.chunk_rows, rows - row0);
-  uint32_t* tab = rowtab[warp];
-  build_row_table(a, s, info, row0, nrows, tab, lane);
-
-  const int r = lane >> 2, c = lane & 3;
-  const int G = a.G;
-  MmaState<D> st;
-  const __nv_bfloat16* qg =
-      static_cast<const __nv_bfloat16*>(a.q) + (static_cast<size_t>(s.b) * a.Hq + static_cast<size_t>(s.g) * G) * D;
-#pragma unroll
-  for (int k = 0; k < D / 16; ++k) {
-    if (r < G) {
-      st.qa0[k] = *reinterpret_cast<const uint32_t*>(qg + r * D + 16 * k + 2 * c);
-      st.qa2[k] = *reinterpret_cast<const uint32_t*>(qg + r * D + 16 * k + 2 * c + 8);
-    } else {
-      st.qa0[k] = 0u;
-      st.qa2[k] = 0u;
-    }
-  }
-#pragma unroll
-  for (int i = 0; i < D / 16; ++i) st.o[i][0] = st.o[i][1] = st.o[i][2] = st.o[i][3] = 0.f;
-  st.m = -1e30f;
-  st.l = 0.f;
-
+  MmaWorker<D> wk;
+  wk.ring = static_cast<uint32_t>(__cvta_generic_to_shared(attend_smem)) + warp * kStages * MmaWorker<D>::kStageBytes;
   const int chunk_off = (lane % (D / 8)) * 16;
-  const LoadBases lb{static_cast<const char*>(a.k_pool) + chunk_off, static_cast<const char*>(a.v_pool) + chunk_off,
-                     static_cast<const char*>(a.sum_k) + chunk_off, static_cast<const char*>(a.sum_v) + chunk_off};
-  const uint32_t ring = static_cast<uint32_t>(__cvta_generic_to_shared(attend_smem)) + warp * kStages * kStageBytes;
-  const int ntiles = (nrows + 15) >> 4;
-#pragma unroll
-  for (int i = 0; i < kStages - 1; ++i) {
-    if (i < ntiles) mma_issue_tile<D>(ring + i * kStageBytes, tab, 16 * i, lane, lb);
-    cp_async_commit();
-  }
-  for (int i = 0; i < ntiles; ++i) {
-    const int nx = i + kStages - 1;
-    __syncwarp();  // every lane is done reading the stage that is refilled next
-    if (nx < ntiles) mma_issue_tile<D>(ring + (nx % kStages) * kStageBytes, tab, 16 * nx, lane, lb);
-    cp_async_commit();
-    cp_async_wait<kStages - 1>();
-    __syncwarp();  // tile i's rows, staged by all lanes, are visible to every lane
-    const uint32_t vmask16 = __ballot_sync(kFull, lane < 16 && tab[16 * i + lane] != kInvalidRow) & 0xFFFFu;
-    mma_compute_tile<D>(st, ring + (i % kStages) * kStageBytes, vmask16, a.scale_log2, lane);
-  }
-
-  // head r's sum: add the parts of the four lanes that share r.
-  float l = st.l;
-  l += __shfl_xor_sync(kFull, l, 1);
-  l += __shfl_xor_sync(kFull, l, 2);
-  if (c == 0 && r < G) a.part_ml[static_cast<size_t>(slot) * G + r] = make_float2(st.m, l);
-#pragma unroll
-  for (int e = 0; e < 2; ++e) {
-    const int h = 2 * c + e;
-    if (h < G) {
-      float* dst = a.part_o + (static_cast<size_t>(slot) * G + h) * D + r;
-#pragma unroll
-      for (int i = 0; i < D / 16; ++i) {
-        dst[16 * i] = st.o[i][e];
-        dst[16 * i + 8] = st.o[i][e + 2];
-      }
-    }
-  }
+  wk.lb = LoadBases{static_cast<const char*>(a.k_pool) + chunk_off, static_cast<const char*>(a.v_pool) + chunk_off,
+                    static_cast<const char*>(a.sum_k) + chunk_off, static_cast<const char*>(a.sum_v) + chunk_off};
+  attend_balanced(a, wk, rowtab[warp], warp, lane);
 }
 
 // ------------------------------------------------------------------ attend: CUDA cores (f32, or any G)
+// Lanes split d (D/32 components each); rows are taken one at a time, logits reduced across the
+// warp, and each query head keeps its own online-softmax state.
 template <typename T, int D>
-__global__ void __launch_bounds__(kAttendWarps * 32) zr_attend_fma_kernel(StepArgs a) {
-  constexpr int E = D / 32;
-  __shared__ uint32_t rowtab[kAttendWarps][kChunkRows];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int slot = blockIdx.x * kAttendWarps + warp;
-  pdl_trigger();
-  if (slot >= a.total_slots) return;
-  const SlotInfo s = decode_slot(a, slot, lane);
-  pdl_wait();
-  const int4 info = a.unit_info[s.u];
-  if (s.c >= info.w) return;
-  const int rows = info.y + info.z;
-  const int row0 = s.c * a.chunk_rows;
-  const int nrows = min(a.chunk_rows, rows - row0);
-  uint32_t* tab = rowtab[warp];
-  build_row_table(a, s, info, row0, nrows, tab, lane);
-
-  const int G = a.G;
-  const T* qg = static_cast<const T*>(a.q) + (static_cast<size_t>(s.b) * a.Hq + static_cast<size_t>(s.g) * G) * D;
+struct FmaWorker {
+  static constexpr int E = D / 32;
   float qv[kMaxGroup][E], o[kMaxGroup][E], m[kMaxGroup], l[kMaxGroup];
-#pragma unroll
-  for (int h = 0; h < kMaxGroup; ++h) {
-    m[h] = -1e30f;
-    l[h] = 0.f;
-#pragma unroll
-    for (int e = 0; e < E; ++e) o[h][e] = 0.f;
-    if (h < G) {
-      load_e<T, E>(qg + h * D + lane * E, qv[h]);
-    } else {
-#pragma unroll
-      for (int e = 0; e < E; ++e) qv[h][e] = 0.f;
-    }
-  }
-  const T* kp = static_cast<const T*>(a.k_pool);
-  const T* vp = static_cast<const T*>(a.v_pool);
-  const T* skp = static_cast<const T*>(a.sum_k);
-  const T* svp = static_cast<const T*>(a.sum_v);
-  for (int j = 0; j < nrows; ++j) {
-    const uint32_t id = tab[j];
-    if (id == kInvalidRow) continue;
-    float kv[E], vv[E];
-    load_e<T, E>(row_ptr<T, D>(id, kp, skp) + lane * E, kv);
-    load_e<T, E>(row_ptr<T, D>(id, vp, svp) + lane * E, vv);
+
+  __device__ void begin_unit(const StepArgs& a, int b, int g, int lane) {
+    const int G = a.G;
+    const T* qg = static_cast<const T*>(a.q) + (static_cast<size_t>(b) * a.Hq + static_cast<size_t>(g) * G) * D;
 #pragma unroll
     for (int h = 0; h < kMaxGroup; ++h) {
+      m[h] = -1e30f;
+      l[h] = 0.f;
+#pragma unroll
+      for (int e = 0; e < E; ++e) o[h][e] = 0.f;
       if (h < G) {
-        float dot = 0.f;
+        load_e<T, E>(qg + h * D + lane * E, qv[h]);
+      } else {
 #pragma unroll
-        for (int e = 0; e < E; ++e) dot = fmaf(qv[h][e], kv[e], dot);
-#pragma unroll
-        for (int o2 = 16; o2 > 0; o2 >>= 1) dot += __shfl_xor_sync(kFull, dot, o2);
-        const float x = dot * a.scale_log2;
-        const float mn = fmaxf(m[h], x);
-        const float alpha = fast_exp2(m[h] - mn);
-        const float p = fast_exp2(x - mn);
-        l[h] = l[h] * alpha + p;
-#pragma unroll
-        for (int e = 0; e < E; ++e) o[h][e] = fmaf(p, vv[e], o[h][e] * alpha);
-        m[h] = mn;
+        for (int e = 0; e < E; ++e) qv[h][e] = 0.f;
       }
     }
   }
+
+  __device__ void run(const StepArgs& a, const uint32_t* tab, int nrows, int lane) {
+    const int G = a.G;
+    const T* kp = static_cast<const T*>(a.k_pool);
+    const T* vp = static_cast<const T*>(a.v_pool);
+    const T* skp = static_cast<const T*>(a.sum_k);
+    const T* svp = static_cast<const T*>(a.sum_v);
+    for (int j = 0; j < nrows; ++j) {
+      const uint32_t id = tab[j];
+      if (id == kInvalidRow) continue;
+      float kv[E], vv[E];
+      load_e<T, E>(row_ptr<T, D>(id, kp, skp) + lane * E, kv);
+      load_e<T, E>(row_ptr<T, D>(id, vp, svp) + lane * E, vv);
 #pragma unroll
-  for (int h = 0; h < kMaxGroup; ++h) {
-    if (h < G) {
-      float* dst = a.part_o + (static_cast<size_t>(slot) * G + h) * D + lane * E;
+      for (int h = 0; h < kMaxGroup; ++h) {
+        if (h < G) {
+          float dot = 0.f;
 #pragma unroll
-      for (int e = 0; e < E; ++e) dst[e] = o[h][e];
-      if (lane == 0) a.part_ml[static_cast<size_t>(slot) * G + h] = make_float2(m[h], l[h]);
+          for (int e = 0; e < E; ++e) dot = fmaf(qv[h][e], kv[e], dot);
+#pragma unroll
+          for (int o2 = 16; o2 > 0; o2 >>= 1) dot += __shfl_xor_sync(kFull, dot, o2);
+          const float x = dot * a.scale_log2;
+          const float mn = fmaxf(m[h], x);
+          const float alpha = fast_exp2(m[h] - mn);
+          const float p = fast_exp2(x - mn);
+          l[h] = l[h] * alpha + p;
+#pragma unroll
+          for (int e = 0; e < E; ++e) o[h][e] = fmaf(p, vv[e], o[h][e] * alpha);
+          m[h] = mn;
+        }
+      }
     }
   }
+
+  __device__ void end_unit(const StepArgs& a, int slot, int lane) {
+    const int G = a.G;
+#pragma unroll
+    for (int h = 0; h < kMaxGroup; ++h) {
+      if (h < G) {
+        float* dst = a.part_o + (static_cast<size_t>(slot) * G + h) * D + lane * E;
+#pragma unroll
+        for (int e = 0; e < E; ++e) dst[e] = o[h][e];
+        if (lane == 0) a.part_ml[static_cast<size_t>(slot) * G + h] = make_float2(m[h], l[h]);
+      }
+    }
+  }
+};
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kAttendWarps * 32) zr_attend_fma_kernel(StepArgs a) {
+  __shared__ uint32_t rowtab[kAttendWarps][kChunkRows];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_trigger();
+  pdl_wait();
+  FmaWorker<T, D> wk;
+  attend_balanced(a, wk, rowtab[warp], warp, lane);
 }
 
 // ------------------------------------------------------------------ merge
-// Lanes first own chunks (max, weights, weighted sums of l), then own d components while
-// the chunk loop is unrolled so that several partial rows are in flight at once.
+// One warp per (sequence, query head, 32-wide slice of d). Lane k sums the unit's partials
+// k, k + 32, ... over the slice with weights 2^(m_k - M); a transposed warp reduction then
+// leaves the total of component j in lane j.
 template <int D>
 __global__ void __launch_bounds__(kAttendWarps * 32) zr_merge_kernel(StepArgs a) {
-  constexpr int E = D / 32;
+  constexpr int NDC = D / 32;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int w = blockIdx.x * kAttendWarps + warp;
   pdl_trigger();
-  if (w >= a.B * a.Hq) return;
-  const int b = w / a.Hq, h = w - b * a.Hq;
+  if (w >= a.B * a.Hq * NDC) return;
+  const int dc = w % NDC, bh = w / NDC;
+  const int b = bh / a.Hq, h = bh - b * a.Hq;
   const int G = a.G, g = h / G, hh = h - g * G;
   const int u = b * a.Hkv + g;
-  const int base = a.meta.slot_base[b] + g * a.meta.slots[b];
   pdl_wait();
-  const int nch = a.unit_info[u].w;
-  const float2* ml = a.part_ml + static_cast<size_t>(base) * G + hh;
+  const int2 mi = a.merge_info[u];
+  const size_t first = static_cast<size_t>(u) + mi.x;
+  const int cnt = mi.y;
   float M = -INFINITY;
-  for (int c = lane; c < nch; c += 32) M = fmaxf(M, ml[static_cast<size_t>(c) * G].x);
+  for (int k = lane; k < cnt; k += 32) M = fmaxf(M, a.part_ml[(first + k) * G + hh].x);
 #pragma unroll
   for (int o2 = 16; o2 > 0; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o2));
-  float acc[E];
+  float acc[32];
 #pragma unroll
-  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  for (int j = 0; j < 32; ++j) acc[j] = 0.f;
   float Ls = 0.f;
-  const float* po = a.part_o + (static_cast<size_t>(base) * G + hh) * D + lane * E;
-  for (int c0 = 0; c0 < nch; c0 += 32) {
-    float wgt = 0.f;
-    if (c0 + lane < nch) {
-      const float2 v = ml[static_cast<size_t>(c0 + lane) * G];
-      wgt = fast_exp2(v.x - M);
-      Ls = fmaf(v.y, wgt, Ls);
-    }
-    const int cnt = min(32, nch - c0);
-#pragma unroll 8
-    for (int j = 0; j < cnt; ++j) {
-      const float wj = __shfl_sync(kFull, wgt, j);
-      float v[E];
-      load_e<float, E>(po + static_cast<size_t>(c0 + j) * G * D, v);
+  for (int k = lane; k < cnt; k += 32) {
+    const float2 ml = a.part_ml[(first + k) * G + hh];
+    const float wk = fast_exp2(ml.x - M);
+    Ls = fmaf(ml.y, wk, Ls);
+    const float4* src = reinterpret_cast<const float4*>(a.part_o + ((first + k) * G + hh) * D + 32 * dc);
 #pragma unroll
-      for (int e = 0; e < E; ++e) acc[e] = fmaf(wj, v[e], acc[e]);
+    for (int q = 0; q < 8; ++q) {
+      const float4 v = src[q];
+      acc[4 * q + 0] = fmaf(wk, v.x, acc[4 * q + 0]);
+      acc[4 * q + 1] = fmaf(wk, v.y, acc[4 * q + 1]);
+      acc[4 * q + 2] = fmaf(wk, v.z, acc[4 * q + 2]);
+      acc[4 * q + 3] = fmaf(wk, v.w, acc[4 * q + 3]);
     }
   }
 #pragma unroll
   for (int o2 = 16; o2 > 0; o2 >>= 1) Ls += __shfl_xor_sync(kFull, Ls, o2);
-  const float inv = 1.f / Ls;
-  float* dst = a.out + (static_cast<size_t>(b) * a.Hq + h) * D + lane * E;
 #pragma unroll
-  for (int e = 0; e < E; ++e) dst[e] = acc[e] * inv;
+  for (int off = 16; off >= 1; off >>= 1) {
+    const bool upper = (lane & off) != 0;
+#pragma unroll
+    for (int i = 0; i < off; ++i) {
+      const float send = upper ? acc[i] : acc[i + off];
+      const float keep = upper ? acc[i + off] : acc[i];
+      acc[i] = keep + __shfl_xor_sync(kFull, send, off);
+    }
+  }
+  a.out[(static_cast<size_t>(b) * a.Hq + h) * D + 32 * dc + lane] = acc[0] / Ls;
 }
 
 // ------------------------------------------------------------------ launch
@@ -780,21 +1000,56 @@ cudaError_t launch_pdl(Kern kernel, dim3 grid, dim3 block, size_t smem, cudaStre
   return cudaLaunchKernelEx(&cfg, kernel, a);
 }
 
-size_t select_smem_bytes(int d, int n_max) {
-  const size_t fixed = d == 64 ? select_fixed_words<64>() : select_fixed_words<128>();
-  return (fixed + static_cast<size_t>(n_max) * 6 + 3) * 4;
+template <typename T, int D>
+size_t select_smem_bytes(int n_max) {
+  return SelectLayout<T, D>::kFixedBytes + (static_cast<size_t>(n_max) * 6 + 7) * 4;
 }
 
 template <typename T, int D>
-zr_status configure_for(Plan& p) {
-  if constexpr (sizeof(T) == 2) {
-    if (cudaFuncSetAttribute(zr_attend_mma_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(attend_ring_bytes<D>())) != cudaSuccess) {
-      cudaGetLastError();
-      return ZR_ECUDA;
-    }
+bool uses_mma(const Plan& p) {
+  if constexpr (sizeof(T) == 2) return p.G <= kMmaMaxGroup;
+  return false;
+}
+
+template <typename T, int D>
+zr_status configure_for(Plan& p, int64_t useful_warps) {
+  int sms = 0, occ = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, p.device) != cudaSuccess) {
+    cudaGetLastError();
+    return ZR_ECUDA;
   }
-  p.select_smem = select_smem_bytes(D, p.n_max);
+  cudaError_t e = cudaSuccess;
+  if (uses_mma<T, D>(p)) {
+    p.attend_smem = attend_ring_bytes<D>();
+    if constexpr (sizeof(T) == 2) {
+      e = cudaFuncSetAttribute(zr_attend_mma_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(p.attend_smem));
+      if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, zr_attend_mma_kernel<D>, kAttendWarps * 32,
+                                                          p.attend_smem);
+    }
+  } else {
+    p.attend_smem = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, zr_attend_fma_kernel<T, D>, kAttendWarps * 32, 0);
+  }
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return ZR_ECUDA;
+  }
+  int64_t ctas = static_cast<int64_t>(sms) * (occ > 0 ? occ : 1);
+  ctas = std::min<int64_t>(ctas, (useful_warps + kAttendWarps - 1) / kAttendWarps);
+  p.attend_ctas = static_cast<int>(std::max<int64_t>(ctas, 1));
+  p.attend_warps = p.attend_ctas * kAttendWarps;
+  // One shared-memory carveout for all three kernels: a kernel whose preferred L1/shared split
+  // differs from the previous one's makes the SM drain and reconfigure between them.
+  const int carve = cudaSharedmemCarveoutMaxShared;
+  cudaFuncSetAttribute(zr_select_kernel<T, D>, cudaFuncAttributePreferredSharedMemoryCarveout, carve);
+  cudaFuncSetAttribute(zr_merge_kernel<D>, cudaFuncAttributePreferredSharedMemoryCarveout, carve);
+  cudaFuncSetAttribute(zr_attend_fma_kernel<T, D>, cudaFuncAttributePreferredSharedMemoryCarveout, carve);
+  if constexpr (sizeof(T) == 2)
+    cudaFuncSetAttribute(zr_attend_mma_kernel<D>, cudaFuncAttributePreferredSharedMemoryCarveout, carve);
+  cudaGetLastError();
+  p.select_smem = select_smem_bytes<T, D>(p.n_max);
   if (p.select_smem > 48 * 1024) {
     if (cudaFuncSetAttribute(zr_select_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(p.select_smem)) != cudaSuccess) {
@@ -824,28 +1079,27 @@ cudaError_t launch_for(const Plan& p, const StepArgs& a, cudaStream_t s, cudaEve
   cudaError_t e = launch_pdl(zr_select_kernel<T, D>, dim3(p.Hkv, p.B), dim3(kSelectThreads), p.select_smem, s, a);
   if (e != cudaSuccess) return report("select launch", e), e;
   if (ev0 && (e = record_event(ev0, s)) != cudaSuccess) return report("start event record", e), e;
-  const dim3 grid_attend((p.total_slots + kAttendWarps - 1) / kAttendWarps);
-  bool use_mma = false;
-  if constexpr (sizeof(T) == 2) use_mma = p.G <= kMmaMaxGroup;
-  if (use_mma) {
-    if constexpr (sizeof(T) == 2)
-      e = launch_pdl(zr_attend_mma_kernel<D>, grid_attend, dim3(kAttendWarps * 32), attend_ring_bytes<D>(), s, a);
+  const dim3 grid_attend(p.attend_ctas), block(kAttendWarps * 32);
+  if (uses_mma<T, D>(p)) {
+    if constexpr (sizeof(T) == 2) e = launch_pdl(zr_attend_mma_kernel<D>, grid_attend, block, p.attend_smem, s, a);
   } else {
-    e = launch_pdl(zr_attend_fma_kernel<T, D>, grid_attend, dim3(kAttendWarps * 32), 0, s, a);
+    e = launch_pdl(zr_attend_fma_kernel<T, D>, grid_attend, block, 0, s, a);
   }
   if (e != cudaSuccess) return report("attend launch", e), e;
   if (ev1 && (e = record_event(ev1, s)) != cudaSuccess) return report("stop event record", e), e;
-  const dim3 grid_merge((p.B * p.Hq + kAttendWarps - 1) / kAttendWarps);
-  e = launch_pdl(zr_merge_kernel<D>, grid_merge, dim3(kAttendWarps * 32), 0, s, a);
+  const dim3 grid_merge((p.B * p.Hq * (D / 32) + kAttendWarps - 1) / kAttendWarps);
+  e = launch_pdl(zr_merge_kernel<D>, grid_merge, block, 0, s, a);
   if (e != cudaSuccess) report("merge launch", e);
   return e;
 }
 
 }  // namespace
 
-zr_status configure_kernels(Plan& p) {
-  if (p.cfg.dtype == ZR_BF16) return p.d == 64 ? configure_for<__nv_bfloat16, 64>(p) : configure_for<__nv_bfloat16, 128>(p);
-  return p.d == 64 ? configure_for<float, 64>(p) : configure_for<float, 128>(p);
+zr_status configure_kernels(Plan& p, int64_t useful_warps) {
+  if (p.cfg.dtype == ZR_BF16)
+    return p.d == 64 ? configure_for<__nv_bfloat16, 64>(p, useful_warps)
+                     : configure_for<__nv_bfloat16, 128>(p, useful_warps);
+  return p.d == 64 ? configure_for<float, 64>(p, useful_warps) : configure_for<float, 128>(p, useful_warps);
 }
 
 zr_status launch_step(const Plan& p, const StepArgs& a, void* stream, void* ev_start, void* ev_stop) {

@@ -2,12 +2,12 @@
 // workspace layout, device-error readback.
 //
 // The plan turns the caller's host metadata (sequence lengths, segment bounds,
-// per-sequence top-k) into a few small device arrays and fixes, per sequence,
-// how many split slots each (sequence, KV head) unit may use. The bound on a
-// unit's gathered rows is exact arithmetic on the metadata: at most
-// min(L, min(w, L) + sum of the k largest segment lengths) tokens (the window
-// and the selected segments' ranges, ZoomR page 3.3 "Constructing the Final
-// Multi-Granularity Context") plus exactly n - k summary rows.
+// per-sequence top-k) into a few small device arrays and sizes the persistent
+// attend grid. The bound on a unit's gathered rows is exact arithmetic on the
+// metadata: at most min(L, min(w, L) + sum of the k largest segment lengths)
+// tokens (the window and the selected segments' ranges, ZoomR page 3.3
+// "Constructing the Final Multi-Granularity Context") plus exactly n - k
+// summary rows.
 
 #include <cuda_runtime.h>
 
@@ -87,12 +87,13 @@ zr_status zr_plan(const zr_config* cfg, const int32_t* seq_lens, const int32_t* 
   p.num_blocks = cfg->num_blocks;
   p.max_blocks = cfg->max_blocks_per_seq;
   p.total_segments = seg_ptr[p.B];
-  p.chunk_rows = zr::kChunkRows;
 
-  std::vector<int32_t> kclip(p.B), slots(p.B), slot_base(p.B + 1, 0);
+  // Upper bound on the rows all units gather (window + the k longest segments, plus n - k summary
+  // rows per unit): the attend grid never needs more than one warp per 16 of them.
+  std::vector<int32_t> kclip(p.B);
   p.k_max = 1;
   p.n_max = 1;
-  int64_t total_slots = 0;
+  int64_t rows_bound = 0;
   for (int b = 0; b < p.B; ++b) {
     const int n = seg_ptr[b + 1] - seg_ptr[b];
     const int32_t* bd = seg_bounds + seg_ptr[b] + b;
@@ -106,20 +107,22 @@ zr_status zr_plan(const zr_config* cfg, const int32_t* seq_lens, const int32_t* 
     int64_t top = 0;
     for (int i = 0; i < kclip[b]; ++i) top += lens[i];
     const int64_t tok_bound = std::min<int64_t>(L, std::min<int64_t>(p.window, L) + top);
-    const int64_t rows_bound = tok_bound + (n - kclip[b]);
-    slots[b] = static_cast<int32_t>((rows_bound + p.chunk_rows - 1) / p.chunk_rows);
-    slot_base[b] = static_cast<int32_t>(total_slots);
-    total_slots += static_cast<int64_t>(slots[b]) * p.Hkv;
-    if (total_slots >= (int64_t(1) << 30)) {
-      delete P;
-      return ZR_EUNSUPPORTED;
-    }
+    rows_bound += (tok_bound + (n - kclip[b])) * p.Hkv;
   }
-  slot_base[p.B] = static_cast<int32_t>(total_slots);
-  p.total_slots = static_cast<int>(total_slots);
+  if (cudaGetDevice(&p.device) != cudaSuccess) {
+    cudaGetLastError();
+    delete P;
+    return ZR_ECUDA;
+  }
+  st = zr::configure_kernels(p, (rows_bound + 15) / 16);
+  if (st != ZR_OK) {
+    delete P;
+    return st;
+  }
 
   // Workspace layout (each region 256-byte aligned).
   const size_t U = static_cast<size_t>(p.B) * p.Hkv;
+  const size_t slots = U + static_cast<size_t>(p.attend_warps);
   size_t off = 0;
   auto take = [&](size_t bytes) {
     size_t at = off;
@@ -132,8 +135,9 @@ zr_status zr_plan(const zr_config* cfg, const int32_t* seq_lens, const int32_t* 
   p.ws.cum = take(U * (p.k_max + 2) * sizeof(int32_t));
   p.ws.sumlist = take(U * p.n_max * sizeof(int32_t));
   p.ws.sel = take(U * p.k_max * sizeof(int32_t));
-  p.ws.part_o = take(static_cast<size_t>(p.total_slots) * p.G * p.d * sizeof(float));
-  p.ws.part_ml = take(static_cast<size_t>(p.total_slots) * p.G * 2 * sizeof(float));
+  p.ws.merge_info = take(U * 2 * sizeof(int32_t));
+  p.ws.part_o = take(slots * p.G * p.d * sizeof(float));
+  p.ws.part_ml = take(slots * p.G * 2 * sizeof(float));
   p.ws.total = off;
 
   // Device metadata: one allocation, synchronous copies.
@@ -145,13 +149,7 @@ zr_status zr_plan(const zr_config* cfg, const int32_t* seq_lens, const int32_t* 
     moff = align_up(moff + count * sizeof(int32_t), 256);
     return at;
   };
-  const size_t o_len = mtake(nb), o_ptr = mtake(nb + 1), o_bnd = mtake(n_bounds), o_topk = mtake(nb),
-               o_sbase = mtake(nb + 1), o_slots = mtake(nb);
-  if (cudaGetDevice(&p.device) != cudaSuccess) {
-    cudaGetLastError();
-    delete P;
-    return ZR_ECUDA;
-  }
+  const size_t o_len = mtake(nb), o_ptr = mtake(nb + 1), o_bnd = mtake(n_bounds), o_topk = mtake(nb);
   void* base = nullptr;
   cudaError_t ce = cudaMalloc(&base, moff);
   if (ce != cudaSuccess) {
@@ -165,25 +163,15 @@ zr_status zr_plan(const zr_config* cfg, const int32_t* seq_lens, const int32_t* 
   p.meta.seg_ptr = reinterpret_cast<int32_t*>(cb + o_ptr);
   p.meta.seg_bounds = reinterpret_cast<int32_t*>(cb + o_bnd);
   p.meta.topk = reinterpret_cast<int32_t*>(cb + o_topk);
-  p.meta.slot_base = reinterpret_cast<int32_t*>(cb + o_sbase);
-  p.meta.slots = reinterpret_cast<int32_t*>(cb + o_slots);
   bool ok = cudaMemcpy(p.meta.seq_lens, seq_lens, nb * 4, cudaMemcpyHostToDevice) == cudaSuccess &&
             cudaMemcpy(p.meta.seg_ptr, seg_ptr, (nb + 1) * 4, cudaMemcpyHostToDevice) == cudaSuccess &&
             cudaMemcpy(p.meta.seg_bounds, seg_bounds, n_bounds * 4, cudaMemcpyHostToDevice) == cudaSuccess &&
-            cudaMemcpy(p.meta.topk, kclip.data(), nb * 4, cudaMemcpyHostToDevice) == cudaSuccess &&
-            cudaMemcpy(p.meta.slot_base, slot_base.data(), (nb + 1) * 4, cudaMemcpyHostToDevice) == cudaSuccess &&
-            cudaMemcpy(p.meta.slots, slots.data(), nb * 4, cudaMemcpyHostToDevice) == cudaSuccess;
+            cudaMemcpy(p.meta.topk, kclip.data(), nb * 4, cudaMemcpyHostToDevice) == cudaSuccess;
   if (!ok) {
     cudaGetLastError();
     cudaFree(base);
     delete P;
     return ZR_ECUDA;
-  }
-  st = zr::configure_kernels(p);
-  if (st != ZR_OK) {
-    cudaFree(base);
-    delete P;
-    return st;
   }
   *out_plan = P;
   *workspace_bytes = p.ws.total;
@@ -229,6 +217,7 @@ zr_status decode_into(zr_plan_t plan, void* workspace, const void* q, const void
   a.cum = reinterpret_cast<int32_t*>(ws + p.ws.cum);
   a.sumlist = reinterpret_cast<int32_t*>(ws + p.ws.sumlist);
   a.sel = reinterpret_cast<int32_t*>(ws + p.ws.sel);
+  a.merge_info = reinterpret_cast<int2*>(ws + p.ws.merge_info);
   a.part_o = reinterpret_cast<float*>(ws + p.ws.part_o);
   a.part_ml = reinterpret_cast<float2*>(ws + p.ws.part_ml);
   a.B = p.B;
@@ -240,8 +229,7 @@ zr_status decode_into(zr_plan_t plan, void* workspace, const void* q, const void
   a.max_blocks = p.max_blocks;
   a.k_max = p.k_max;
   a.n_max = p.n_max;
-  a.total_slots = p.total_slots;
-  a.chunk_rows = p.chunk_rows;
+  a.attend_warps = p.attend_warps;
   a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(p.d)));
   return zr::launch_step(p, a, stream, ev_start, ev_stop);
 }

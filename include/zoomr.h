@@ -179,8 +179,8 @@ ZR_API zr_status zr_decode_attend_static(zr_plan_t plan, const void* q, const vo
 /*
  * zr_get_device_error -- synchronize `stream`, then read and clear the sticky
  * device error word of `workspace` into *err_code (0 = none; bit 1 = a physical
- * block id outside the pool; bit 2 = a unit needed more split slots than the
- * plan bound). Returns ZR_EDEVICE if the word was non-zero, ZR_OK otherwise.
+ * block id outside the pool). Returns ZR_EDEVICE if the word was non-zero, ZR_OK
+ * otherwise.
  */
 ZR_API zr_status zr_get_device_error(zr_plan_t plan, void* workspace, void* stream, int32_t* err_code);
 

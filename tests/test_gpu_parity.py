@@ -106,6 +106,8 @@ EDGE = {
     "group16_cuda_cores": dict(num_q_heads=16, num_kv_heads=1),
     "ragged_batch": dict(batch=5, seq_len=None, seq_len_range=(1, 700), topk=None, topk_range=(0, 6)),
     "shared_prefix": dict(batch=4, seq_len=None, seq_len_range=(300, 900), shared_prefix_tokens=256),
+    "many_segments": dict(seq_len=3000, seg_len_range=(4, 8), topk=40, window=50),  # n ~ 500 > one per thread
+    "very_many_segments": dict(batch=1, seq_len=4000, seg_len_range=(2, 6), topk=300, window=9),  # n ~ 1000
 }
 
 

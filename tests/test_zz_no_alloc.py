@@ -53,9 +53,10 @@ def test_static_scratch_matches_the_workspace_entry_point_twice(cfg):
 
 
 def test_plan_over_the_static_limit_is_refused():
-    # 6 sequences x 8 KV heads, every segment selected over 64K tokens: ~24 MiB of split partials
-    spec = W.small_spec(dtype="bf16", head_dim=128, batch=6, num_q_heads=32, num_kv_heads=8, seq_len=65536,
-                        seg_len_range=(512, 1024), topk=10_000, window=0)
+    # 32 sequences x 8 KV heads x 4096 two-token segments, all selected: the per-unit range,
+    # prefix, selection and summary lists alone take ~21 MB of workspace
+    spec = W.small_spec(dtype="bf16", head_dim=128, batch=32, num_q_heads=32, num_kv_heads=8, seq_len=8192,
+                        seg_len_range=(2, 2), topk=10_000, window=0)
     st = W.make_structure(spec)
     plan = Z.DecodePlan(batch=st.batch, num_q_heads=32, num_kv_heads=8, head_dim=128, num_blocks=st.num_blocks,
                         max_blocks_per_seq=st.max_blocks_per_seq, window=0, dtype="bf16", seq_lens=st.seq_lens,
