@@ -545,9 +545,13 @@ __device__ void build_row_table(const StepArgs& a, int b, int g, int u, int4 inf
   const int tok_end = min(r0 + n, n_tok);
   for (int base = 0; base < nr && r0 < tok_end; base += 32) {
     const int i = base + lane;
-    const int cs = i < nr ? cum[i] : 0x7fffffff;
-    const int ce = i < nr ? cum[i + 1] : 0x7fffffff;
-    const int st = i < nr ? rg[2 * i] : 0;
+    // read within the unit's arrays whatever nr is, then mask: the loads need not wait for info
+    const bool in_region = i <= a.k_max;
+    const int cs_raw = in_region ? cum[i] : 0, ce_raw = in_region ? cum[i + 1] : 0;
+    const int st_raw = in_region ? rg[2 * i] : 0;
+    const int cs = i < nr ? cs_raw : 0x7fffffff;
+    const int ce = i < nr ? ce_raw : 0x7fffffff;
+    const int st = i < nr ? st_raw : 0;
     unsigned m = __ballot_sync(kFull, i < nr && ce > r0 && cs < tok_end);
     while (m) {
       const int l = __ffs(m) - 1;
@@ -929,9 +933,11 @@ __global__ void __launch_bounds__(kAttendWarps * 32) zr_attend_fma_kernel(StepAr
 }
 
 // ------------------------------------------------------------------ merge
-// One warp per (sequence, query head, 32-wide slice of d). Lane k sums the unit's partials
-// k, k + 32, ... over the slice with weights 2^(m_k - M); a transposed warp reduction then
-// leaves the total of component j in lane j.
+// One warp per (sequence, query head, 32-wide slice of d); lane j owns component j of the slice.
+// The unit's partials are taken 32 at a time: lane k loads partial k's (m, l) while every lane
+// loads its component of all 32 partial rows (all independent loads, one round trip); then each
+// partial's weight 2^(m_k - M) is broadcast from lane k and accumulated. A running maximum keeps
+// the weights bounded when a unit has more than 32 partials.
 template <int D>
 __global__ void __launch_bounds__(kAttendWarps * 32) zr_merge_kernel(StepArgs a) {
   constexpr int NDC = D / 32;
@@ -947,41 +953,32 @@ __global__ void __launch_bounds__(kAttendWarps * 32) zr_merge_kernel(StepArgs a)
   const int2 mi = a.merge_info[u];
   const size_t first = static_cast<size_t>(u) + mi.x;
   const int cnt = mi.y;
-  float M = -INFINITY;
-  for (int k = lane; k < cnt; k += 32) M = fmaxf(M, a.part_ml[(first + k) * G + hh].x);
+  float M = -INFINITY, Ls = 0.f, acc = 0.f;
+  for (int c0 = 0; c0 < cnt; c0 += 32) {
+    const int n = min(32, cnt - c0);
+    float2 ml = make_float2(-INFINITY, 0.f);
+    if (lane < n) ml = a.part_ml[(first + c0 + lane) * G + hh];
+    float v[32];
+    const float* src = a.part_o + ((first + c0) * G + hh) * D + 32 * dc + lane;
 #pragma unroll
-  for (int o2 = 16; o2 > 0; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o2));
-  float acc[32];
+    for (int k = 0; k < 32; ++k) v[k] = k < n ? src[static_cast<size_t>(k) * G * D] : 0.f;
+    float mc = ml.x;
 #pragma unroll
-  for (int j = 0; j < 32; ++j) acc[j] = 0.f;
-  float Ls = 0.f;
-  for (int k = lane; k < cnt; k += 32) {
-    const float2 ml = a.part_ml[(first + k) * G + hh];
-    const float wk = fast_exp2(ml.x - M);
-    Ls = fmaf(ml.y, wk, Ls);
-    const float4* src = reinterpret_cast<const float4*>(a.part_o + ((first + k) * G + hh) * D + 32 * dc);
+    for (int o2 = 16; o2 > 0; o2 >>= 1) mc = fmaxf(mc, __shfl_xor_sync(kFull, mc, o2));
+    const float Mn = fmaxf(M, mc);
+    const float rescale = fast_exp2(M - Mn);  // 0 on the first batch (M = -inf)
+    acc *= rescale;
+    Ls *= rescale;
+    M = Mn;
+    const float wk = lane < n ? fast_exp2(ml.x - M) : 0.f;
+    float lsum = ml.y * wk;
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const float4 v = src[q];
-      acc[4 * q + 0] = fmaf(wk, v.x, acc[4 * q + 0]);
-      acc[4 * q + 1] = fmaf(wk, v.y, acc[4 * q + 1]);
-      acc[4 * q + 2] = fmaf(wk, v.z, acc[4 * q + 2]);
-      acc[4 * q + 3] = fmaf(wk, v.w, acc[4 * q + 3]);
-    }
+    for (int o2 = 16; o2 > 0; o2 >>= 1) lsum += __shfl_xor_sync(kFull, lsum, o2);
+    Ls += lsum;
+#pragma unroll
+    for (int k = 0; k < 32; ++k) acc = fmaf(__shfl_sync(kFull, wk, k), v[k], acc);
   }
-#pragma unroll
-  for (int o2 = 16; o2 > 0; o2 >>= 1) Ls += __shfl_xor_sync(kFull, Ls, o2);
-#pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) {
-    const bool upper = (lane & off) != 0;
-#pragma unroll
-    for (int i = 0; i < off; ++i) {
-      const float send = upper ? acc[i] : acc[i + off];
-      const float keep = upper ? acc[i + off] : acc[i];
-      acc[i] = keep + __shfl_xor_sync(kFull, send, off);
-    }
-  }
-  a.out[(static_cast<size_t>(b) * a.Hq + h) * D + 32 * dc + lane] = acc[0] / Ls;
+  a.out[(static_cast<size_t>(b) * a.Hq + h) * D + 32 * dc + lane] = acc / Ls;
 }
 
 // ------------------------------------------------------------------ launch
@@ -1036,7 +1033,10 @@ zr_status configure_for(Plan& p, int64_t useful_warps) {
     cudaGetLastError();
     return ZR_ECUDA;
   }
-  int64_t ctas = static_cast<int64_t>(sms) * (occ > 0 ? occ : 1);
+#ifndef ZR_ATTEND_WAVES
+#define ZR_ATTEND_WAVES 1
+#endif
+  int64_t ctas = static_cast<int64_t>(sms) * (occ > 0 ? occ : 1) * ZR_ATTEND_WAVES;
   ctas = std::min<int64_t>(ctas, (useful_warps + kAttendWarps - 1) / kAttendWarps);
   p.attend_ctas = static_cast<int>(std::max<int64_t>(ctas, 1));
   p.attend_warps = p.attend_ctas * kAttendWarps;
