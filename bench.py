@@ -111,8 +111,8 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------- inputs
-def make_inputs(device, layers=None):
-    spec = W.WORKLOADS[WORKLOAD_ID]
+def make_inputs(device, workload=WORKLOAD_ID, layers=None):
+    spec = W.WORKLOADS[workload]
     st = W.make_structure(spec)
     nl = spec.layers if layers is None else layers
     lts = [W.make_layer(st, l, device) for l in range(nl)]
@@ -123,7 +123,7 @@ def config_dict(spec, extra=None):
     d = {"workload": spec.name, "batch": spec.batch, "seq_len": spec.seq_len, "layers": spec.layers,
          "q_heads": spec.num_q_heads, "kv_heads": spec.num_kv_heads, "head_dim": spec.head_dim,
          "top_k": spec.topk, "window": spec.window, "segment_len": list(spec.seg_len_range), "block_size": 16,
-         "l2": "inputs exceed L2 (each step reads ~5.1 GB of K/V; no flush)"}
+         "l2": "inputs exceed L2 (each step reads ~4.7 GB of K/V; no flush)"}
     if extra:
         d.update(extra)
     return d
@@ -190,7 +190,7 @@ def run_reference(args):
     world, rank, local = dist_setup(args.gpus)
     if rank != 0:
         return 0
-    spec = W.WORKLOADS[WORKLOAD_ID]
+    spec = W.WORKLOADS[args.workload]
     st = W.make_structure(spec)
     device = "cuda" if torch.cuda.is_available() else "cpu"
     lt = W.make_layer(st, 0, device)
@@ -230,7 +230,7 @@ def run_zoomr(args):
     barrier(world)
     Z.load()
     dev = torch.device("cuda", torch.cuda.current_device())
-    spec, st, lts = make_inputs(dev)
+    spec, st, lts = make_inputs(dev, args.workload)
     L = len(lts)
     plan = Z.DecodePlan.from_structure(st, device=dev)
     bt = torch.from_numpy(st.block_tables.astype(np.int32)).to(dev)
@@ -240,6 +240,7 @@ def run_zoomr(args):
     # Algorithmic bytes of each layer's attend launch (from that layer's selection).
     dbg = plan.new_debug_outputs()
     attend_bytes, select_bytes, tok_total = [], 0, 0
+    eb = 2 if spec.dtype == "bf16" else 4  # element bytes of q, K/V and summaries
     for l, lt in enumerate(lts):
         plan.run(lt.q, lt.k_pool, lt.v_pool, bt, lt.sum_k, lt.sum_v, outs[l], dbg)
         _, rng, nr = (x.cpu().numpy() for x in dbg)
@@ -251,8 +252,8 @@ def run_zoomr(args):
                 r = rng[b, g, :nr[b, g]]
                 ntok = A.ranges_token_count(r)
                 tok_total += ntok
-                tot += A.attend_bytes_per_unit(ntok, n_b - k_b, A.ranges_block_count(r), G, spec.head_dim, 2)
-                select_bytes += A.select_bytes_per_unit(n_b, G, spec.head_dim, 2)
+                tot += A.attend_bytes_per_unit(ntok, n_b - k_b, A.ranges_block_count(r), G, spec.head_dim, eb)
+                select_bytes += A.select_bytes_per_unit(n_b, G, spec.head_dim, eb)
         attend_bytes.append(tot)
     torch.cuda.synchronize()
     assert plan.device_error() == 0
@@ -352,17 +353,22 @@ def run_zoomr(args):
 
     peak, peak_kind = read_peak()
     achieved = attend_bytes_avg / (attend_ms * 1e-3) / 1e9
-    traffic = read_traffic()
+    traffic = read_traffic() if args.workload == WORKLOAD_ID else None
+    mma = spec.dtype == "bf16" and G <= 8
+    kernel = f"zr_attend_mma_kernel<{spec.head_dim}>" if mma else \
+        f"zr_attend_fma_kernel<{'bf16' if spec.dtype == 'bf16' else 'float'}, {spec.head_dim}>"
+    l2 = (f"inputs exceed L2 (each step reads ~{step_bytes / 1e9:.2f} GB of K/V; no flush)" if step_bytes > 129e6 else
+          f"inputs fit in L2 (each step reads ~{step_bytes / 1e6:.1f} MB; no flush: L2-resident timing)")
     line = {
         "impl": "zoomr", "metric": METRIC, "value": world * 1e3 / ms, "unit": "steps/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "scaling": "weak", "vs_baseline": None, "dtype": spec.dtype,
         "data": "synthetic (seeded N(0,1) K/V, segment-mean summaries + N(0,0.1), queries near segment means)",
-        "config": config_dict(spec, {"graph": not args.no_graph, "replicas_per_gpu": 1}),
+        "config": config_dict(spec, {"graph": not args.no_graph, "replicas_per_gpu": 1, "l2": l2}),
         "hbm_gbs": step_bytes / (ms * 1e-3) / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_kind": f"{peak_kind} copy bandwidth", "traffic": traffic,
-                     "kernel": "zr_attend_mma_kernel<128>", "attend_us": attend_ms * 1e3,
+                     "kernel": kernel, "attend_us": attend_ms * 1e3,
                      "alg_bytes_per_launch": attend_bytes_avg},
         "e2e": {"value": world * 1e3 / e2e_ms, "unit": "steps/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
@@ -377,8 +383,9 @@ def run_zoomr(args):
         units_per_step = L * st.batch * spec.num_kv_heads
         v = n / t / units_per_step
         line["cpu_baseline"] = {"value": v, "unit": "steps/s", "cores": 1, "kind": "oracle",
-                                "sample": f"{n} of the {units_per_step} (layer, sequence, KV head) units of one step "
-                                          f"({t:.1f} s), scaled to a full step"}
+                                "sample": f"{n} (sequence, KV head) unit computations of layer 0 in {t:.1f} s "
+                                          f"(cycling over its {st.batch * spec.num_kv_heads} units); a step is "
+                                          f"{units_per_step} units"}
     if rank == 0:
         print(json.dumps(line), flush=True)
     plan.close()
@@ -395,6 +402,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["zoomr", "reference"], default="zoomr")
+    ap.add_argument("--workload", type=int, default=WORKLOAD_ID, choices=sorted(W.WORKLOADS),
+                    help="seeded workload (default: the 8 x 16K, 32-layer headline step)")
     ap.add_argument("--no-graph", action="store_true", help="launch eagerly instead of replaying CUDA graphs")
     ap.add_argument("--max-graphs", type=int, default=64, help="distinct captured steps (each with its own events)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
