@@ -39,7 +39,6 @@ struct WsLayout {
   size_t cum;         // int32 [U][k_max+2] prefix sums of range lengths
   size_t sumlist;     // int32 [U][n_max] non-selected segments, ascending
   size_t sel;         // int32 [U][k_max] selected segments, ascending
-  size_t merge_info;  // int32 [U][2]: first attend warp of the unit, number of its warps
   size_t part_o;      // float [U + attend_warps][G][d] unnormalised split outputs
   size_t part_ml;     // float [U + attend_warps][G][2] split (max, sum) in log2 units
   size_t total;
@@ -78,7 +77,6 @@ struct StepArgs {
   int32_t* cum;
   int32_t* sumlist;
   int32_t* sel;
-  int2* merge_info;
   float* part_o;
   float2* part_ml;
   int B, Hq, Hkv, G, window, num_blocks, max_blocks, k_max, n_max, attend_warps;

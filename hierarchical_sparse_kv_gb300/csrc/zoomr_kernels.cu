@@ -18,7 +18,9 @@
 //           unit's partials into the fp32 output.
 //
 // Launches are chained with programmatic dependent launch: every kernel waits
-// (griddepcontrol.wait) for its predecessor before touching the workspace.
+// (griddepcontrol.wait) for its predecessor before it reads what that one writes.
+// The attend kernel releases its dependents only after its own wait, so the merge
+// kernel may read the select kernel's unit sizes before it waits on the attend.
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -578,8 +580,7 @@ __device__ void build_row_table(const StepArgs& a, int b, int g, int u, int4 inf
 }
 
 // One warp's walk over its rows: for every unit its range touches, begin_unit, run over row
-// tables of up to kChunkRows rows, and end_unit into slot u + w. The warp holding a unit's first
-// row records which warps hold the unit, for the merge.
+// tables of up to kChunkRows rows, and end_unit into slot u + w.
 template <class Worker>
 __device__ void attend_balanced(const StepArgs& a, Worker& wk, uint32_t* tab, int warp, int lane) {
   const int w = blockIdx.x * kAttendWarps + warp;
@@ -594,10 +595,6 @@ __device__ void attend_balanced(const StepArgs& a, Worker& wk, uint32_t* tab, in
     const int4 info = a.unit_info[u];
     const long long end = min(wr.e, P + Ru);
     const int lo = static_cast<int>(pos - P), hi = static_cast<int>(end - P);
-    if (lo == 0 && lane == 0) {
-      const long long w_last = ((P + Ru) * wr.N + wr.R - 1) / wr.R - 1;  // warp holding the unit's last row
-      a.merge_info[u] = make_int2(w, static_cast<int>(w_last - w + 1));
-    }
     wk.begin_unit(a, b, g, lane);
     for (int r0 = lo; r0 < hi; r0 += kChunkRows) {
       const int nrow = min(kChunkRows, hi - r0);
@@ -839,8 +836,8 @@ __global__ void __launch_bounds__(kAttendWarps * 32, 3) zr_attend_mma_kernel(Ste
   extern __shared__ __align__(16) unsigned char attend_smem[];
   __shared__ uint32_t rowtab[kAttendWarps][kChunkRows];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();  // after the wait: the merge kernel may read the select kernel's unit sizes at once
   MmaWorker<D> wk;
   wk.ring = static_cast<uint32_t>(__cvta_generic_to_shared(attend_smem)) + warp * kStages * MmaWorker<D>::kStageBytes;
   const int chunk_off = (lane % (D / 8)) * 16;
@@ -926,8 +923,8 @@ template <typename T, int D>
 __global__ void __launch_bounds__(kAttendWarps * 32) zr_attend_fma_kernel(StepArgs a) {
   __shared__ uint32_t rowtab[kAttendWarps][kChunkRows];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();  // after the wait: the merge kernel may read the select kernel's unit sizes at once
   FmaWorker<T, D> wk;
   attend_balanced(a, wk, rowtab[warp], warp, lane);
 }
@@ -949,10 +946,31 @@ __global__ void __launch_bounds__(kAttendWarps * 32) zr_merge_kernel(StepArgs a)
   const int b = bh / a.Hq, h = bh - b * a.Hq;
   const int G = a.G, g = h / G, hh = h - g * G;
   const int u = b * a.Hkv + g;
+  // The warps holding unit u follow from the select kernel's unit sizes alone. This kernel is
+  // launched only after every attend CTA has passed its own wait on the select kernel, so those
+  // sizes are complete here, before the wait on the attend kernel.
+  const int U = a.B * a.Hkv;
+  long long R = 0, Pu = 0;
+  int Ru = 0;
+  for (int base = 0; base < U; base += 32) {
+    const int uu = base + lane;
+    const int r = uu < U ? unit_rows(a, uu) : 0;
+    R += r;
+    if (uu < u) Pu += r;
+    if (uu == u) Ru = r;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    R += __shfl_xor_sync(kFull, R, o);
+    Pu += __shfl_xor_sync(kFull, Pu, o);
+    Ru += __shfl_xor_sync(kFull, Ru, o);
+  }
+  const long long N = min(static_cast<long long>(a.attend_warps), R);
+  // warp holding global row r of the even split: ceil((r + 1) N / R) - 1
+  const long long wf = ((Pu + 1) * N + R - 1) / R - 1, wl = ((Pu + Ru) * N + R - 1) / R - 1;
+  const size_t first = static_cast<size_t>(u) + wf;
+  const int cnt = static_cast<int>(wl - wf + 1);
   pdl_wait();
-  const int2 mi = a.merge_info[u];
-  const size_t first = static_cast<size_t>(u) + mi.x;
-  const int cnt = mi.y;
   float M = -INFINITY, Ls = 0.f, acc = 0.f;
   for (int c0 = 0; c0 < cnt; c0 += 32) {
     const int n = min(32, cnt - c0);

@@ -135,7 +135,6 @@ zr_status zr_plan(const zr_config* cfg, const int32_t* seq_lens, const int32_t* 
   p.ws.cum = take(U * (p.k_max + 2) * sizeof(int32_t));
   p.ws.sumlist = take(U * p.n_max * sizeof(int32_t));
   p.ws.sel = take(U * p.k_max * sizeof(int32_t));
-  p.ws.merge_info = take(U * 2 * sizeof(int32_t));
   p.ws.part_o = take(slots * p.G * p.d * sizeof(float));
   p.ws.part_ml = take(slots * p.G * 2 * sizeof(float));
   p.ws.total = off;
@@ -217,7 +216,6 @@ zr_status decode_into(zr_plan_t plan, void* workspace, const void* q, const void
   a.cum = reinterpret_cast<int32_t*>(ws + p.ws.cum);
   a.sumlist = reinterpret_cast<int32_t*>(ws + p.ws.sumlist);
   a.sel = reinterpret_cast<int32_t*>(ws + p.ws.sel);
-  a.merge_info = reinterpret_cast<int2*>(ws + p.ws.merge_info);
   a.part_o = reinterpret_cast<float*>(ws + p.ws.part_o);
   a.part_ml = reinterpret_cast<float2*>(ws + p.ws.part_ml);
   a.B = p.B;
