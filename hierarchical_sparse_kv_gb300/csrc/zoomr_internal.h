@@ -17,7 +17,7 @@ constexpr int kChunkRows = 256;       // rows of one attend warp's row table (a 
 #define ZR_ATTEND_WARPS 4
 #endif
 constexpr int kAttendWarps = ZR_ATTEND_WARPS;  // warps per attend CTA
-constexpr int kSelectThreads = 256;   // threads per select CTA
+constexpr int kSelectThreads = 512;   // threads per select CTA
 constexpr uint32_t kSummaryFlag = 0x80000000u;  // row id refers to the summary tensors
 constexpr uint32_t kInvalidRow = 0xFFFFFFFFu;   // masked row (past the chunk end, or a bad block id)
 
@@ -35,6 +35,7 @@ struct DeviceMeta {
 struct WsLayout {
   size_t err;         // int32 sticky error word
   size_t unit_info;   // int32 [U][4]: n_ranges, n_tok, n_sum, 0
+  size_t unit_rows;   // int32 [U]: n_tok + n_sum, the rows the unit gathers
   size_t ranges;      // int32 [U][k_max+1][2]
   size_t cum;         // int32 [U][k_max+2] prefix sums of range lengths
   size_t sumlist;     // int32 [U][n_max] non-selected segments, ascending
@@ -54,6 +55,7 @@ struct Plan {
   void* d_meta_base;
   DeviceMeta meta;
   WsLayout ws;
+  int merge_parts;     // merge layout: 1 lanes over partials, 0 lanes over components
   size_t select_smem;  // dynamic shared memory of the select kernel
   size_t attend_smem;  // dynamic shared memory of the attend kernel
 };
@@ -73,6 +75,7 @@ struct StepArgs {
   DeviceMeta meta;
   int32_t* err;
   int4* unit_info;
+  int32_t* unit_rows;
   int32_t* ranges;
   int32_t* cum;
   int32_t* sumlist;

@@ -29,6 +29,7 @@
 #include <cstdint>
 #include <cstdio>
 #include <cstdlib>
+#include <cstring>
 
 #include "zoomr_internal.h"
 
@@ -359,6 +360,7 @@ __global__ void __launch_bounds__(kSelectThreads) zr_select_kernel(StepArgs a) {
       if (lane == 0) {
         cum[nr] = carry;
         a.unit_info[u] = make_int4(nr, carry, n - k, 0);
+        a.unit_rows[u] = carry + n - k;
         if (a.nranges_out) a.nranges_out[u] = nr;
       }
     }
@@ -439,6 +441,7 @@ __global__ void __launch_bounds__(kSelectThreads) zr_select_kernel(StepArgs a) {
     if (tid == 0) {
       cum[nr] = n_tok;
       a.unit_info[u] = make_int4(nr, n_tok, n - k, 0);
+      a.unit_rows[u] = n_tok + n - k;
       if (a.nranges_out) a.nranges_out[u] = nr;
     }
   }
@@ -456,10 +459,7 @@ __global__ void __launch_bounds__(kSelectThreads) zr_select_kernel(StepArgs a) {
 // range touches, into slot u + w: the (unit, warp) pairs that intersect form a monotone
 // staircase, so u + w is unique and the slots never exceed U + N.
 
-__device__ __forceinline__ int unit_rows(const StepArgs& a, int u) {
-  const int4 i = a.unit_info[u];
-  return i.y + i.z;
-}
+__device__ __forceinline__ int unit_rows(const StepArgs& a, int u) { return a.unit_rows[u]; }
 
 struct WarpRange {
   long long s, e;  // this warp's global rows [s, e)
@@ -930,13 +930,16 @@ __global__ void __launch_bounds__(kAttendWarps * 32) zr_attend_fma_kernel(StepAr
 }
 
 // ------------------------------------------------------------------ merge
-// One warp per (sequence, query head, 32-wide slice of d); lane j owns component j of the slice.
+// Two layouts of the same log-sum-exp combination; zr_plan picks one (configure_for).
+//
+// zr_merge_comp_kernel: one warp per (sequence, query head, 32-wide slice of d); lane j owns
+// component j of the slice.
 // The unit's partials are taken 32 at a time: lane k loads partial k's (m, l) while every lane
 // loads its component of all 32 partial rows (all independent loads, one round trip); then each
 // partial's weight 2^(m_k - M) is broadcast from lane k and accumulated. A running maximum keeps
 // the weights bounded when a unit has more than 32 partials.
 template <int D>
-__global__ void __launch_bounds__(kAttendWarps * 32) zr_merge_kernel(StepArgs a) {
+__global__ void __launch_bounds__(kAttendWarps * 32) zr_merge_comp_kernel(StepArgs a) {
   constexpr int NDC = D / 32;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int w = blockIdx.x * kAttendWarps + warp;
@@ -999,6 +1002,112 @@ __global__ void __launch_bounds__(kAttendWarps * 32) zr_merge_kernel(StepArgs a)
   a.out[(static_cast<size_t>(b) * a.Hq + h) * D + 32 * dc + lane] = acc / Ls;
 }
 
+// zr_merge_part_kernel: one warp per (sequence, query head, kMergeComp-wide slice of d), four
+// slices of one head per CTA. Lane j takes the unit's partials
+// j, j + 32, ... (kMergeBatch per lane per memory round trip, so up to 32 * kMergeBatch partials
+// arrive in one trip) and folds them into its own running (m, l, o) with log-sum-exp weights; the
+// 32 lane states are then combined by a butterfly (max, rescale, sum). Each partial row slice is
+// 32 contiguous bytes, a whole sector. The CTA's first warp finds which attend warps hold the unit.
+constexpr int kMergeComp = 8;
+constexpr int kMergeBatch = 4;
+constexpr int kMergeWarps = 4;
+
+template <int D>
+__global__ void __launch_bounds__(kMergeWarps * 32, 8) zr_merge_part_kernel(StepArgs a) {
+  constexpr int NC = D / kMergeComp;
+  static_assert(NC % kMergeWarps == 0, "a CTA's slices belong to one query head");
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int w = blockIdx.x * kMergeWarps + warp;
+  const int cs = w % NC, bh = w / NC;
+  const int b = bh / a.Hq, h = bh - b * a.Hq;
+  const int G = a.G, g = h / G, hh = h - g * G;
+  const int u = b * a.Hkv + g;
+  __shared__ long long s_first;
+  __shared__ int s_cnt;
+  pdl_trigger();
+  // The warps holding unit u follow from the select kernel's unit sizes alone. This kernel is
+  // launched only after every attend CTA has passed its own wait on the select kernel, so those
+  // sizes are complete here, before the wait on the attend kernel.
+  if (warp == 0) {
+    const int U = a.B * a.Hkv;
+    long long R = 0, Pu = 0;
+    int Ru = 0;
+    for (int base = 0; base < U; base += 32) {
+      const int uu = base + lane;
+      const int r = uu < U ? unit_rows(a, uu) : 0;
+      R += r;
+      if (uu < u) Pu += r;
+      if (uu == u) Ru = r;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      R += __shfl_xor_sync(kFull, R, o);
+      Pu += __shfl_xor_sync(kFull, Pu, o);
+      Ru += __shfl_xor_sync(kFull, Ru, o);
+    }
+    const long long N = min(static_cast<long long>(a.attend_warps), R);
+    // warp holding global row r of the even split: ceil((r + 1) N / R) - 1
+    const long long wf = ((Pu + 1) * N + R - 1) / R - 1, wl = ((Pu + Ru) * N + R - 1) / R - 1;
+    if (lane == 0) {
+      s_first = u + wf;
+      s_cnt = static_cast<int>(wl - wf + 1);
+    }
+  }
+  __syncthreads();
+  const size_t first = static_cast<size_t>(s_first);
+  const int cnt = s_cnt;
+  pdl_wait();
+  float m = -INFINITY, l = 0.f, acc[kMergeComp];
+#pragma unroll
+  for (int c = 0; c < kMergeComp; ++c) acc[c] = 0.f;
+  for (int p0 = 0; p0 < cnt; p0 += 32 * kMergeBatch) {
+    float2 ml[kMergeBatch];
+    float4 o0[kMergeBatch], o1[kMergeBatch];
+#pragma unroll
+    for (int j = 0; j < kMergeBatch; ++j) {
+      const int p = p0 + 32 * j + lane;
+      if (p < cnt) {
+        const size_t row = (first + p) * G + hh;
+        ml[j] = a.part_ml[row];
+        const float4* src = reinterpret_cast<const float4*>(a.part_o + row * D + kMergeComp * cs);
+        o0[j] = src[0];
+        o1[j] = src[1];
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kMergeBatch; ++j) {
+      if (p0 + 32 * j + lane < cnt) {
+        const float mn = fmaxf(m, ml[j].x);
+        const float sc = fast_exp2(m - mn), wt = fast_exp2(ml[j].x - mn);  // sc = 0 while m = -inf
+        l = fmaf(l, sc, ml[j].y * wt);
+        const float v[kMergeComp] = {o0[j].x, o0[j].y, o0[j].z, o0[j].w, o1[j].x, o1[j].y, o1[j].z, o1[j].w};
+#pragma unroll
+        for (int c = 0; c < kMergeComp; ++c) acc[c] = fmaf(acc[c], sc, wt * v[c]);
+        m = mn;
+      }
+    }
+  }
+  float M = m;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+  const float s = fast_exp2(m - M);  // 0 for lanes that took no partial
+  l *= s;
+#pragma unroll
+  for (int c = 0; c < kMergeComp; ++c) acc[c] *= s;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    l += __shfl_xor_sync(kFull, l, o);
+#pragma unroll
+    for (int c = 0; c < kMergeComp; ++c) acc[c] += __shfl_xor_sync(kFull, acc[c], o);
+  }
+  if (lane == 0) {
+    const float inv = 1.f / l;
+    float4* dst = reinterpret_cast<float4*>(a.out + (static_cast<size_t>(b) * a.Hq + h) * D + kMergeComp * cs);
+    dst[0] = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
+    dst[1] = make_float4(acc[4] * inv, acc[5] * inv, acc[6] * inv, acc[7] * inv);
+  }
+}
+
 // ------------------------------------------------------------------ launch
 template <typename Kern>
 cudaError_t launch_pdl(Kern kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t s, const StepArgs& a) {
@@ -1058,11 +1167,22 @@ zr_status configure_for(Plan& p, int64_t useful_warps) {
   ctas = std::min<int64_t>(ctas, (useful_warps + kAttendWarps - 1) / kAttendWarps);
   p.attend_ctas = static_cast<int>(std::max<int64_t>(ctas, 1));
   p.attend_warps = p.attend_ctas * kAttendWarps;
+  // Merge layout (both measured on GB300): lanes over partials when a unit has few partials on
+  // average (at most 64) and its warps fit one resident wave (64 registers: 32 warps per SM);
+  // otherwise lanes over components, which is faster with many partials per unit or many heads.
+  const int64_t units = static_cast<int64_t>(p.B) * p.Hkv;
+  const int64_t part_warps = static_cast<int64_t>(p.B) * p.Hq * (D / kMergeComp);
+  p.merge_parts = p.attend_warps <= 64 * units && part_warps <= static_cast<int64_t>(sms) * 32;
+  if (const char* m = std::getenv("ZOOMR_MERGE")) {  // pin the layout (used by the tests to cover both)
+    if (std::strcmp(m, "parts") == 0) p.merge_parts = 1;
+    if (std::strcmp(m, "comp") == 0) p.merge_parts = 0;
+  }
   // One shared-memory carveout for all three kernels: a kernel whose preferred L1/shared split
   // differs from the previous one's makes the SM drain and reconfigure between them.
   const int carve = cudaSharedmemCarveoutMaxShared;
   cudaFuncSetAttribute(zr_select_kernel<T, D>, cudaFuncAttributePreferredSharedMemoryCarveout, carve);
-  cudaFuncSetAttribute(zr_merge_kernel<D>, cudaFuncAttributePreferredSharedMemoryCarveout, carve);
+  cudaFuncSetAttribute(zr_merge_comp_kernel<D>, cudaFuncAttributePreferredSharedMemoryCarveout, carve);
+  cudaFuncSetAttribute(zr_merge_part_kernel<D>, cudaFuncAttributePreferredSharedMemoryCarveout, carve);
   cudaFuncSetAttribute(zr_attend_fma_kernel<T, D>, cudaFuncAttributePreferredSharedMemoryCarveout, carve);
   if constexpr (sizeof(T) == 2)
     cudaFuncSetAttribute(zr_attend_mma_kernel<D>, cudaFuncAttributePreferredSharedMemoryCarveout, carve);
@@ -1105,8 +1225,13 @@ cudaError_t launch_for(const Plan& p, const StepArgs& a, cudaStream_t s, cudaEve
   }
   if (e != cudaSuccess) return report("attend launch", e), e;
   if (ev1 && (e = record_event(ev1, s)) != cudaSuccess) return report("stop event record", e), e;
-  const dim3 grid_merge((p.B * p.Hq * (D / 32) + kAttendWarps - 1) / kAttendWarps);
-  e = launch_pdl(zr_merge_kernel<D>, grid_merge, block, 0, s, a);
+  if (p.merge_parts) {
+    e = launch_pdl(zr_merge_part_kernel<D>, dim3(p.B * p.Hq * (D / kMergeComp) / kMergeWarps),
+                   dim3(kMergeWarps * 32), 0, s, a);
+  } else {
+    const dim3 grid_merge((p.B * p.Hq * (D / 32) + kAttendWarps - 1) / kAttendWarps);
+    e = launch_pdl(zr_merge_comp_kernel<D>, grid_merge, block, 0, s, a);
+  }
   if (e != cudaSuccess) report("merge launch", e);
   return e;
 }

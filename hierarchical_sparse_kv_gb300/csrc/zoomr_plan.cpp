@@ -131,6 +131,7 @@ zr_status zr_plan(const zr_config* cfg, const int32_t* seq_lens, const int32_t* 
   };
   p.ws.err = take(sizeof(int32_t));
   p.ws.unit_info = take(U * 4 * sizeof(int32_t));
+  p.ws.unit_rows = take(U * sizeof(int32_t));
   p.ws.ranges = take(U * (p.k_max + 1) * 2 * sizeof(int32_t));
   p.ws.cum = take(U * (p.k_max + 2) * sizeof(int32_t));
   p.ws.sumlist = take(U * p.n_max * sizeof(int32_t));
@@ -212,6 +213,7 @@ zr_status decode_into(zr_plan_t plan, void* workspace, const void* q, const void
   a.meta = p.meta;
   a.err = reinterpret_cast<int32_t*>(ws + p.ws.err);
   a.unit_info = reinterpret_cast<int4*>(ws + p.ws.unit_info);
+  a.unit_rows = reinterpret_cast<int32_t*>(ws + p.ws.unit_rows);
   a.ranges = reinterpret_cast<int32_t*>(ws + p.ws.ranges);
   a.cum = reinterpret_cast<int32_t*>(ws + p.ws.cum);
   a.sumlist = reinterpret_cast<int32_t*>(ws + p.ws.sumlist);

@@ -121,6 +121,18 @@ def test_edge_cases(name, dtype, head_dim):
     C.parity(st, lt)
 
 
+@pytest.mark.parametrize("merge", ["parts", "comp"])
+@pytest.mark.parametrize("name", ["ragged_batch", "many_chunks_ragged_tail", "group8_mqa", "one_token", "shared_prefix"])
+def test_both_merge_layouts(name, merge, monkeypatch):
+    """The plan picks one of two merge layouts by shape; pin each in turn on the same inputs."""
+    monkeypatch.setenv("ZOOMR_MERGE", merge)
+    kw = dict(dtype="bf16", head_dim=128, batch=2, num_q_heads=8, num_kv_heads=2, seq_len=300,
+              seg_len_range=(10, 60), topk=3, window=20, seed=zlib.crc32(name.encode()) % 1000)
+    kw.update(EDGE[name])
+    st, lt = _layer(W.small_spec(**kw))
+    C.parity(st, lt)
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_unowned_pool_rows_are_never_read(dtype):
     """NaN in every pool row no sequence owns (tails of last blocks, spare blocks)."""
