@@ -234,7 +234,13 @@ def run_zoomr(args):
     L = len(lts)
     plan = Z.DecodePlan.from_structure(st, device=dev)
     bt = torch.from_numpy(st.block_tables.astype(np.int32)).to(dev)
-    outs = [torch.empty(lt.q.shape, dtype=torch.float32, device=dev) for lt in lts]
+    # every layer's queries and outputs are slices of one buffer each, so the end-to-end leg moves a
+    # step's inputs and results with one copy per direction
+    q_all = torch.stack([lt.q for lt in lts])
+    for l, lt in enumerate(lts):
+        lt.q = q_all[l]
+    out_all = torch.empty((len(lts),) + tuple(q_all.shape[1:]), dtype=torch.float32, device=dev)
+    outs = [out_all[l] for l in range(len(lts))]
     G = spec.num_q_heads // spec.num_kv_heads
 
     # Algorithmic bytes of each layer's attend launch (from that layer's selection).
@@ -266,18 +272,33 @@ def run_zoomr(args):
     # their programmatic-dependent-launch overlap, which an event node between kernels would break.
     n_graphs = max(1, min(args.steps, args.max_graphs))
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_graphs)]
+    # Captured step i times layer i mod L in one of three ways (mode i mod 3): 0 the attend launch
+    # alone (an event pair around it, which also breaks its overlap with the select kernel); 1 the
+    # select and attend launches together and 2 the select launch alone, both from an event of our
+    # own before the call, so 1 - 2 is what the attend kernel adds to the step with its launch
+    # overlap intact. Modes 1 and 2 need events that a capture records as graph nodes.
+    try:
+        pev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(n_graphs)]
+    except TypeError:
+        pev = None
+    modes = [i % 3 if pev is not None else 0 for i in range(n_graphs)]
 
     def step(i, s):
         for l, lt in enumerate(lts):
             if i is not None and l == i % L:
-                plan.run_timed(lt.q, lt.k_pool, lt.v_pool, bt, lt.sum_k, lt.sum_v, outs[l], evs[i][0], evs[i][1],
-                               stream=s)
+                m = modes[i]
+                if m > 0:
+                    pev[i].record(s)
+                plan.run_timed(lt.q, lt.k_pool, lt.v_pool, bt, lt.sum_k, lt.sum_v, outs[l],
+                               evs[i][0] if m != 1 else None, evs[i][1] if m != 2 else None, stream=s)
             else:
                 plan.run(lt.q, lt.k_pool, lt.v_pool, bt, lt.sum_k, lt.sum_v, outs[l], stream=s)
 
     for a_, b_ in evs:  # torch creates CUDA events lazily: create them all before any capture
         a_.record(stream)
         b_.record(stream)
+    for e_ in pev or []:
+        e_.record(stream)
     stream.wait_stream(torch.cuda.current_stream())
     graphs = []
     with torch.cuda.stream(stream):
@@ -317,36 +338,40 @@ def run_zoomr(args):
     ms = t_start.elapsed_time(t_stop) / args.steps
     ms = max_over_ranks(ms, world)
     # attend kernel: the timed layer of each capture (its last replay in the timed region)
-    timed = range(min(n_graphs, args.steps))
+    timed = [i for i in range(min(n_graphs, args.steps)) if modes[i] == 0]
     attend_ms_sum = sum(evs[i][0].elapsed_time(evs[i][1]) for i in timed)
     attend_bytes_sum = sum(attend_bytes[i % L] for i in timed)
     attend_ms = attend_ms_sum / len(timed)
     attend_bytes_avg = attend_bytes_sum / len(timed)
+    in_step = None
+    sa = [pev[i].elapsed_time(evs[i][1]) for i in range(min(n_graphs, args.steps)) if modes[i] == 1]
+    so = [pev[i].elapsed_time(evs[i][0]) for i in range(min(n_graphs, args.steps)) if modes[i] == 2]
+    if sa and so:
+        in_step_ms = sum(sa) / len(sa) - sum(so) / len(so)
+        mean_bytes = sum(attend_bytes) / L
+        in_step = {"attend_us": in_step_ms * 1e3, "achieved": mean_bytes / (in_step_ms * 1e-3) / 1e9,
+                   "select_us": sum(so) / len(so) * 1e3, "select_attend_us": sum(sa) / len(sa) * 1e3}
 
-    # e2e through the public API with host buffers: H2D of every layer's queries from pinned
-    # memory, the step, D2H of every layer's output into pinned memory.
-    host_q = [lt.q.cpu().pin_memory() for lt in lts]
-    host_out = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
-    h2d = sum(x.numel() * x.element_size() for x in host_q)
-    d2h = sum(x.numel() * x.element_size() for x in host_out)
+    # e2e through the public API with host buffers: one H2D of all layers' queries from pinned
+    # memory, the step, one D2H of all layers' outputs into pinned memory.
+    host_q = q_all.cpu().pin_memory()
+    host_out = torch.empty(out_all.shape, dtype=out_all.dtype).pin_memory()
+    h2d = host_q.numel() * host_q.element_size()
+    d2h = host_out.numel() * host_out.element_size()
     e2e_steps = max(3, min(args.steps, 50))
     with torch.cuda.stream(stream):
         for _ in range(2):
-            for l, lt in enumerate(lts):
-                lt.q.copy_(host_q[l], non_blocking=True)
+            q_all.copy_(host_q, non_blocking=True)
             step(None, stream)
-            for l in range(L):
-                host_out[l].copy_(outs[l], non_blocking=True)
+            host_out.copy_(out_all, non_blocking=True)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         e0.record(stream)
         for _ in range(e2e_steps):
-            for l, lt in enumerate(lts):
-                lt.q.copy_(host_q[l], non_blocking=True)
+            q_all.copy_(host_q, non_blocking=True)
             step(None, stream)
-            for l in range(L):
-                host_out[l].copy_(outs[l], non_blocking=True)
+            host_out.copy_(out_all, non_blocking=True)
         e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
@@ -369,10 +394,15 @@ def run_zoomr(args):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_kind": f"{peak_kind} copy bandwidth", "traffic": traffic,
                      "kernel": kernel, "attend_us": attend_ms * 1e3,
-                     "alg_bytes_per_launch": attend_bytes_avg},
+                     "alg_bytes_per_launch": attend_bytes_avg,
+                     "timing": "event pair around single attend launches (includes their launch latency)"},
         "e2e": {"value": world * 1e3 / e2e_ms, "unit": "steps/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": 3 * L * args.steps,
+        "attend_in_step": None if in_step is None else dict(
+            in_step, frac=in_step["achieved"] / peak,
+            method="mean(select+attend) - mean(select), events before the call and after attend or select, "
+                   "launch overlap between the two kernels intact"),
         "timing": "CUDA events on the launching stream around the graph replays; the attend kernel is timed with "
                   "an event pair around one layer per captured step, rotating over the layers",
         "clocks": clk,

@@ -248,7 +248,7 @@ zr_status zr_decode_attend(zr_plan_t plan, void* workspace, const void* q, const
 zr_status zr_decode_attend_timed(zr_plan_t plan, void* workspace, const void* q, const void* k_pool,
                                  const void* v_pool, const int32_t* block_tables, const void* sum_k,
                                  const void* sum_v, float* out, void* ev_start, void* ev_stop, void* stream) {
-  if (!ev_start || !ev_stop) return ZR_EINVAL;
+  if (!ev_start && !ev_stop) return ZR_EINVAL;
   return zr::decode_into(plan, workspace, q, k_pool, v_pool, block_tables, sum_k, sum_v, out, nullptr, nullptr,
                        nullptr, stream, ev_start, ev_stop);
 }

@@ -149,16 +149,17 @@ def zr_decode_attend(plan: int, workspace: torch.Tensor, q: torch.Tensor, k_pool
 
 def zr_decode_attend_timed(plan: int, workspace: torch.Tensor, q: torch.Tensor, k_pool: torch.Tensor,
                            v_pool: torch.Tensor, block_tables: torch.Tensor, sum_k: torch.Tensor,
-                           sum_v: torch.Tensor, out: torch.Tensor, ev_start: torch.cuda.Event,
-                           ev_stop: torch.cuda.Event, stream=None) -> None:
+                           sum_v: torch.Tensor, out: torch.Tensor, ev_start: Optional[torch.cuda.Event],
+                           ev_stop: Optional[torch.cuda.Event], stream=None) -> None:
     for ev in (ev_start, ev_stop):
-        if ev.cuda_event == 0:  # torch creates the CUDA event lazily, at its first record
+        if ev is not None and ev.cuda_event == 0:  # torch creates the CUDA event lazily, at its first record
             if torch.cuda.is_current_stream_capturing():
                 raise ValueError("zoomr: record timing events once before using them inside a stream capture")
             ev.record(torch.cuda.current_stream() if stream is None or isinstance(stream, int) else stream)
     st = load().zr_decode_attend_timed(plan, _dev(workspace), _dev(q), _dev(k_pool), _dev(v_pool),
                                        _dev(block_tables), _dev(sum_k), _dev(sum_v), _dev(out),
-                                       ev_start.cuda_event, ev_stop.cuda_event, _stream(stream))
+                                       ev_start.cuda_event if ev_start is not None else None,
+                                       ev_stop.cuda_event if ev_stop is not None else None, _stream(stream))
     if st != ZR_OK:
         raise ZoomrError(st, "zr_decode_attend_timed")
 

@@ -138,11 +138,14 @@ ZR_API zr_status zr_decode_attend(zr_plan_t plan, void* workspace, const void* q
 
 /*
  * zr_decode_attend_timed -- zr_decode_attend without debug outputs that also
- * records two caller-owned CUDA events (cudaEvent_t, created with timing
- * enabled) on `stream`: ev_start right before the gather-attention kernel and
- * ev_stop right after it, so the caller can time that kernel alone. The events
- * are recorded with the "external" flag, so inside a stream capture they become
- * event-record nodes of the graph.
+ * records caller-owned CUDA events (cudaEvent_t, created with timing enabled)
+ * on `stream`: ev_start right before the gather-attention kernel and ev_stop
+ * right after it, so the caller can time that kernel alone. Either may be NULL
+ * (not recorded), not both: with only one, the caller's own event before the
+ * call times the select kernel (ev_start) or the select and gather-attention
+ * kernels with their launch overlap intact (ev_stop). The events are recorded
+ * with the "external" flag, so inside a stream capture they become event-record
+ * nodes of the graph.
  */
 ZR_API zr_status zr_decode_attend_timed(zr_plan_t plan, void* workspace, const void* q, const void* k_pool,
                                  const void* v_pool, const int32_t* block_tables, const void* sum_k,

@@ -197,6 +197,12 @@ def test_repeated_calls_are_deterministic_and_graph_capture_replays():
     plan.run_timed(lt.q, lt.k_pool, lt.v_pool, bt, lt.sum_k, lt.sum_v, c, e0, e1)
     torch.cuda.synchronize()
     assert torch.equal(a, c) and e0.elapsed_time(e1) > 0
+    # either event alone: the one before the attend kernel, or the one after it
+    for ev0, ev1 in ((None, e1), (e0, None)):
+        c.zero_()
+        plan.run_timed(lt.q, lt.k_pool, lt.v_pool, bt, lt.sum_k, lt.sum_v, c, ev0, ev1)
+        torch.cuda.synchronize()
+        assert torch.equal(a, c)
 
 
 def test_out_of_pool_block_id_sets_the_error_word_and_nothing_faults():
