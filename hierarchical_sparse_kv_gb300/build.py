@@ -1,6 +1,6 @@
 """Build the in-tree C-ABI library ``libzoomr.so`` for sm_103a with nvcc.
 
-The two translation units compile in parallel; the CUDA runtime is linked
+The translation units compile in parallel; the CUDA runtime is linked
 statically so that the library loads without a CUDA toolkit on the loader path.
 Run ``python -m hierarchical_sparse_kv_gb300.build`` (or ``__graft_entry__.build()``).
 """
@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libzoomr.so")
-SOURCES = ["zoomr_plan.cpp", "zoomr_kernels.cu", "zoomr_static.cu"]
+SOURCES = ["zoomr_plan.cpp", "zoomr_kernels.cu", "zoomr_static.cu", "zoomr_append.cu"]
 HEADERS = ["zoomr_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -21,7 +21,7 @@ constexpr int kSelectThreads = 512;   // threads per select CTA
 constexpr uint32_t kSummaryFlag = 0x80000000u;  // row id refers to the summary tensors
 constexpr uint32_t kInvalidRow = 0xFFFFFFFFu;   // masked row (past the chunk end, or a bad block id)
 
-enum : int32_t { kErrBadBlock = 1 };
+enum : int32_t { kErrBadBlock = 1, kErrBadIndex = 2 };
 
 // Small device metadata copied from the host at plan time (one allocation).
 struct DeviceMeta {

@@ -66,6 +66,13 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.zr_decode_attend_static.restype = ctypes.c_int
     lib.zr_get_device_error.argtypes = [_P, _P, _P, _I32P]
     lib.zr_get_device_error.restype = ctypes.c_int
+    lib.zr_append_kv.argtypes = [ctypes.POINTER(zr_config)] + [_P] * 8
+    lib.zr_append_kv.restype = ctypes.c_int
+    lib.zr_copy_blocks.argtypes = [ctypes.POINTER(zr_config), _P, ctypes.c_int32, _P, _P, _P, _P]
+    lib.zr_copy_blocks.restype = ctypes.c_int
+    lib.zr_segment_summaries.argtypes = [ctypes.POINTER(zr_config), _P, ctypes.c_int32] + [_P] * 5 + \
+        [ctypes.c_int32, _P, _P]
+    lib.zr_segment_summaries.restype = ctypes.c_int
     lib.zr_free.argtypes = [_P]
     lib.zr_free.restype = None
     lib.zr_status_string.argtypes = [ctypes.c_int]
@@ -186,6 +193,74 @@ def zr_get_device_error(plan: int, workspace: torch.Tensor, stream=None) -> int:
 def zr_free(plan: Optional[int]) -> None:
     if plan:
         load().zr_free(plan)
+
+
+def cache_config(*, batch: int, num_kv_heads: int, head_dim: int, num_blocks: int, max_blocks_per_seq: int,
+                 dtype: str, num_q_heads: int = 0, window: int = 0) -> zr_config:
+    """A zr_config for the append-path calls (they ignore num_q_heads and window)."""
+    return zr_config(batch, num_q_heads, num_kv_heads, head_dim, 16, num_blocks, max_blocks_per_seq, window,
+                     DTYPES[dtype])
+
+
+def _check_cache(cfg: zr_config, k_pool: torch.Tensor, v_pool: torch.Tensor,
+                 block_tables: Optional[torch.Tensor] = None) -> None:
+    """The C ABI cannot see buffer sizes: check the tensors against the config here."""
+    want = (cfg.num_blocks, cfg.num_kv_heads, cfg.block_size, cfg.head_dim)
+    dt = TORCH_DTYPES.get(cfg.dtype)
+    for name, t in (("k_pool", k_pool), ("v_pool", v_pool)):
+        if tuple(t.shape) != want or t.dtype != dt:
+            raise ValueError(f"zoomr: {name} must be {want} {dt}, got {tuple(t.shape)} {t.dtype}")
+    if block_tables is not None and (tuple(block_tables.shape) != (cfg.batch, cfg.max_blocks_per_seq)
+                                     or block_tables.dtype != torch.int32):
+        raise ValueError(f"zoomr: block_tables must be int32 {(cfg.batch, cfg.max_blocks_per_seq)}")
+
+
+def _check_rows(name: str, t: Optional[torch.Tensor], shape: tuple, dtype: torch.dtype) -> None:
+    if t is not None and (tuple(t.shape) != shape or t.dtype != dtype):
+        raise ValueError(f"zoomr: {name} must be {shape} {dtype}, got {tuple(t.shape)} {t.dtype}")
+
+
+def zr_append_kv(cfg: zr_config, positions: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                 block_tables: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+                 err: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Writes k_new/v_new [B, Hkv, d] at token positions[b] (int32, negative: skip) of each sequence."""
+    _check_cache(cfg, k_pool, v_pool, block_tables)
+    _check_rows("positions", positions, (cfg.batch,), torch.int32)
+    for name, t in (("k_new", k_new), ("v_new", v_new)):
+        _check_rows(name, t, (cfg.batch, cfg.num_kv_heads, cfg.head_dim), TORCH_DTYPES[cfg.dtype])
+    st = load().zr_append_kv(ctypes.byref(cfg), _dev(positions), _dev(k_new), _dev(v_new), _dev(block_tables),
+                             _dev(k_pool), _dev(v_pool), _dev(err), _stream(stream))
+    if st != ZR_OK:
+        raise ZoomrError(st, "zr_append_kv")
+
+
+def zr_copy_blocks(cfg: zr_config, pairs: Optional[torch.Tensor], k_pool: torch.Tensor, v_pool: torch.Tensor,
+                   err: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Copies whole blocks pairs[i, 0] -> pairs[i, 1] (int32 [n, 2]) in both pools."""
+    n = 0 if pairs is None else int(pairs.shape[0])
+    _check_cache(cfg, k_pool, v_pool)
+    _check_rows("pairs", pairs, (n, 2), torch.int32)
+    st = load().zr_copy_blocks(ctypes.byref(cfg), _dev(pairs) if n else None, n, _dev(k_pool), _dev(v_pool),
+                               _dev(err), _stream(stream))
+    if st != ZR_OK:
+        raise ZoomrError(st, "zr_copy_blocks")
+
+
+def zr_segment_summaries(cfg: zr_config, segs: Optional[torch.Tensor], block_tables: torch.Tensor,
+                         k_pool: torch.Tensor, v_pool: torch.Tensor, sum_k: torch.Tensor, sum_v: torch.Tensor,
+                         err: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Mean summary K/V rows of segs[i] = (b, start, end, row) (int32 [n, 4]) into sum_k/sum_v [rows, Hkv, d]."""
+    n = 0 if segs is None else int(segs.shape[0])
+    _check_cache(cfg, k_pool, v_pool, block_tables)
+    _check_rows("segs", segs, (n, 4), torch.int32)
+    rows = (int(sum_k.shape[0]), cfg.num_kv_heads, cfg.head_dim)
+    _check_rows("sum_k", sum_k, rows, TORCH_DTYPES[cfg.dtype])
+    _check_rows("sum_v", sum_v, rows, TORCH_DTYPES[cfg.dtype])
+    st = load().zr_segment_summaries(ctypes.byref(cfg), _dev(segs) if n else None, n, _dev(block_tables),
+                                     _dev(k_pool), _dev(v_pool), _dev(sum_k), _dev(sum_v), int(sum_k.shape[0]),
+                                     _dev(err), _stream(stream))
+    if st != ZR_OK:
+        raise ZoomrError(st, "zr_segment_summaries")
 
 
 class DecodePlan:

@@ -187,6 +187,69 @@ ZR_API zr_status zr_decode_attend_static(zr_plan_t plan, const void* q, const vo
  */
 ZR_API zr_status zr_get_device_error(zr_plan_t plan, void* workspace, void* stream, int32_t* err_code);
 
+/*
+ * ---------------------------------------------------------------- append path
+ * Three plan-free calls that keep the cache a decode step reads up to date.
+ * They take a zr_config for the shapes (batch, num_kv_heads, head_dim,
+ * block_size = 16, num_blocks, max_blocks_per_seq and dtype are used; the other
+ * fields are ignored), are asynchronous on `stream` and allocate nothing. `err`
+ * is an optional device int32 word (NULL: none) into which device-detected bad
+ * indices are OR-ed: bit 1 a physical block id outside [0, num_blocks), bit 2 a
+ * token position, segment or row index out of range; the offending row, pair
+ * or segment is skipped (no trap). Host errors: ZR_EINVAL for a bad config, a
+ * null required pointer, a negative count or a pool/row pointer that is not
+ * 16-byte aligned; ZR_EUNSUPPORTED for a head_dim other than 64 or 128 (in
+ * both cases nothing is launched); ZR_ECUDA if a launch fails.
+ */
+
+/*
+ * zr_append_kv -- write one new token's K and V rows per sequence into the
+ * paged pools ("KV-cache management" page, "Paged KV cache (PagedAttention)":
+ * token t of sequence b lives in physical block block_tables[b][t / 16], slot
+ * t % 16, for every KV head).
+ *   positions      [B] int32: the token index t_b sequence b writes; negative:
+ *                  sequence b writes nothing; t_b >= 16 * max_blocks_per_seq: bit 2
+ *   k_new, v_new   [B, Hkv, d] dtype
+ *   block_tables   [B, max_blocks_per_seq] int32; the block of t_b must already
+ *                  be in the table and private to sequence b (the caller adds a
+ *                  block when the last one is full and copies a shared last
+ *                  block first, with zr_copy_blocks)
+ *   k_pool, v_pool [num_blocks, Hkv, 16, d] dtype (written)
+ */
+ZR_API zr_status zr_append_kv(const zr_config* cfg, const int32_t* positions, const void* k_new, const void* v_new,
+                              const int32_t* block_tables, void* k_pool, void* v_pool, int32_t* err, void* stream);
+
+/*
+ * zr_copy_blocks -- the copy-on-write step of the "KV-cache management" page,
+ * "Block sharing with reference counts and copy-on-write", batched into one
+ * launch: every (src, dst) pair copies the whole physical block src (all KV
+ * heads, 16 rows) onto block dst, in both pools.
+ *   pairs          [n][2] int32 (src, dst); n >= 0. The dst blocks must be
+ *                  distinct and none may be a src of the same call (the copies
+ *                  run concurrently).
+ */
+ZR_API zr_status zr_copy_blocks(const zr_config* cfg, const int32_t* pairs, int32_t n, void* k_pool, void* v_pool,
+                                int32_t* err, void* stream);
+
+/*
+ * zr_segment_summaries -- the summary rows of completed segments (ZoomR page,
+ * 3.3 "Representing Context with Mean Summary Keys": the mean summary key is
+ * the average of the key vectors of the segment's tokens, per KV head; the
+ * summary value row is the same average of the V rows).
+ *   segs           [n][4] int32 (sequence b, first token s, end token e > s,
+ *                  output row r), 16-byte aligned; n >= 0
+ *   block_tables, k_pool, v_pool as in zr_append_kv (read)
+ *   sum_k, sum_v   [num_rows, Hkv, d] dtype; row r is written for every KV
+ *                  head: the rows are added in fp64 in ascending token order,
+ *                  the sum is divided by e - s, and the mean is rounded to fp32
+ *                  and then to dtype, each to nearest even. A segment with an
+ *                  out-of-range index, or a block id outside the pool, is not
+ *                  written.
+ */
+ZR_API zr_status zr_segment_summaries(const zr_config* cfg, const int32_t* segs, int32_t n, const int32_t* block_tables,
+                                      const void* k_pool, const void* v_pool, void* sum_k, void* sum_v,
+                                      int32_t num_rows, int32_t* err, void* stream);
+
 /* zr_free -- release the plan and its small device metadata (NULL is a no-op). */
 ZR_API void zr_free(zr_plan_t plan);
 

@@ -87,3 +87,60 @@ def test_too_many_segments_is_unsupported(lib):
     n = 4097
     cfg = Z.zr_config(1, 4, 1, 64, 16, 300, 300, 0, Z.ZR_BF16)
     assert Z.zr_plan_status(cfg, [n], [0, n], list(range(n + 1)), [1]) == Z.ZR_EUNSUPPORTED
+
+
+# ---------------------------------------------------------------- append path
+# Fake, 16-byte aligned "device" addresses: every case below is rejected (or is a
+# no-op) before any CUDA call, so nothing is dereferenced.
+_A = 1 << 20
+
+
+def _cache_cfg(**kw):
+    base = dict(batch=2, num_kv_heads=2, head_dim=64, num_blocks=8, max_blocks_per_seq=3, dtype="bf16")
+    base.update(kw)
+    return Z.cache_config(**base)
+
+
+@pytest.mark.parametrize("field,value,want", [
+    ("batch", 0, Z.ZR_EINVAL), ("num_kv_heads", 0, Z.ZR_EINVAL), ("block_size", 8, Z.ZR_EINVAL),
+    ("num_blocks", 0, Z.ZR_EINVAL), ("max_blocks_per_seq", 0, Z.ZR_EINVAL), ("dtype", 3, Z.ZR_EINVAL),
+    ("head_dim", 0, Z.ZR_EINVAL), ("head_dim", 96, Z.ZR_EUNSUPPORTED), ("num_blocks", 1 << 27, Z.ZR_EUNSUPPORTED),
+])
+def test_append_calls_reject_bad_configs(lib, field, value, want):
+    cfg = _cache_cfg()
+    setattr(cfg, field, value)
+    c = ctypes.byref(cfg)
+    assert lib.zr_append_kv(c, _A, _A, _A, _A, _A, _A, None, None) == want
+    assert lib.zr_copy_blocks(c, _A, 1, _A, _A, None, None) == want
+    assert lib.zr_segment_summaries(c, _A, 1, _A, _A, _A, _A, _A, 4, None, None) == want
+
+
+def test_append_calls_reject_null_misaligned_and_negative_arguments(lib):
+    c = ctypes.byref(_cache_cfg())
+    assert lib.zr_append_kv(None, _A, _A, _A, _A, _A, _A, None, None) == Z.ZR_EINVAL
+    for i in range(6):
+        args = [_A] * 6
+        args[i] = None
+        assert lib.zr_append_kv(c, *args, None, None) == Z.ZR_EINVAL, i
+    for i in (1, 2, 4, 5):  # k_new, v_new, k_pool, v_pool must be 16-byte aligned
+        args = [_A] * 6
+        args[i] = _A + 8
+        assert lib.zr_append_kv(c, *args, None, None) == Z.ZR_EINVAL, i
+    assert lib.zr_copy_blocks(c, _A, -1, _A, _A, None, None) == Z.ZR_EINVAL
+    assert lib.zr_copy_blocks(c, None, 2, _A, _A, None, None) == Z.ZR_EINVAL
+    assert lib.zr_copy_blocks(c, _A, 2, _A + 4, _A, None, None) == Z.ZR_EINVAL
+    assert lib.zr_segment_summaries(c, _A, -1, _A, _A, _A, _A, _A, 4, None, None) == Z.ZR_EINVAL
+    assert lib.zr_segment_summaries(c, _A, 1, _A, _A, _A, _A, _A, -1, None, None) == Z.ZR_EINVAL
+    assert lib.zr_segment_summaries(c, None, 1, _A, _A, _A, _A, _A, 4, None, None) == Z.ZR_EINVAL
+    for i in range(5):  # block_tables, k_pool, v_pool, sum_k, sum_v
+        args = [_A] * 5
+        args[i] = None
+        assert lib.zr_segment_summaries(c, _A, 1, *args, 4, None, None) == Z.ZR_EINVAL, i
+    assert lib.zr_segment_summaries(c, _A + 4, 1, _A, _A, _A, _A, _A, 4, None, None) == Z.ZR_EINVAL
+    assert lib.zr_segment_summaries(c, _A, 1, _A, _A, _A, _A + 2, _A, 4, None, None) == Z.ZR_EINVAL
+
+
+def test_empty_copy_and_summary_batches_launch_nothing(lib):
+    c = ctypes.byref(_cache_cfg())
+    assert lib.zr_copy_blocks(c, None, 0, _A, _A, None, None) == Z.ZR_OK
+    assert lib.zr_segment_summaries(c, None, 0, _A, _A, _A, _A, _A, 0, None, None) == Z.ZR_OK
