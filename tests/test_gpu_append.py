@@ -223,6 +223,49 @@ def test_summaries_of_every_segment_match_the_oracle(dtype, d):
     assert _same(_np32(sk), wk) and _same(_np32(sv), wv)
 
 
+def test_summaries_with_values_outside_the_exact_window_match_the_oracle():
+    """Tiny (far below the int64 window), large (above it) and subnormal values, exact zeros and negative zeros,
+    and a sum that fp64 cannot hold exactly (1 + 2^-60): every summary row still equals the oracle's fp64 loop."""
+    st, lt = _setup("bf16", 128, extra_cols=0)
+    segs = _all_segments(st)
+    long_segs = [sg for sg in segs if sg[2] - sg[1] >= 4]
+    bt = st.block_tables
+
+    def at(b, t):
+        return int(bt[b, t // 16]), t % 16
+
+    plants = [
+        (long_segs[0], "k", 3e-12), (long_segs[1], "v", 3000.0), (long_segs[2], "k", 1e-40),
+        (long_segs[3], "v", 2.0 ** -60), (long_segs[4], "k", 0.0), (long_segs[5], "v", -0.0),
+    ]
+    for (b, s0, _, _), which, val in plants:
+        pool = lt.k_pool if which == "k" else lt.v_pool
+        blk, slot = at(b, s0 + 1)
+        pool[blk, 1, slot, 3] = val
+        pool[blk, 0, slot, 64:96] = val
+    # an all-zero token row, and a segment whose values are all exactly 1 apart from one 2^-60
+    b, s0, e0, _ = long_segs[6]
+    blk, slot = at(b, s0)
+    lt.k_pool[blk, :, slot, :] = 0.0
+    b, s0, e0, _ = long_segs[7]
+    for t in range(s0, e0):
+        blk, slot = at(b, t)
+        lt.v_pool[blk, :, slot, :] = 1.0
+    blk, slot = at(b, s0 + 2)
+    lt.v_pool[blk, :, slot, 5] = 2.0 ** -60
+    torch.cuda.synchronize()
+    rows = st.total_segments
+    sk = torch.empty_like(lt.sum_k)
+    sv = torch.empty_like(lt.sum_v)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    Z.zr_segment_summaries(_cfg(st), torch.tensor(segs, dtype=torch.int32, device="cuda"), C.device_tables(st),
+                           lt.k_pool, lt.v_pool, sk, sv, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    wk, wv = A.segment_summaries(_np32(lt.k_pool), _np32(lt.v_pool), st.block_tables, segs, "bf16", rows)
+    assert _same(_np32(sk), wk) and _same(_np32(sv), wv)
+
+
 def test_summaries_of_chosen_spans_leave_other_rows_alone():
     """Arbitrary spans (one token, a whole block, across blocks, a whole sequence), rows out of order."""
     st, lt = _setup("bf16", 128, extra_cols=0)
