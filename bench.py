@@ -9,6 +9,7 @@ step reads ~5.1 GB, far more than the 129 MB L2, so no flush is needed between
 steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl zoomr|reference]
+  python bench.py --path append   # the cache-update path: token appends and segment summaries
 
 Prints one JSON line (rank 0). Under torchrun each rank runs its own replica of
 the workload on its own GPU (weak scaling) and the reported time is the max over
@@ -472,6 +473,224 @@ def run_zoomr(args):
     return 0
 
 
+# ---------------------------------------------------------------------- append path
+APPEND_METRIC = ("append-path generation steps/s at 8B shape, 16K ctx, batch 8, 32 layers (every sequence appends "
+                 "a token and closes a segment); HBM GB/s of the summary kernel vs peak")
+
+
+def append_step_plan(st):
+    """One generation step of the cache: every sequence appends its next token (a spare block when its last
+    one is full) and closes its last segment with it. Returns (block tables with one spare column, positions,
+    closing segments as (b, start, end, output row b))."""
+    B = st.batch
+    tables = np.concatenate([st.block_tables, np.full((B, 1), -1, np.int32)], axis=1)
+    used = set(int(x) for x in st.block_tables.ravel() if x >= 0)
+    free = [x for x in range(st.num_blocks) if x not in used]
+    pos = st.seq_lens.astype(np.int32).copy()
+    segs = []
+    for b in range(B):
+        t = int(pos[b])
+        if tables[b, t // 16] < 0:
+            tables[b, t // 16] = free.pop(0)
+        segs.append((b, int(st.bounds(b)[-2]), t + 1, b))
+    return tables, pos, np.array(segs, dtype=np.int32)
+
+
+def append_cpu_baseline(spec, budget_s: float, layers: int) -> dict:
+    """The append-path oracle (one core) on layer 0 of one generation step, repeated for ``budget_s``."""
+    from oracle import zoomr_append as OA
+
+    st = W.make_structure(spec, spare_blocks=spec.batch)
+    tables, pos, segs = append_step_plan(st)
+    lt = W.make_layer(st, 0, "cpu")
+    kp, vp = W.to_numpy32(lt.k_pool), W.to_numpy32(lt.v_pool)
+    rng = np.random.default_rng(5)
+    kn = rng.standard_normal((st.batch, spec.num_kv_heads, spec.head_dim)).astype(np.float32)
+    vn = rng.standard_normal((st.batch, spec.num_kv_heads, spec.head_dim)).astype(np.float32)
+    done, t0 = 0, time.perf_counter()
+    while True:
+        k2, v2 = OA.append_kv(kp, vp, tables, pos, kn, vn)
+        OA.segment_summaries(k2, v2, tables, [tuple(x) for x in segs], spec.dtype, st.batch)
+        done += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    t = time.perf_counter() - t0
+    return {"value": done / t / layers, "unit": "steps/s", "cores": 1, "kind": "oracle",
+            "sample": f"{done} layer updates (append 8 tokens, 8 closing-segment summaries) of layer 0 in {t:.1f} s, "
+                      f"scaled to a {layers}-layer step"}
+
+
+def run_append(args):
+    """Times one generation step of the append path (every layer: zr_append_kv, then zr_segment_summaries of
+    the segments the new tokens close), replayed as a CUDA graph; also times the summary kernel alone."""
+    spec = W.WORKLOADS[WORKLOAD_ID]
+    solo = int(os.environ.get("WORLD_SIZE", "1")) == 1
+    layers = spec.layers if args.layers is None else max(1, min(args.layers, spec.layers))
+    cpu_line = append_cpu_baseline(spec, args.cpu_budget, layers) if solo and not args.no_cpu_baseline else None
+    world, rank, local = dist_setup(args.gpus)
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: the append path needs a CUDA GPU")
+    from hierarchical_sparse_kv_gb300 import build as B
+    from hierarchical_sparse_kv_gb300 import zoomr as Z
+
+    if rank == 0 or world == 1:
+        B.build()
+    barrier(world)
+    Z.load()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    st = W.make_structure(spec, spare_blocks=spec.batch)
+    tables, pos, segs = append_step_plan(st)
+    L = spec.layers if args.layers is None else max(1, min(args.layers, spec.layers))
+    Bn, H, d = st.batch, spec.num_kv_heads, spec.head_dim
+    eb = 2 if spec.dtype == "bf16" else 4
+    lts = [W.make_layer(st, l, dev) for l in range(L)]
+    cfg = Z.cache_config(batch=Bn, num_kv_heads=H, head_dim=d, num_blocks=st.num_blocks,
+                         max_blocks_per_seq=tables.shape[1], dtype=spec.dtype)
+    bt = torch.from_numpy(tables).to(dev)
+    pos_d = torch.from_numpy(pos).to(dev)
+    segs_d = torch.from_numpy(segs).to(dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(spec.seed)
+    dt = W.torch_dtype(spec.dtype)
+    kn_all = torch.randn((L, Bn, H, d), generator=gen, device=dev).to(dt)
+    vn_all = torch.randn((L, Bn, H, d), generator=gen, device=dev).to(dt)
+    rows_all = torch.empty((2, L, Bn, H, d), dtype=dt, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(kind, s):
+        for l, lt in enumerate(lts):
+            if kind in ("full", "append"):
+                Z.zr_append_kv(cfg, pos_d, kn_all[l], vn_all[l], bt, lt.k_pool, lt.v_pool, err, stream=s)
+            if kind in ("full", "summaries"):
+                Z.zr_segment_summaries(cfg, segs_d, bt, lt.k_pool, lt.v_pool, rows_all[0, l], rows_all[1, l], err,
+                                       stream=s)
+
+    kinds = ("full", "append", "summaries")
+    graphs = {}
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        step("full", stream)  # eager warm-up (also sets the summary kernel's shared-memory attribute)
+        for k in kinds:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                step(k, stream)
+            graphs[k] = g
+    torch.cuda.synchronize()
+
+    def timed(kind, steps, sampler=None):
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                graphs[kind].replay()
+        torch.cuda.synchronize()
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(steps):
+                graphs[kind].replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        return max_over_ranks(e0.elapsed_time(e1) / steps, world)
+
+    clocks = ClockSampler(dev.index) if rank == 0 else None
+    time.sleep(0.25 if clocks and clocks.proc else 0)
+    ms = timed("full", args.steps)
+    clk = clocks.stop() if clocks else None
+    ms_append = timed("append", args.steps)
+    ms_sums = timed("summaries", args.steps)
+    assert int(err.item()) == 0, "device error word set"
+
+    # bulk: every segment of layer 0 (the whole 16K-token cache of each sequence)
+    segs_all = []
+    for b in range(Bn):
+        bnd = st.bounds(b)
+        segs_all += [(b, int(bnd[i]), int(bnd[i + 1]), int(st.seg_ptr[b]) + i) for i in range(len(bnd) - 1)]
+    segs_all_d = torch.tensor(segs_all, dtype=torch.int32, device=dev)
+    bulk_k = torch.empty((len(segs_all), H, d), dtype=dt, device=dev)
+    bulk_v = torch.empty_like(bulk_k)
+    bulk_ms = []
+    for i in range(3 + 20):
+        l = i % L  # rotate over the layers' pools (each far larger than L2)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        Z.zr_segment_summaries(cfg, segs_all_d, bt, lts[l].k_pool, lts[l].v_pool, bulk_k, bulk_v, err, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if i >= 3:
+            bulk_ms.append(e0.elapsed_time(e1))
+    bulk_t = float(np.median(bulk_ms))
+    bulk_bytes = sum(e - s for _, s, e, _ in segs_all) * H * d * eb * 2 + len(segs_all) * H * d * eb * 2
+
+    # e2e: each step's new K/V rows from pinned host memory, the step, the new summary rows back to the host
+    host_new = torch.stack([kn_all, vn_all]).cpu().pin_memory()
+    dev_new = torch.stack([kn_all, vn_all])
+    host_rows = torch.empty(rows_all.shape, dtype=dt).pin_memory()
+    kn_all, vn_all = dev_new[0], dev_new[1]  # the graphs read the old buffers: re-capture on the new ones
+
+    with torch.cuda.stream(stream):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step("full", stream)
+    e2e_steps = max(3, min(args.steps, 50))
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            dev_new.copy_(host_new, non_blocking=True)
+            g.replay()
+            host_rows.copy_(rows_all, non_blocking=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            dev_new.copy_(host_new, non_blocking=True)
+            g.replay()
+            host_rows.copy_(rows_all, non_blocking=True)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
+
+    peak, peak_kind = read_peak()
+    sum_bytes = int(sum(int(e) - int(s) for _, s, e, _ in segs)) * H * d * eb * 2 + Bn * H * d * eb * 2
+    sum_us = ms_sums * 1e3 / L
+    achieved = sum_bytes / (sum_us * 1e-6) / 1e9
+    line = {
+        "impl": "zoomr", "path": "append", "metric": APPEND_METRIC, "value": world * 1e3 / ms, "unit": "steps/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": spec.dtype,
+        "data": "synthetic (seeded N(0,1) K/V cache, new rows N(0,1))",
+        "config": {"workload": spec.name + "_append" + ("" if L == spec.layers else f"_first{L}layers"), "batch": Bn,
+                   "seq_len": spec.seq_len, "layers": L,
+                   "kv_heads": H, "head_dim": d, "block_size": 16,
+                   "closing_segment_tokens": [int(e) - int(s) for _, s, e, _ in segs],
+                   "graph": True, "l2": "each step touches 32 layers' pools (far beyond L2); no flush"},
+        "append_us_per_layer": ms_append * 1e3 / L, "summaries_us_per_layer": sum_us,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_kind": f"{peak_kind} copy bandwidth", "traffic": None,
+                     "kernel": f"zr_summaries_exact_kernel<{d}>", "alg_bytes_per_launch": sum_bytes,
+                     "timing": "summaries-only graph of 32 launches, time / 32 (latency-bound: 8 segments per launch)"},
+        "bulk_summaries": {"segments": len(segs_all), "ms": bulk_t, "alg_bytes": bulk_bytes,
+                           "achieved_gbs": bulk_bytes / (bulk_t * 1e-3) / 1e9,
+                           "frac": bulk_bytes / (bulk_t * 1e-3) / 1e9 / peak,
+                           "timing": "median of 20 single launches, event pair, layers rotated"},
+        "e2e": {"value": world * 1e3 / e2e_ms, "unit": "steps/s",
+                "h2d_bytes_per_step": host_new.numel() * host_new.element_size(),
+                "d2h_bytes_per_step": host_rows.numel() * host_rows.element_size()},
+        "gpu_launches": 2 * L * args.steps,
+        "clocks": clk,
+    }
+    if cpu_line is not None:
+        line["cpu_baseline"] = cpu_line
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -486,10 +705,17 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle work for cpu_baseline, once on one core and once on all cores")
     ap.add_argument("--ref-units", type=int, default=16, help="oracle units per reference-arm step")
+    ap.add_argument("--path", choices=["decode", "append"], default="decode",
+                    help="decode: the headline decode step; append: the cache-update path (appends and summaries)")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="append path only: run the first N layers (a small case for profiling; the metric is "
+                         "defined on all 32)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
-    return run_reference(args) if args.impl == "reference" else run_zoomr(args)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_append(args) if args.path == "append" else run_zoomr(args)
 
 
 if __name__ == "__main__":

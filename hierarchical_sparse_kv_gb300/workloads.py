@@ -36,6 +36,7 @@ on a GPU differ; each run is deterministic on its own device.
 
 from __future__ import annotations
 
+import dataclasses
 import math
 from dataclasses import dataclass, field
 from typing import Dict, List, Optional, Sequence
@@ -344,3 +345,175 @@ def small_spec(**kw) -> WorkloadSpec:
                 shared_prefix_tokens=0, peaky_query=False, seed=0)
     base.update(kw)
     return WorkloadSpec(**base)
+
+
+# --------------------------------------------------------------------------
+# the consensus layout: prompt, then (regular segment, summary segment) pairs
+# --------------------------------------------------------------------------
+@dataclass(frozen=True)
+class ConsensusSpec:
+    """A workload of ZoomR's consensus path (3.3 "Global Aggregation and Consensus").
+
+    Every sequence holds ``prompt_len`` prompt tokens and ``gen_len`` generated
+    ones. The generated tokens are pairs of a regular segment R_i (length
+    U{reg_len_range}) followed by its summary segment S_i (U{sum_len_range}),
+    then a tail shorter than the next pair (a paragraph with no summary yet).
+    """
+
+    name: str
+    dtype: str
+    batch: int
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    prompt_len: int
+    gen_len: int
+    reg_len_range: tuple
+    sum_len_range: tuple
+    topk: int
+    consensus: int
+    window: int
+    layers: int = 1
+    seed: int = 0
+
+
+CONSENSUS_WORKLOADS: Dict[int, ConsensusSpec] = {
+    # tiny fp32 case the oracle finishes in seconds
+    0: ConsensusSpec("consensus_tiny_f32_b2_h8x2_d64_P32_G480", "f32", 2, 8, 2, 64, 32, 480, (16, 48), (4, 8),
+                     2, 2, 32, layers=2, seed=10),
+    # the ZoomR page's analysis shape (3.5: N_p = 512, N_w = 512, c = 2, mean R 250, mean S 20) at the
+    # 8B model's attention shape, 16K generated tokens, batch 8, 32 layers
+    1: ConsensusSpec("consensus_llama8b_bf16_b8_P512_G16384_32layers", "bf16", 8, 32, 8, 128, 512, 16384,
+                     (200, 300), (10, 30), 4, 2, 512, layers=32, seed=12),
+}
+
+
+@dataclass
+class ConsensusStructure:
+    spec: ConsensusSpec
+    seq_lens: np.ndarray      # int32 [B]
+    prompt_lens: np.ndarray   # int32 [B]
+    seg_ptr: np.ndarray       # int32 [B+1]; n_b = seg_ptr[b+1] - seg_ptr[b] pairs
+    seg_bounds: np.ndarray    # int32; sequence b's 2 n_b + 1 pair bounds start at 2 seg_ptr[b] + b
+    topk: np.ndarray          # int32 [B]
+    consensus: np.ndarray     # int32 [B]
+    window: int
+    num_blocks: int
+    block_tables: np.ndarray  # int32 [B, max_blocks], unused entries -1
+
+    @property
+    def batch(self) -> int:
+        return int(self.seq_lens.shape[0])
+
+    @property
+    def total_segments(self) -> int:
+        return int(self.seg_ptr[-1])
+
+    @property
+    def max_blocks_per_seq(self) -> int:
+        return int(self.block_tables.shape[1])
+
+    def num_segments(self, b: int) -> int:
+        return int(self.seg_ptr[b + 1] - self.seg_ptr[b])
+
+    def pair_bounds(self, b: int) -> np.ndarray:
+        s = 2 * int(self.seg_ptr[b]) + b
+        return self.seg_bounds[s:s + 2 * self.num_segments(b) + 1]
+
+    def summary_spans(self, b: int):
+        """(start, end) of every summary segment S_i of sequence b."""
+        bd = self.pair_bounds(b)
+        return [(int(bd[2 * i + 1]), int(bd[2 * i + 2])) for i in range(self.num_segments(b))]
+
+
+def make_consensus_structure(spec: ConsensusSpec, *, seq_lens: Optional[Sequence[int]] = None,
+                             spare_blocks: int = 0) -> ConsensusStructure:
+    """Pairs, block pool and block tables for ``spec`` (seeded by spec.seed)."""
+    rng = np.random.default_rng(spec.seed)
+    B = spec.batch
+    lens = (np.full(B, spec.prompt_len + spec.gen_len, dtype=np.int64) if seq_lens is None
+            else np.asarray(seq_lens, dtype=np.int64))
+    bounds_list = []
+    for b in range(B):
+        L = int(lens[b])
+        bd = [spec.prompt_len]
+        pos = spec.prompt_len
+        while True:
+            r = int(rng.integers(spec.reg_len_range[0], spec.reg_len_range[1] + 1))
+            s = int(rng.integers(spec.sum_len_range[0], spec.sum_len_range[1] + 1))
+            if pos + r + s > L:
+                break
+            bd += [pos + r, pos + r + s]
+            pos += r + s
+        assert len(bd) >= 3, "sequence too short for one (regular, summary) pair"
+        bounds_list.append(np.array(bd, dtype=np.int32))
+    n_seg = np.array([(len(x) - 1) // 2 for x in bounds_list], dtype=np.int64)
+    seg_ptr = np.concatenate([[0], np.cumsum(n_seg)]).astype(np.int32)
+    seg_bounds = np.concatenate(bounds_list).astype(np.int32)
+    nblk = (lens + BLOCK_SIZE - 1) // BLOCK_SIZE
+    num_blocks = int(nblk.sum()) + spare_blocks
+    alloc = PagedBlockAllocator(num_blocks, rng)
+    tables = np.full((B, int(nblk.max())), -1, dtype=np.int32)
+    for b in range(B):
+        own = alloc.alloc(int(nblk[b]))
+        tables[b, :len(own)] = own
+    return ConsensusStructure(spec, lens.astype(np.int32), np.full(B, spec.prompt_len, np.int32), seg_ptr,
+                              seg_bounds, np.full(B, spec.topk, np.int32), np.full(B, spec.consensus, np.int32),
+                              spec.window, num_blocks, tables)
+
+
+@dataclass
+class ConsensusLayer:
+    q: torch.Tensor        # [B, Hq, d] dtype
+    k_pool: torch.Tensor   # [num_blocks, Hkv, 16, d] dtype
+    v_pool: torch.Tensor   # [num_blocks, Hkv, 16, d] dtype
+    logical_k: Optional[List[torch.Tensor]] = field(default=None)  # per seq [L_b, Hkv, d] dtype
+    logical_v: Optional[List[torch.Tensor]] = field(default=None)
+
+
+def make_consensus_layer(st: ConsensusStructure, layer: int, device: str | torch.device = "cpu", *,
+                         keep_logical: bool = False) -> ConsensusLayer:
+    """One layer's queries and paged K/V pools: K, V ~ N(0, 1) in the storage dtype; every query head's
+    query is 3 x the mean of the stored K rows (its KV head) of one uniformly drawn summary segment, plus
+    N(0, 1). Seeded by spec.seed * 1000 + layer (torch generator on the device, numpy for the choices)."""
+    spec = st.spec
+    dev = torch.device(device)
+    dt = torch_dtype(spec.dtype)
+    seed = spec.seed * 1000 + layer
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed)
+    nrng = np.random.default_rng(seed)
+    B, Hq, Hkv, d = spec.batch, spec.num_q_heads, spec.num_kv_heads, spec.head_dim
+    G = Hq // Hkv
+    k_pool = torch.zeros((st.num_blocks, Hkv, BLOCK_SIZE, d), dtype=dt, device=dev)
+    v_pool = torch.zeros((st.num_blocks, Hkv, BLOCK_SIZE, d), dtype=dt, device=dev)
+    q = torch.empty((B, Hq, d), dtype=dt, device=dev)
+    lk_all, lv_all = [], []
+    for b in range(B):
+        L = int(st.seq_lens[b])
+        kk = torch.randn((L, Hkv, d), generator=gen, device=dev).to(dt)
+        vv = torch.randn((L, Hkv, d), generator=gen, device=dev).to(dt)
+        nblk = (L + BLOCK_SIZE - 1) // BLOCK_SIZE
+        idx = torch.from_numpy(st.block_tables[b, :nblk].astype(np.int64)).to(dev)
+        for src, pool in ((kk, k_pool), (vv, v_pool)):
+            pad = torch.zeros((nblk * BLOCK_SIZE, Hkv, d), dtype=dt, device=dev)
+            pad[:L] = src
+            pool[idx] = pad.view(nblk, BLOCK_SIZE, Hkv, d).permute(0, 2, 1, 3)
+        spans = st.summary_spans(b)
+        picks = nrng.integers(0, len(spans), size=Hq)
+        for h in range(Hq):
+            s, e = spans[int(picks[h])]
+            base = kk[s:e, h // G].to(torch.float64).mean(0)
+            noise = torch.randn((d,), generator=gen, device=dev).to(torch.float64)
+            q[b, h] = (3.0 * base + noise).to(torch.float32).to(dt)
+        if keep_logical:
+            lk_all.append(kk)
+            lv_all.append(vv)
+    return ConsensusLayer(q, k_pool, v_pool, lk_all if keep_logical else None, lv_all if keep_logical else None)
+
+
+def consensus_spec(**kw) -> ConsensusSpec:
+    """A custom consensus workload for tests (defaults: the tiny fp32 case)."""
+    base = dataclasses.asdict(CONSENSUS_WORKLOADS[0])
+    base.update(kw)
+    return ConsensusSpec(**base)
