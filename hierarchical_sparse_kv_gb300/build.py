@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libzoomr.so")
-SOURCES = ["zoomr_plan.cpp", "zoomr_kernels.cu", "zoomr_static.cu", "zoomr_append.cu"]
+SOURCES = ["zoomr_plan.cpp", "zoomr_kernels.cu", "zoomr_static.cu", "zoomr_append.cu", "zoomr_consensus.cu"]
 HEADERS = ["zoomr_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

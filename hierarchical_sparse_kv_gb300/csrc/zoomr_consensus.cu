@@ -1,0 +1,269 @@
+// Consensus selection of the ZoomR page, section 3.3, on the device.
+//
+//   vote       one CTA per (sequence b, KV head g) and layer: for every query head
+//              of the group, the fp32 score of every summary (3.3 "Per-Head
+//              Importance Scoring and Voting", alpha_i = q^T kbar_i; each product
+//              and partial sum rounded to nearest-even, components in ascending
+//              order), its top-k by rank counting (ties to the lower index), and
+//              one vote per selected summary added to the sequence's vote counts.
+//   consensus  one CTA per sequence, once per selection: I_all (summaries with a
+//              vote), I_c (the c with the most votes, ties to the lower index),
+//              I_s = I_all minus I_c (3.3 "Global Aggregation and Consensus"); the
+//              final token set I_f = prompt + window + R_i (i in I_c) + S_i (i in
+//              I_s) as maximal ascending ranges (3.3 "Constructing the Final
+//              Multi-Granularity Context"), written as the attend metadata of
+//              every KV head of the sequence; the vote counts are cleared.
+//
+// Layout of a sequence: prompt [0, N_p), then pairs R_i = [bd[2i], bd[2i+1]),
+// S_i = [bd[2i+1], bd[2i+2]) with bd[0] = N_p; S_{i-1} ends where R_i starts,
+// and the prompt ends where R_0 starts: those are the only touching pieces.
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "zoomr_internal.h"
+
+namespace zr {
+namespace {
+
+constexpr unsigned kFullMask = 0xFFFFFFFFu;
+constexpr int kVoteThreads = 256;
+constexpr int kConsensusThreads = 256;
+
+template <typename T>
+__device__ __forceinline__ float elem(const T* p, int i);
+template <>
+__device__ __forceinline__ float elem<float>(const float* p, int i) {
+  return p[i];
+}
+template <>
+__device__ __forceinline__ float elem<__nv_bfloat16>(const __nv_bfloat16* p, int i) {
+  return __bfloat162float(p[i]);
+}
+
+// Shared memory: q of one head [D] f32 | keys [n_max + 4] f32.
+template <typename T, int D>
+__global__ void __launch_bounds__(kVoteThreads) zr_vote_kernel(StepArgs a, const T* __restrict__ mean_keys,
+                                                               int32_t* __restrict__ votes) {
+  extern __shared__ __align__(16) float vsmem[];
+  float* qs = vsmem;
+  float* keys = vsmem + D;
+  const int g = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+  const int s0 = a.meta.seg_ptr[b];
+  const int n = a.meta.seg_ptr[b + 1] - s0;
+  const int k = a.meta.topk[b];  // clipped to n at plan time
+  const T* qb = static_cast<const T*>(a.q) + static_cast<size_t>(b) * a.Hq * D;
+  int32_t* vb = votes + static_cast<size_t>(b) * a.n_max;
+  for (int hh = 0; hh < a.G; ++hh) {
+    const int h = g * a.G + hh;
+    __syncthreads();  // the previous head's readers are done
+    for (int t = tid; t < D; t += kVoteThreads) qs[t] = elem<T>(qb + static_cast<size_t>(h) * D, t);
+    __syncthreads();
+    for (int i = tid; i < n; i += kVoteThreads) {
+      const T* kr = mean_keys + (static_cast<size_t>(s0 + i) * a.Hkv + g) * D;
+      float acc = 0.0f;
+      for (int t = 0; t < D; ++t) acc = __fadd_rn(acc, __fmul_rn(qs[t], elem<T>(kr, t)));
+      keys[i] = acc;
+    }
+    __syncthreads();
+    for (int i = tid; i < n; i += kVoteThreads) {
+      const float ki = keys[i];
+      int beat = 0;
+      for (int j = 0; j < n; ++j) {
+        const float kj = keys[j];
+        beat += (kj > ki) | ((kj == ki) & (j < i));
+      }
+      if (beat < k) atomicAdd(vb + i, 1);
+    }
+  }
+}
+
+__device__ __forceinline__ int warp_inclusive_sum(int x, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(kFullMask, x, o);
+    if (lane >= o) x += y;
+  }
+  return x;
+}
+
+// Shared memory: votes [n_max] | flag [n_max + 1] | bd [2 n_max + 1] | runs_s, runs_e [n_max + 2] each.
+__global__ void __launch_bounds__(kConsensusThreads) zr_consensus_kernel(StepArgs a, int32_t* __restrict__ votes,
+                                                                         int32_t* votes_out, int32_t* ic_out,
+                                                                         int c_max) {
+  extern __shared__ __align__(16) int csmem[];
+  const int nmax = a.n_max;
+  int* v = csmem;
+  int* flag = v + nmax;
+  int* bd = flag + nmax + 1;
+  int* runs_s = bd + 2 * nmax + 1;
+  int* runs_e = runs_s + nmax + 2;
+  __shared__ int s_cand, s_rstar;
+  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int s0 = a.meta.seg_ptr[b];
+  const int n = a.meta.seg_ptr[b + 1] - s0;
+  const int L = a.meta.seq_lens[b];
+  const int Np = a.meta.prompt_lens[b];
+  const int32_t* pb = a.meta.seg_bounds + 2 * static_cast<size_t>(s0) + b;
+  int32_t* vb = votes + static_cast<size_t>(b) * nmax;
+  if (tid == 0) s_cand = 0;
+  __syncthreads();
+  int local = 0;
+  for (int i = tid; i < n; i += kConsensusThreads) {
+    v[i] = vb[i];
+    vb[i] = 0;  // consumed: the next selection starts from zero
+    local += v[i] > 0;
+  }
+  for (int i = tid; i <= 2 * n; i += kConsensusThreads) bd[i] = pb[i];
+  if (local) atomicAdd(&s_cand, local);
+  __syncthreads();
+  const int c = min(a.meta.consensus[b], s_cand);
+  // I_c: candidates that fewer than c candidates beat (more votes, or as many and a lower index)
+  for (int i = tid; i < n; i += kConsensusThreads) {
+    const int vi = v[i];
+    int f = 0;
+    if (vi > 0) {
+      int beat = 0;
+      for (int j = 0; j < n; ++j) beat += (v[j] > vi) | ((v[j] == vi) & (j < i));
+      f = beat < c ? 1 : 2;  // 1: zoom in (R_i), 2: keep the summary (S_i)
+    }
+    flag[i] = f;
+  }
+  if (tid == 0) flag[n] = 0;
+  __syncthreads();
+  if (votes_out)
+    for (int i = tid; i < nmax; i += kConsensusThreads) votes_out[static_cast<size_t>(b) * nmax + i] = i < n ? v[i] : 0;
+  if (ic_out && warp == 1) {
+    int carry = 0;
+    for (int base = 0; base < n; base += 32) {
+      const int i = base + lane;
+      const bool in = i < n && flag[i] == 1;
+      const unsigned m = __ballot_sync(kFullMask, in);
+      if (in) ic_out[static_cast<size_t>(b) * c_max + carry + __popc(m & ((1u << lane) - 1u))] = i;
+      carry += __popc(m);
+    }
+    for (int j = carry + lane; j < c_max; j += 32) ic_out[static_cast<size_t>(b) * c_max + j] = -1;
+  }
+  // Runs of touching pieces, in ascending order; the prompt (if any) is run 0.
+  const int prompt_runs = Np > 0 ? 1 : 0;
+  if (warp == 0) {
+    if (lane == 0 && prompt_runs) {
+      runs_s[0] = 0;
+      runs_e[0] = Np;  // replaced below if R_0 extends the prompt's run
+    }
+    int carry = 0;
+    for (int base = 0; base < n; base += 32) {
+      const int i = base + lane;
+      const int f = i < n ? flag[i] : 0;
+      const bool touch_prev = f == 1 && (i == 0 ? Np > 0 : flag[i - 1] == 2);
+      const bool start = f != 0 && !touch_prev;
+      const bool last = f != 0 && !(f == 2 && flag[i + 1] == 1);
+      const unsigned m = __ballot_sync(kFullMask, start);
+      const int rid = prompt_runs + carry + __popc(m & ((2u << lane) - 1u)) - 1;
+      if (start) runs_s[rid] = f == 1 ? bd[2 * i] : bd[2 * i + 1];
+      if (last) runs_e[rid] = f == 1 ? bd[2 * i + 1] : bd[2 * i + 2];
+      carry += __popc(m);
+    }
+    if (lane == 0) s_rstar = prompt_runs + carry;  // run count, before the window search
+  }
+  __syncthreads();
+  const int m = s_rstar;
+  const int W0 = max(0, L - a.window);
+  __syncthreads();
+  for (int r = tid; r < m; r += kConsensusThreads)
+    if (runs_e[r] >= W0 && (r == 0 || runs_e[r - 1] < W0)) s_rstar = r;
+  __syncthreads();
+  const int rstar = s_rstar;
+  const int nr = rstar < m ? rstar + 1 : m + (W0 < L ? 1 : 0);
+  // final ranges and their prefix sums, written for every KV head of the sequence
+  if (warp == 0) {
+    int carry = 0;
+    for (int base = 0; base < nr; base += 32) {
+      const int r = base + lane;
+      int s_ = 0, e_ = 0;
+      if (r < nr) {
+        if (r < rstar) {
+          s_ = runs_s[r];
+          e_ = runs_e[r];
+        } else {
+          s_ = rstar < m ? min(W0, runs_s[rstar]) : W0;
+          e_ = L;
+        }
+      }
+      const int len = e_ - s_;
+      const int incl = warp_inclusive_sum(len, lane);
+      if (r < nr) {
+        for (int g = 0; g < a.Hkv; ++g) {
+          const size_t u = static_cast<size_t>(b) * a.Hkv + g;
+          a.ranges[(u * (a.k_max + 1) + r) * 2] = s_;
+          a.ranges[(u * (a.k_max + 1) + r) * 2 + 1] = e_;
+          a.cum[u * (a.k_max + 2) + r] = carry + incl - len;
+        }
+        if (a.ranges_out) {
+          a.ranges_out[(static_cast<size_t>(b) * (a.k_max + 1) + r) * 2] = s_;
+          a.ranges_out[(static_cast<size_t>(b) * (a.k_max + 1) + r) * 2 + 1] = e_;
+        }
+      }
+      carry += __shfl_sync(kFullMask, incl, 31);
+    }
+    for (int g = lane; g < a.Hkv; g += 32) {
+      const size_t u = static_cast<size_t>(b) * a.Hkv + g;
+      a.cum[u * (a.k_max + 2) + nr] = carry;
+      a.unit_info[u] = make_int4(nr, carry, 0, 0);
+      a.unit_rows[u] = carry;
+    }
+    if (lane == 0 && a.nranges_out) a.nranges_out[b] = nr;
+  }
+}
+
+}  // namespace
+
+size_t vote_smem_bytes(int d, int n_max) { return (static_cast<size_t>(d) + n_max + 4) * sizeof(float); }
+size_t consensus_smem_bytes(int n_max) {
+  return (static_cast<size_t>(n_max) + (n_max + 1) + (2 * n_max + 1) + 2 * (n_max + 2)) * sizeof(int);
+}
+
+zr_status launch_vote(const Plan& p, const StepArgs& a, const void* mean_keys, int32_t* votes, void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const dim3 grid(p.Hkv, p.B), block(kVoteThreads);
+  const size_t smem = vote_smem_bytes(p.d, p.n_max);
+  cudaError_t e = cudaSuccess;
+  if (p.cfg.dtype == ZR_BF16) {
+    auto* mk = static_cast<const __nv_bfloat16*>(mean_keys);
+    if (p.d == 64) {
+      cudaFuncSetAttribute(zr_vote_kernel<__nv_bfloat16, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem));
+      zr_vote_kernel<__nv_bfloat16, 64><<<grid, block, smem, s>>>(a, mk, votes);
+    } else {
+      cudaFuncSetAttribute(zr_vote_kernel<__nv_bfloat16, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem));
+      zr_vote_kernel<__nv_bfloat16, 128><<<grid, block, smem, s>>>(a, mk, votes);
+    }
+  } else {
+    auto* mk = static_cast<const float*>(mean_keys);
+    if (p.d == 64) {
+      cudaFuncSetAttribute(zr_vote_kernel<float, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem));
+      zr_vote_kernel<float, 64><<<grid, block, smem, s>>>(a, mk, votes);
+    } else {
+      cudaFuncSetAttribute(zr_vote_kernel<float, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem));
+      zr_vote_kernel<float, 128><<<grid, block, smem, s>>>(a, mk, votes);
+    }
+  }
+  e = cudaGetLastError();
+  return e == cudaSuccess ? ZR_OK : ZR_ECUDA;
+}
+
+zr_status launch_consensus(const Plan& p, const StepArgs& a, int32_t* votes, int32_t* votes_out, int32_t* ic_out,
+                           void* stream) {
+  const size_t smem = consensus_smem_bytes(p.n_max);
+  cudaFuncSetAttribute(zr_consensus_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  zr_consensus_kernel<<<p.B, kConsensusThreads, smem, static_cast<cudaStream_t>(stream)>>>(a, votes, votes_out,
+                                                                                           ic_out, p.c_max);
+  return cudaGetLastError() == cudaSuccess ? ZR_OK : ZR_ECUDA;
+}
+
+}  // namespace zr

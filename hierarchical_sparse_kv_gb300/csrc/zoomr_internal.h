@@ -25,10 +25,12 @@ enum : int32_t { kErrBadBlock = 1, kErrBadIndex = 2 };
 
 // Small device metadata copied from the host at plan time (one allocation).
 struct DeviceMeta {
-  int32_t* seq_lens;    // [B]
-  int32_t* seg_ptr;     // [B+1]
-  int32_t* seg_bounds;  // [total_segments + B]
-  int32_t* topk;        // [B], already clipped to n_b
+  int32_t* seq_lens;     // [B]
+  int32_t* seg_ptr;      // [B+1]
+  int32_t* seg_bounds;   // decode: [total_segments + B] segment bounds; consensus: [2 total_segments + B] pair bounds
+  int32_t* topk;         // [B], already clipped to n_b
+  int32_t* prompt_lens;  // consensus only: [B] N_p
+  int32_t* consensus;    // consensus only: [B] c, already clipped to n_b
 };
 
 // Byte offsets into the caller's workspace.
@@ -42,13 +44,18 @@ struct WsLayout {
   size_t sel;         // int32 [U][k_max] selected segments, ascending
   size_t part_o;      // float [U + attend_warps][G][d] unnormalised split outputs
   size_t part_ml;     // float [U + attend_warps][G][2] split (max, sum) in log2 units
+  size_t votes;       // consensus only: int32 [B][n_max] vote counts, zero between selections
   size_t total;
 };
 
+enum PlanMode : int { kDecodePlan = 0, kConsensusPlan = 1 };
+
 struct Plan {
+  int mode;  // PlanMode
   zr_config cfg;
   int B, Hq, Hkv, G, d, window, num_blocks, max_blocks;
-  int k_max, n_max, total_segments;
+  int k_max, n_max, total_segments;  // consensus: k_max = n_max + 1 (range capacity n_max + 2 per unit)
+  int c_max;                          // consensus: max clipped c (at least 1)
   int attend_ctas;   // persistent attend grid (one resident wave)
   int attend_warps;  // attend_ctas * kAttendWarps
   int device;
@@ -86,6 +93,9 @@ struct StepArgs {
   float scale_log2;  // log2(e) / sqrt(d)
 };
 
+// Implemented in zoomr_plan.cpp: the launch arguments that point into `workspace` (plus the plan's sizes).
+StepArgs step_args(const Plan& p, void* workspace);
+
 // Implemented in zoomr_plan.cpp: argument checks, then one decode step on `workspace`.
 zr_status decode_into(zr_plan_t plan, void* workspace, const void* q, const void* k_pool, const void* v_pool,
                       const int32_t* block_tables, const void* sum_k, const void* sum_v, float* out,
@@ -97,6 +107,15 @@ zr_status decode_into(zr_plan_t plan, void* workspace, const void* q, const void
 // for at most `useful_warps` warps.
 zr_status configure_kernels(Plan& p, int64_t useful_warps);
 zr_status launch_step(const Plan& p, const StepArgs& a, void* stream, void* ev_start, void* ev_stop);
+// Gather-attention and merge only, over the unit metadata already in the workspace.
+zr_status launch_attend_only(const Plan& p, const StepArgs& a, void* stream);
+
+// Implemented in zoomr_consensus.cu.
+size_t vote_smem_bytes(int d, int n_max);
+size_t consensus_smem_bytes(int n_max);
+zr_status launch_vote(const Plan& p, const StepArgs& a, const void* mean_keys, int32_t* votes, void* stream);
+zr_status launch_consensus(const Plan& p, const StepArgs& a, int32_t* votes, int32_t* votes_out, int32_t* ic_out,
+                           void* stream);
 
 }  // namespace zr
 

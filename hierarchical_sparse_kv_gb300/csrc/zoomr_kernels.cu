@@ -1236,6 +1236,27 @@ cudaError_t launch_for(const Plan& p, const StepArgs& a, cudaStream_t s, cudaEve
   return e;
 }
 
+template <typename T, int D>
+cudaError_t launch_attend_for(const Plan& p, const StepArgs& a, cudaStream_t s) {
+  const dim3 grid_attend(p.attend_ctas), block(kAttendWarps * 32);
+  cudaError_t e = cudaSuccess;
+  if (uses_mma<T, D>(p)) {
+    if constexpr (sizeof(T) == 2) e = launch_pdl(zr_attend_mma_kernel<D>, grid_attend, block, p.attend_smem, s, a);
+  } else {
+    e = launch_pdl(zr_attend_fma_kernel<T, D>, grid_attend, block, 0, s, a);
+  }
+  if (e != cudaSuccess) return report("attend launch", e), e;
+  if (p.merge_parts) {
+    e = launch_pdl(zr_merge_part_kernel<D>, dim3(p.B * p.Hq * (D / kMergeComp) / kMergeWarps),
+                   dim3(kMergeWarps * 32), 0, s, a);
+  } else {
+    const dim3 grid_merge((p.B * p.Hq * (D / 32) + kAttendWarps - 1) / kAttendWarps);
+    e = launch_pdl(zr_merge_comp_kernel<D>, grid_merge, block, 0, s, a);
+  }
+  if (e != cudaSuccess) report("merge launch", e);
+  return e;
+}
+
 }  // namespace
 
 zr_status configure_kernels(Plan& p, int64_t useful_warps) {
@@ -1243,6 +1264,20 @@ zr_status configure_kernels(Plan& p, int64_t useful_warps) {
     return p.d == 64 ? configure_for<__nv_bfloat16, 64>(p, useful_warps)
                      : configure_for<__nv_bfloat16, 128>(p, useful_warps);
   return p.d == 64 ? configure_for<float, 64>(p, useful_warps) : configure_for<float, 128>(p, useful_warps);
+}
+
+zr_status launch_attend_only(const Plan& p, const StepArgs& a, void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (p.cfg.dtype == ZR_BF16)
+    e = p.d == 64 ? launch_attend_for<__nv_bfloat16, 64>(p, a, s) : launch_attend_for<__nv_bfloat16, 128>(p, a, s);
+  else
+    e = p.d == 64 ? launch_attend_for<float, 64>(p, a, s) : launch_attend_for<float, 128>(p, a, s);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return ZR_ECUDA;
+  }
+  return ZR_OK;
 }
 
 zr_status launch_step(const Plan& p, const StepArgs& a, void* stream, void* ev_start, void* ev_stop) {

@@ -62,6 +62,73 @@ zr_status validate(const zr_config* c, const int32_t* seq_lens, const int32_t* s
   return ZR_OK;
 }
 
+// The shape checks shared by both plan kinds.
+zr_status validate_shape(const zr_config* c) {
+  if (c->batch < 1 || c->num_q_heads < 1 || c->num_kv_heads < 1) return ZR_EINVAL;
+  if (c->num_q_heads % c->num_kv_heads != 0) return ZR_EINVAL;
+  if (c->block_size != zr::kBlockTokens) return ZR_EINVAL;
+  if (c->num_blocks < 1 || c->max_blocks_per_seq < 1 || c->window < 0) return ZR_EINVAL;
+  if (c->dtype != ZR_F32 && c->dtype != ZR_BF16) return ZR_EINVAL;
+  if (c->head_dim != 64 && c->head_dim != 128) return c->head_dim < 1 ? ZR_EINVAL : ZR_EUNSUPPORTED;
+  if (c->num_q_heads / c->num_kv_heads > zr::kMaxGroup) return ZR_EUNSUPPORTED;
+  if (static_cast<int64_t>(c->num_blocks) * c->num_kv_heads * zr::kBlockTokens >= (int64_t(1) << 31))
+    return ZR_EUNSUPPORTED;
+  return ZR_OK;
+}
+
+zr_status validate_consensus(const zr_config* c, const int32_t* seq_lens, const int32_t* prompt_lens,
+                             const int32_t* seg_ptr, const int32_t* pair_bounds, const int32_t* topk,
+                             const int32_t* consensus) {
+  if (!c || !seq_lens || !prompt_lens || !seg_ptr || !pair_bounds || !topk || !consensus) return ZR_EINVAL;
+  const zr_status st = validate_shape(c);
+  if (st != ZR_OK) return st;
+  if (seg_ptr[0] != 0) return ZR_EINVAL;
+  for (int b = 0; b < c->batch; ++b) {
+    const int32_t L = seq_lens[b];
+    if (L < 1 || static_cast<int64_t>(L) > static_cast<int64_t>(c->max_blocks_per_seq) * zr::kBlockTokens)
+      return ZR_EINVAL;
+    const int64_t n = static_cast<int64_t>(seg_ptr[b + 1]) - seg_ptr[b];
+    if (n < 1) return ZR_EINVAL;
+    if (n > zr::kMaxSegments) return ZR_EUNSUPPORTED;
+    if (topk[b] < 0 || consensus[b] < 0 || prompt_lens[b] < 0 || prompt_lens[b] > L) return ZR_EINVAL;
+    // I_f must never be empty: a prompt, a window or at least one vote
+    if (prompt_lens[b] == 0 && c->window == 0 && topk[b] == 0) return ZR_EINVAL;
+  }
+  const int64_t total = seg_ptr[c->batch];
+  if (2 * total * c->num_kv_heads >= (int64_t(1) << 31)) return ZR_EUNSUPPORTED;
+  for (int b = 0; b < c->batch; ++b) {
+    const int32_t* bd = pair_bounds + 2 * static_cast<int64_t>(seg_ptr[b]) + b;
+    const int n = seg_ptr[b + 1] - seg_ptr[b];
+    if (bd[0] != prompt_lens[b] || bd[2 * n] > seq_lens[b]) return ZR_EINVAL;
+    for (int i = 0; i < 2 * n; ++i)
+      if (bd[i + 1] <= bd[i]) return ZR_EINVAL;
+  }
+  return ZR_OK;
+}
+
+// Workspace layout shared by both plan kinds (each region 256-byte aligned).
+void layout_workspace(zr::Plan& p) {
+  const size_t U = static_cast<size_t>(p.B) * p.Hkv;
+  const size_t slots = U + static_cast<size_t>(p.attend_warps);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t at = off;
+    off = align_up(off + bytes, 256);
+    return at;
+  };
+  p.ws.err = take(sizeof(int32_t));
+  p.ws.unit_info = take(U * 4 * sizeof(int32_t));
+  p.ws.unit_rows = take(U * sizeof(int32_t));
+  p.ws.ranges = take(U * (p.k_max + 1) * 2 * sizeof(int32_t));
+  p.ws.cum = take(U * (p.k_max + 2) * sizeof(int32_t));
+  p.ws.sumlist = take(U * p.n_max * sizeof(int32_t));
+  p.ws.sel = take(U * p.k_max * sizeof(int32_t));
+  p.ws.part_o = take(slots * p.G * p.d * sizeof(float));
+  p.ws.part_ml = take(slots * p.G * 2 * sizeof(float));
+  p.ws.votes = p.mode == zr::kConsensusPlan ? take(static_cast<size_t>(p.B) * p.n_max * sizeof(int32_t)) : 0;
+  p.ws.total = off;
+}
+
 }  // namespace
 
 extern "C" {
@@ -77,6 +144,7 @@ zr_status zr_plan(const zr_config* cfg, const int32_t* seq_lens, const int32_t* 
   struct zr_plan* P = new (std::nothrow) struct zr_plan();
   if (!P) return ZR_ENOMEM;
   zr::Plan& p = P->p;
+  p.mode = zr::kDecodePlan;
   p.cfg = *cfg;
   p.B = cfg->batch;
   p.Hq = cfg->num_q_heads;
@@ -120,25 +188,7 @@ zr_status zr_plan(const zr_config* cfg, const int32_t* seq_lens, const int32_t* 
     return st;
   }
 
-  // Workspace layout (each region 256-byte aligned).
-  const size_t U = static_cast<size_t>(p.B) * p.Hkv;
-  const size_t slots = U + static_cast<size_t>(p.attend_warps);
-  size_t off = 0;
-  auto take = [&](size_t bytes) {
-    size_t at = off;
-    off = align_up(off + bytes, 256);
-    return at;
-  };
-  p.ws.err = take(sizeof(int32_t));
-  p.ws.unit_info = take(U * 4 * sizeof(int32_t));
-  p.ws.unit_rows = take(U * sizeof(int32_t));
-  p.ws.ranges = take(U * (p.k_max + 1) * 2 * sizeof(int32_t));
-  p.ws.cum = take(U * (p.k_max + 2) * sizeof(int32_t));
-  p.ws.sumlist = take(U * p.n_max * sizeof(int32_t));
-  p.ws.sel = take(U * p.k_max * sizeof(int32_t));
-  p.ws.part_o = take(slots * p.G * p.d * sizeof(float));
-  p.ws.part_ml = take(slots * p.G * 2 * sizeof(float));
-  p.ws.total = off;
+  layout_workspace(p);
 
   // Device metadata: one allocation, synchronous copies.
   const size_t nb = static_cast<size_t>(p.B);
@@ -179,7 +229,7 @@ zr_status zr_plan(const zr_config* cfg, const int32_t* seq_lens, const int32_t* 
 }
 
 zr_status zr_plan_dims(zr_plan_t plan, int32_t* k_max, int32_t* n_max) {
-  if (!plan || !k_max || !n_max) return ZR_EINVAL;
+  if (!plan || !k_max || !n_max || plan->p.mode != zr::kDecodePlan) return ZR_EINVAL;
   *k_max = plan->p.k_max;
   *n_max = plan->p.n_max;
   return ZR_OK;
@@ -194,12 +244,11 @@ zr_status decode_into(zr_plan_t plan, void* workspace, const void* q, const void
                                int32_t* sel_out, int32_t* ranges_out, int32_t* nranges_out, void* stream,
                                void* ev_start, void* ev_stop) {
   if (!plan || !workspace || !q || !k_pool || !v_pool || !block_tables || !sum_k || !sum_v || !out) return ZR_EINVAL;
+  if (plan->p.mode != kDecodePlan) return ZR_EINVAL;
   if (!aligned(workspace, 256) || !aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) ||
       !aligned(sum_k, 16) || !aligned(sum_v, 16) || !aligned(out, 16) || !aligned(block_tables, 4))
     return ZR_EINVAL;
-  const zr::Plan& p = plan->p;
-  char* ws = static_cast<char*>(workspace);
-  zr::StepArgs a;
+  zr::StepArgs a = step_args(plan->p, workspace);
   a.q = q;
   a.k_pool = k_pool;
   a.v_pool = v_pool;
@@ -210,6 +259,12 @@ zr_status decode_into(zr_plan_t plan, void* workspace, const void* q, const void
   a.sel_out = sel_out;
   a.ranges_out = ranges_out;
   a.nranges_out = nranges_out;
+  return zr::launch_step(plan->p, a, stream, ev_start, ev_stop);
+}
+
+StepArgs step_args(const Plan& p, void* workspace) {
+  char* ws = static_cast<char*>(workspace);
+  StepArgs a{};
   a.meta = p.meta;
   a.err = reinterpret_cast<int32_t*>(ws + p.ws.err);
   a.unit_info = reinterpret_cast<int4*>(ws + p.ws.unit_info);
@@ -231,7 +286,7 @@ zr_status decode_into(zr_plan_t plan, void* workspace, const void* q, const void
   a.n_max = p.n_max;
   a.attend_warps = p.attend_warps;
   a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(p.d)));
-  return zr::launch_step(p, a, stream, ev_start, ev_stop);
+  return a;
 }
 
 }  // namespace zr
@@ -289,6 +344,160 @@ const char* zr_status_string(zr_status s) {
     case ZR_EDEVICE: return "ZR_EDEVICE: the device reported a bad index";
   }
   return "unknown zr_status";
+}
+
+}  // extern "C"
+
+extern "C" {
+
+zr_status zr_consensus_plan(const zr_config* cfg, const int32_t* seq_lens, const int32_t* prompt_lens,
+                            const int32_t* seg_ptr, const int32_t* pair_bounds, const int32_t* topk,
+                            const int32_t* consensus, zr_plan_t* out_plan, size_t* workspace_bytes) {
+  if (!out_plan || !workspace_bytes) return ZR_EINVAL;
+  *out_plan = nullptr;
+  *workspace_bytes = 0;
+  zr_status st = validate_consensus(cfg, seq_lens, prompt_lens, seg_ptr, pair_bounds, topk, consensus);
+  if (st != ZR_OK) return st;
+  struct zr_plan* P = new (std::nothrow) struct zr_plan();
+  if (!P) return ZR_ENOMEM;
+  zr::Plan& p = P->p;
+  p.mode = zr::kConsensusPlan;
+  p.cfg = *cfg;
+  p.B = cfg->batch;
+  p.Hq = cfg->num_q_heads;
+  p.Hkv = cfg->num_kv_heads;
+  p.G = p.Hq / p.Hkv;
+  p.d = cfg->head_dim;
+  p.window = cfg->window;
+  p.num_blocks = cfg->num_blocks;
+  p.max_blocks = cfg->max_blocks_per_seq;
+  p.total_segments = seg_ptr[p.B];
+
+  // Rows bound per unit: at most min(L, N_p + min(w, L) + the c longest regular segments + every
+  // summary segment) tokens (I_c contributes regular segments, I_s summary segments).
+  std::vector<int32_t> kclip(p.B), cclip(p.B);
+  p.n_max = 1;
+  p.c_max = 1;
+  int64_t rows_bound = 0;
+  for (int b = 0; b < p.B; ++b) {
+    const int n = seg_ptr[b + 1] - seg_ptr[b];
+    const int32_t* bd = pair_bounds + 2 * static_cast<int64_t>(seg_ptr[b]) + b;
+    const int L = seq_lens[b];
+    kclip[b] = std::min(topk[b], n);
+    cclip[b] = std::min(consensus[b], n);
+    p.n_max = std::max(p.n_max, n);
+    p.c_max = std::max(p.c_max, cclip[b]);
+    std::vector<int32_t> reg(n);
+    int64_t sum_s = 0;
+    for (int i = 0; i < n; ++i) {
+      reg[i] = bd[2 * i + 1] - bd[2 * i];
+      sum_s += bd[2 * i + 2] - bd[2 * i + 1];
+    }
+    std::sort(reg.begin(), reg.end(), std::greater<int32_t>());
+    int64_t top = 0;
+    for (int i = 0; i < cclip[b]; ++i) top += reg[i];
+    const int64_t tok = std::min<int64_t>(L, prompt_lens[b] + std::min<int64_t>(p.window, L) + top + sum_s);
+    rows_bound += tok * p.Hkv;
+  }
+  p.k_max = p.n_max + 1;  // range capacity per unit: prompt, one piece per pair, window
+  if (cudaGetDevice(&p.device) != cudaSuccess) {
+    cudaGetLastError();
+    delete P;
+    return ZR_ECUDA;
+  }
+  st = zr::configure_kernels(p, (rows_bound + 15) / 16);
+  if (st != ZR_OK) {
+    delete P;
+    return st;
+  }
+  layout_workspace(p);
+
+  const size_t nb = static_cast<size_t>(p.B);
+  const size_t n_bounds = 2 * static_cast<size_t>(p.total_segments) + nb;
+  size_t moff = 0;
+  auto mtake = [&](size_t count) {
+    size_t at = moff;
+    moff = align_up(moff + count * sizeof(int32_t), 256);
+    return at;
+  };
+  const size_t o_len = mtake(nb), o_ptr = mtake(nb + 1), o_bnd = mtake(n_bounds), o_topk = mtake(nb),
+               o_np = mtake(nb), o_c = mtake(nb);
+  void* base = nullptr;
+  cudaError_t ce = cudaMalloc(&base, moff);
+  if (ce != cudaSuccess) {
+    cudaGetLastError();
+    delete P;
+    return ce == cudaErrorMemoryAllocation ? ZR_ENOMEM : ZR_ECUDA;
+  }
+  p.d_meta_base = base;
+  char* cb = static_cast<char*>(base);
+  p.meta.seq_lens = reinterpret_cast<int32_t*>(cb + o_len);
+  p.meta.seg_ptr = reinterpret_cast<int32_t*>(cb + o_ptr);
+  p.meta.seg_bounds = reinterpret_cast<int32_t*>(cb + o_bnd);
+  p.meta.topk = reinterpret_cast<int32_t*>(cb + o_topk);
+  p.meta.prompt_lens = reinterpret_cast<int32_t*>(cb + o_np);
+  p.meta.consensus = reinterpret_cast<int32_t*>(cb + o_c);
+  bool ok = cudaMemcpy(p.meta.seq_lens, seq_lens, nb * 4, cudaMemcpyHostToDevice) == cudaSuccess &&
+            cudaMemcpy(p.meta.seg_ptr, seg_ptr, (nb + 1) * 4, cudaMemcpyHostToDevice) == cudaSuccess &&
+            cudaMemcpy(p.meta.seg_bounds, pair_bounds, n_bounds * 4, cudaMemcpyHostToDevice) == cudaSuccess &&
+            cudaMemcpy(p.meta.topk, kclip.data(), nb * 4, cudaMemcpyHostToDevice) == cudaSuccess &&
+            cudaMemcpy(p.meta.prompt_lens, prompt_lens, nb * 4, cudaMemcpyHostToDevice) == cudaSuccess &&
+            cudaMemcpy(p.meta.consensus, cclip.data(), nb * 4, cudaMemcpyHostToDevice) == cudaSuccess;
+  if (!ok) {
+    cudaGetLastError();
+    cudaFree(base);
+    delete P;
+    return ZR_ECUDA;
+  }
+  *out_plan = P;
+  *workspace_bytes = p.ws.total;
+  return ZR_OK;
+}
+
+zr_status zr_consensus_dims(zr_plan_t plan, int32_t* c_max, int32_t* n_max) {
+  if (!plan || !c_max || !n_max || plan->p.mode != zr::kConsensusPlan) return ZR_EINVAL;
+  *c_max = plan->p.c_max;
+  *n_max = plan->p.n_max;
+  return ZR_OK;
+}
+
+zr_status zr_consensus_vote(zr_plan_t plan, void* workspace, const void* q, const void* mean_keys, void* stream) {
+  if (!plan || !workspace || !q || !mean_keys || plan->p.mode != zr::kConsensusPlan) return ZR_EINVAL;
+  if (!aligned(workspace, 256) || !aligned(q, 16) || !aligned(mean_keys, 16)) return ZR_EINVAL;
+  zr::StepArgs a = zr::step_args(plan->p, workspace);
+  a.q = q;
+  return zr::launch_vote(plan->p, a, mean_keys,
+                         reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + plan->p.ws.votes), stream);
+}
+
+zr_status zr_consensus_select(zr_plan_t plan, void* workspace, int32_t* votes_out, int32_t* consensus_out,
+                              int32_t* ranges_out, int32_t* nranges_out, void* stream) {
+  if (!plan || !workspace || plan->p.mode != zr::kConsensusPlan) return ZR_EINVAL;
+  if (!aligned(workspace, 256)) return ZR_EINVAL;
+  zr::StepArgs a = zr::step_args(plan->p, workspace);
+  a.ranges_out = ranges_out;
+  a.nranges_out = nranges_out;
+  return zr::launch_consensus(plan->p, a,
+                              reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + plan->p.ws.votes),
+                              votes_out, consensus_out, stream);
+}
+
+zr_status zr_consensus_attend(zr_plan_t plan, void* workspace, const void* q, const void* k_pool,
+                              const void* v_pool, const int32_t* block_tables, float* out, void* stream) {
+  if (!plan || !workspace || !q || !k_pool || !v_pool || !block_tables || !out) return ZR_EINVAL;
+  if (plan->p.mode != zr::kConsensusPlan) return ZR_EINVAL;
+  if (!aligned(workspace, 256) || !aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) ||
+      !aligned(out, 16) || !aligned(block_tables, 4))
+    return ZR_EINVAL;
+  zr::StepArgs a = zr::step_args(plan->p, workspace);
+  a.q = q;
+  a.k_pool = k_pool;
+  a.v_pool = v_pool;
+  a.block_tables = block_tables;
+  a.sum_k = k_pool;  // no summary rows are gathered: every unit's summary count is 0
+  a.sum_v = v_pool;
+  a.out = out;
+  return zr::launch_attend_only(plan->p, a, stream);
 }
 
 }  // extern "C"

@@ -60,6 +60,7 @@ zr_status zr_decode_attend_static(zr_plan_t plan, const void* q, const void* k_p
                                   const int32_t* block_tables, const void* sum_k, const void* sum_v, float* out,
                                   void* stream) {
   if (!plan) return ZR_EINVAL;
+  if (plan->p.mode != zr::kDecodePlan) return ZR_EINVAL;
   if (plan->p.ws.total > kStaticScratchBytes) return ZR_EUNSUPPORTED;
   void* ws = nullptr;
   zr_status st = scratch_on_current_device(&ws);

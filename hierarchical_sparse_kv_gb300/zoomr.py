@@ -73,6 +73,17 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.zr_segment_summaries.argtypes = [ctypes.POINTER(zr_config), _P, ctypes.c_int32] + [_P] * 5 + \
         [ctypes.c_int32, _P, _P]
     lib.zr_segment_summaries.restype = ctypes.c_int
+    lib.zr_consensus_plan.argtypes = [ctypes.POINTER(zr_config)] + [_I32P] * 6 + [ctypes.POINTER(_P),
+                                                                             ctypes.POINTER(ctypes.c_size_t)]
+    lib.zr_consensus_plan.restype = ctypes.c_int
+    lib.zr_consensus_dims.argtypes = [_P, _I32P, _I32P]
+    lib.zr_consensus_dims.restype = ctypes.c_int
+    lib.zr_consensus_vote.argtypes = [_P] * 5
+    lib.zr_consensus_vote.restype = ctypes.c_int
+    lib.zr_consensus_select.argtypes = [_P] * 7
+    lib.zr_consensus_select.restype = ctypes.c_int
+    lib.zr_consensus_attend.argtypes = [_P] * 8
+    lib.zr_consensus_attend.restype = ctypes.c_int
     lib.zr_free.argtypes = [_P]
     lib.zr_free.restype = None
     lib.zr_status_string.argtypes = [ctypes.c_int]
@@ -312,6 +323,101 @@ class DecodePlan:
     def run_timed(self, q, k_pool, v_pool, block_tables, sum_k, sum_v, out, ev_start, ev_stop, stream=None):
         zr_decode_attend_timed(self.handle, self.ws, q, k_pool, v_pool, block_tables, sum_k, sum_v, out, ev_start,
                                ev_stop, stream)
+
+    def device_error(self, stream=None) -> int:
+        return zr_get_device_error(self.handle, self.ws, stream)
+
+    def close(self):
+        if getattr(self, "handle", None):
+            zr_free(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def zr_consensus_plan_status(cfg: Optional[zr_config], seq_lens, prompt_lens, seg_ptr, pair_bounds, topk,
+                             consensus) -> int:
+    """zr_consensus_plan's raw status (any plan created is freed): for error-path tests."""
+    lib = load()
+    a = [_i32(x) for x in (seq_lens, prompt_lens, seg_ptr, pair_bounds, topk, consensus)]
+    plan = _P()
+    ws = ctypes.c_size_t()
+    st = lib.zr_consensus_plan(ctypes.byref(cfg) if cfg is not None else None, *[_ptr32(x) for x in a],
+                               ctypes.byref(plan), ctypes.byref(ws))
+    if st == ZR_OK:
+        lib.zr_free(plan)
+    return st
+
+
+class ConsensusPlan:
+    """ZoomR's consensus path (``zr_consensus_*``): per-layer votes, one selection, per-layer attention.
+
+    Host metadata follow the C ABI: seq_lens, prompt_lens [B]; seg_ptr [B+1] (CSR over the (regular,
+    summary) pairs); pair_bounds (sequence b's 2 n_b + 1 bounds start at 2 seg_ptr[b] + b); topk and
+    consensus [B].
+    """
+
+    def __init__(self, *, batch: int, num_q_heads: int, num_kv_heads: int, head_dim: int, num_blocks: int,
+                 max_blocks_per_seq: int, window: int, dtype: str, seq_lens, prompt_lens, seg_ptr, pair_bounds,
+                 topk, consensus, device=None):
+        self.cfg = zr_config(batch, num_q_heads, num_kv_heads, head_dim, 16, num_blocks, max_blocks_per_seq, window,
+                             DTYPES[dtype])
+        self.device = torch.device(device if device is not None else "cuda")
+        lib = load()
+        a = [_i32(x) for x in (seq_lens, prompt_lens, seg_ptr, pair_bounds, topk, consensus)]
+        plan, ws = _P(), ctypes.c_size_t()
+        with torch.cuda.device(self.device):
+            st = lib.zr_consensus_plan(ctypes.byref(self.cfg), *[_ptr32(x) for x in a], ctypes.byref(plan),
+                                       ctypes.byref(ws))
+            if st != ZR_OK:
+                raise ZoomrError(st, "zr_consensus_plan")
+            self.handle, self.workspace_bytes = plan.value, ws.value
+            c_max, n_max = ctypes.c_int32(), ctypes.c_int32()
+            st = lib.zr_consensus_dims(self.handle, ctypes.byref(c_max), ctypes.byref(n_max))
+            if st != ZR_OK:
+                raise ZoomrError(st, "zr_consensus_dims")
+            self.c_max, self.n_max = c_max.value, n_max.value
+            self.workspace = torch.zeros(max(self.workspace_bytes, 256) // 4 + 64, dtype=torch.int32,
+                                         device=self.device)
+        off = (-self.workspace.data_ptr()) % 256
+        self.ws = self.workspace[off // 4:]
+        self.batch, self.num_q_heads, self.num_kv_heads, self.head_dim = batch, num_q_heads, num_kv_heads, head_dim
+
+    @classmethod
+    def from_structure(cls, st, device=None) -> "ConsensusPlan":
+        """Plan for a ``workloads.ConsensusStructure`` (any object with the same fields)."""
+        sp = st.spec
+        return cls(batch=st.batch, num_q_heads=sp.num_q_heads, num_kv_heads=sp.num_kv_heads, head_dim=sp.head_dim,
+                   num_blocks=st.num_blocks, max_blocks_per_seq=st.max_blocks_per_seq, window=st.window,
+                   dtype=sp.dtype, seq_lens=st.seq_lens, prompt_lens=st.prompt_lens, seg_ptr=st.seg_ptr,
+                   pair_bounds=st.seg_bounds, topk=st.topk, consensus=st.consensus, device=device)
+
+    def vote(self, q: torch.Tensor, mean_keys: torch.Tensor, stream=None) -> None:
+        st = load().zr_consensus_vote(self.handle, _dev(self.ws), _dev(q), _dev(mean_keys), _stream(stream))
+        if st != ZR_OK:
+            raise ZoomrError(st, "zr_consensus_vote")
+
+    def new_debug_outputs(self):
+        B = self.batch
+        mk = lambda shape: torch.full(shape, -2, dtype=torch.int32, device=self.device)
+        return mk((B, self.n_max)), mk((B, self.c_max)), mk((B, self.n_max + 2, 2)), mk((B,))
+
+    def select(self, debug=None, stream=None) -> None:
+        votes, ic, rng, nr = debug if debug is not None else (None, None, None, None)
+        st = load().zr_consensus_select(self.handle, _dev(self.ws), _dev(votes), _dev(ic), _dev(rng), _dev(nr),
+                                        _stream(stream))
+        if st != ZR_OK:
+            raise ZoomrError(st, "zr_consensus_select")
+
+    def attend(self, q, k_pool, v_pool, block_tables, out, stream=None) -> None:
+        st = load().zr_consensus_attend(self.handle, _dev(self.ws), _dev(q), _dev(k_pool), _dev(v_pool),
+                                        _dev(block_tables), _dev(out), _stream(stream))
+        if st != ZR_OK:
+            raise ZoomrError(st, "zr_consensus_attend")
 
     def device_error(self, stream=None) -> int:
         return zr_get_device_error(self.handle, self.ws, stream)

@@ -250,6 +250,87 @@ ZR_API zr_status zr_segment_summaries(const zr_config* cfg, const int32_t* segs,
                                       const void* k_pool, const void* v_pool, void* sum_k, void* sum_v,
                                       int32_t num_rows, int32_t* err, void* stream);
 
+/*
+ * ----------------------------------------------------------- consensus path
+ * ZoomR's own selection (ZoomR page, 3.3 "Global Aggregation and Consensus" and
+ * "Constructing the Final Multi-Granularity Context"): every query head of every
+ * layer votes for its top-k summaries, the c summaries with the most votes are
+ * zoomed into their full regular segments, the other voted-for summaries keep
+ * their summary segments, the rest are dropped, and every layer and head of a
+ * sequence then attends over the one final token set
+ *   I_f = prompt [0, N_p) + window [max(0, L - w), L) + R_i (i in I_c) + S_i (i in I_s).
+ *
+ * Layout of sequence b: the prompt [0, N_p), then n_b pairs of a regular segment
+ * R_i and its summary segment S_i laid end to end, then possibly a tail with no
+ * summary yet (only the window reaches it). The 2 n_b + 1 strictly ascending pair
+ * bounds bd start at index 2 seg_ptr[b] + b of pair_bounds, with bd[0] = N_p and
+ * bd[2 n_b] <= L_b: R_i = [bd[2i], bd[2i+1]), S_i = [bd[2i+1], bd[2i+2]).
+ *
+ * A step: zr_consensus_vote once per layer (votes accumulate in the workspace),
+ * zr_consensus_select once (consumes and clears the votes, writes I_f), then
+ * zr_consensus_attend once per layer; I_f stays in the workspace until the next
+ * zr_consensus_select, so attend calls may repeat between selections. Plans of
+ * this kind are rejected by the decode entry points and vice versa; the
+ * workspace rules, zr_get_device_error and zr_free are shared.
+ */
+
+/*
+ * zr_consensus_plan -- validate the consensus problem and build a plan.
+ *   cfg            as for zr_plan (window = w; dtype of q, mean keys and pools)
+ *   seq_lens       [B]  1 <= L_b <= 16 * max_blocks_per_seq
+ *   prompt_lens    [B]  0 <= N_p <= L_b
+ *   seg_ptr        [B+1] CSR over the pairs, 1 <= n_b <= 4096, seg_ptr[0] = 0
+ *   pair_bounds    [2 seg_ptr[B] + B]  as described above
+ *   topk           [B]  k_b >= 0 per query head (clipped to n_b)
+ *   consensus      [B]  c_b >= 0 (clipped to n_b, then to |I_all|)
+ * A sequence with N_p = 0, w = 0 and k_b = 0 could attend nothing: ZR_EINVAL.
+ * Ties: equal scores and equal vote counts go to the lower summary index.
+ * Errors as for zr_plan.
+ */
+ZR_API zr_status zr_consensus_plan(const zr_config* cfg, const int32_t* seq_lens, const int32_t* prompt_lens,
+                                   const int32_t* seg_ptr, const int32_t* pair_bounds, const int32_t* topk,
+                                   const int32_t* consensus, zr_plan_t* out_plan, size_t* workspace_bytes);
+
+/* zr_consensus_dims -- *c_max = max_b min(c_b, n_b) (at least 1), *n_max = max_b n_b. */
+ZR_API zr_status zr_consensus_dims(zr_plan_t plan, int32_t* c_max, int32_t* n_max);
+
+/*
+ * zr_consensus_vote -- one layer's votes (ZoomR 3.3 "Per-Head Importance Scoring
+ * and Voting"): for every query head h, alpha_i = q_h . kbar_i over the
+ * sequence's n_b summaries, with kbar the mean summary key of S_i for the KV
+ * head h / G; the top-k indices each get one vote. alpha is the fp32 dot with
+ * each product and each partial sum rounded to nearest-even, components in
+ * ascending order (no scale).
+ *   q          [B, Hq, d] dtype (device)
+ *   mean_keys  [seg_ptr[B], Hkv, d] dtype (device), pair rows in CSR order
+ *              (zr_segment_summaries over the S_i spans computes them)
+ */
+ZR_API zr_status zr_consensus_vote(zr_plan_t plan, void* workspace, const void* q, const void* mean_keys,
+                                   void* stream);
+
+/*
+ * zr_consensus_select -- the consensus over the accumulated votes and the final
+ * token set of every sequence; clears the votes. Optional debug outputs (NULL:
+ * not written), all int32 device arrays:
+ *   votes_out      [B, n_max]    v_i (0 past n_b)
+ *   consensus_out  [B, c_max]    I_c ascending, -1 padded
+ *   ranges_out     [B, n_max + 2, 2]  I_f as maximal ranges [start, end), ascending
+ *   nranges_out    [B]           number of ranges
+ */
+ZR_API zr_status zr_consensus_select(zr_plan_t plan, void* workspace, int32_t* votes_out, int32_t* consensus_out,
+                                     int32_t* ranges_out, int32_t* nranges_out, void* stream);
+
+/*
+ * zr_consensus_attend -- one layer's attention over the current I_f (ZoomR 2
+ * "Background": softmax(q K^T / sqrt(d)) V for every query head over the K/V rows
+ * of I_f of its KV head, read through the block table).
+ *   q [B, Hq, d] dtype; k_pool/v_pool [num_blocks, Hkv, 16, d] dtype;
+ *   block_tables [B, max_blocks_per_seq] int32; out [B, Hq, d] float32 (written)
+ * Call zr_consensus_select at least once before the first attend on a workspace.
+ */
+ZR_API zr_status zr_consensus_attend(zr_plan_t plan, void* workspace, const void* q, const void* k_pool,
+                                     const void* v_pool, const int32_t* block_tables, float* out, void* stream);
+
 /* zr_free -- release the plan and its small device metadata (NULL is a no-op). */
 ZR_API void zr_free(zr_plan_t plan);
 

@@ -144,3 +144,41 @@ def test_empty_copy_and_summary_batches_launch_nothing(lib):
     c = ctypes.byref(_cache_cfg())
     assert lib.zr_copy_blocks(c, None, 0, _A, _A, None, None) == Z.ZR_OK
     assert lib.zr_segment_summaries(c, None, 0, _A, _A, _A, _A, _A, 0, None, None) == Z.ZR_OK
+
+
+# ---------------------------------------------------------------- consensus plan
+def _good_consensus():
+    # 2 sequences, L = 60 and 40; prompt 4 and 0; pairs (R, S): [4,14),[14,18),[18,30),[30,33) and [0,9),[9,12)
+    cfg = Z.zr_config(2, 8, 2, 64, 16, 8, 4, 8, Z.ZR_BF16)
+    return cfg, [60, 40], [4, 0], [0, 2, 3], [4, 14, 18, 30, 33, 0, 9, 12], [2, 1], [1, 1]
+
+
+@pytest.mark.parametrize("mutate,want", [
+    (lambda c, L, P, S, Bd, K, C: setattr(c, "batch", 0), Z.ZR_EINVAL),
+    (lambda c, L, P, S, Bd, K, C: setattr(c, "head_dim", 96), Z.ZR_EUNSUPPORTED),
+    (lambda c, L, P, S, Bd, K, C: setattr(c, "num_q_heads", 34), Z.ZR_EUNSUPPORTED),
+    (lambda c, L, P, S, Bd, K, C: L.__setitem__(1, 0), Z.ZR_EINVAL),            # empty sequence
+    (lambda c, L, P, S, Bd, K, C: L.__setitem__(0, 65), Z.ZR_EINVAL),           # longer than its table
+    (lambda c, L, P, S, Bd, K, C: P.__setitem__(0, 61), Z.ZR_EINVAL),           # prompt longer than L
+    (lambda c, L, P, S, Bd, K, C: P.__setitem__(0, 3), Z.ZR_EINVAL),            # bd[0] != prompt length
+    (lambda c, L, P, S, Bd, K, C: Bd.__setitem__(2, 14), Z.ZR_EINVAL),          # empty summary segment
+    (lambda c, L, P, S, Bd, K, C: Bd.__setitem__(7, 41), Z.ZR_EINVAL),          # pairs past L
+    (lambda c, L, P, S, Bd, K, C: S.__setitem__(1, 0), Z.ZR_EINVAL),            # a sequence with no pair
+    (lambda c, L, P, S, Bd, K, C: K.__setitem__(0, -1), Z.ZR_EINVAL),
+    (lambda c, L, P, S, Bd, K, C: C.__setitem__(1, -1), Z.ZR_EINVAL),
+    (lambda c, L, P, S, Bd, K, C: (setattr(c, "window", 0), K.__setitem__(1, 0)), Z.ZR_EINVAL),  # nothing to attend
+])
+def test_consensus_plan_rejects_bad_metadata_on_the_host(lib, mutate, want):
+    cfg, L, P, S, Bd, K, C = _good_consensus()
+    mutate(cfg, L, P, S, Bd, K, C)
+    assert Z.zr_consensus_plan_status(cfg, L, P, S, Bd, K, C) == want
+
+
+def test_consensus_entry_points_reject_null_arguments(lib):
+    cfg, L, P, S, Bd, K, C = _good_consensus()
+    assert Z.zr_consensus_plan_status(None, L, P, S, Bd, K, C) == Z.ZR_EINVAL
+    assert lib.zr_consensus_plan(ctypes.byref(cfg), None, None, None, None, None, None, None, None) == Z.ZR_EINVAL
+    assert lib.zr_consensus_vote(None, None, None, None, None) == Z.ZR_EINVAL
+    assert lib.zr_consensus_select(None, None, None, None, None, None, None) == Z.ZR_EINVAL
+    assert lib.zr_consensus_attend(*([None] * 8)) == Z.ZR_EINVAL
+    assert lib.zr_consensus_dims(None, None, None) == Z.ZR_EINVAL
