@@ -9,7 +9,8 @@ step reads ~5.1 GB, far more than the 129 MB L2, so no flush is needed between
 steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl zoomr|reference]
-  python bench.py --path append   # the cache-update path: token appends and segment summaries
+  python bench.py --path append      # the cache-update path: token appends and segment summaries
+  python bench.py --path consensus   # ZoomR's consensus selection and attention over its final set
 
 Prints one JSON line (rank 0). Under torchrun each rank runs its own replica of
 the workload on its own GPU (weak scaling) and the reported time is the max over
@@ -691,6 +692,203 @@ def run_append(args):
     return 0
 
 
+# ---------------------------------------------------------------------- consensus path
+CONSENSUS_METRIC = ("consensus decode steps/s at 8B shape, 512-token prompt + 16K generated, batch 8, 32 layers "
+                    "(one selection per 35 steps); HBM GB/s of the gather-attention kernel vs peak")
+SELECTION_INTERVAL = 35  # mean tokens between semantic boundaries (ZoomR appendix A.3)
+
+
+def consensus_cpu_baseline(spec, budget_s: float) -> dict:
+    """The consensus oracle (one core) on sequence 0: the votes of every layer and one layer's attention."""
+    from oracle import zoomr_append as OA
+    from oracle import zoomr_consensus as OC
+
+    st = W.make_consensus_structure(spec)
+    lt = W.make_consensus_layer(st, 0, "cpu")
+    kp, vp, q = W.to_numpy32(lt.k_pool), W.to_numpy32(lt.v_pool), W.to_numpy32(lt.q)
+    s0, s1 = int(st.seg_ptr[0]), int(st.seg_ptr[1])
+    kbar = np.zeros((st.total_segments, spec.num_kv_heads, spec.head_dim), np.float32)
+    for i, (s, e) in enumerate(st.summary_spans(0)):
+        for g in range(spec.num_kv_heads):
+            kbar[s0 + i, g] = OA.round_to_dtype(OA.segment_mean(kp, st.block_tables[0], g, s, e), spec.dtype)
+    done, t0 = 0, time.perf_counter()
+    while True:  # layer 0's inputs stand in for every layer: the work per layer is the same
+        OC.consensus_step([q] * spec.layers, [kbar] * spec.layers, [kp], [vp], st.block_tables, st.seg_ptr,
+                          st.seg_bounds, st.prompt_lens, st.seq_lens, st.topk, st.consensus, st.window,
+                          attend_layers=[0], batch=[0])
+        done += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    t = time.perf_counter() - t0
+    per_seq_step = t / done  # votes of all layers + one layer's attention, one sequence
+    # a selection step is that plus (layers - 1) more attention layers; attention dominates the rest
+    t_att0 = time.perf_counter()
+    OC.consensus_step([q], [kbar], [kp], [vp], st.block_tables, st.seg_ptr, st.seg_bounds, st.prompt_lens,
+                      st.seq_lens, st.topk, st.consensus, st.window, attend_layers=[0], batch=[0])
+    t_att = time.perf_counter() - t_att0
+    step_s = st.batch * (per_seq_step + (spec.layers - 1) * t_att)
+    return {"value": 1.0 / step_s, "unit": "steps/s", "cores": 1, "kind": "oracle",
+            "sample": f"{done} runs of sequence 0's votes over {spec.layers} layers and one layer's attention in "
+                      f"{t:.1f} s, plus one single-layer run; scaled to {st.batch} sequences and "
+                      f"{spec.layers} attention layers (every step treated as a selection step)"}
+
+
+def run_consensus(args):
+    """Times ZoomR's consensus decode on the device: a selection step (votes of every layer, one consensus,
+    every layer's attention), an attention-only step (I_f reused between semantic boundaries) and the
+    selection part alone, each replayed as a CUDA graph."""
+    spec = W.CONSENSUS_WORKLOADS[1]
+    solo = int(os.environ.get("WORLD_SIZE", "1")) == 1
+    cpu_line = consensus_cpu_baseline(spec, args.cpu_budget) if solo and not args.no_cpu_baseline else None
+    world, rank, local = dist_setup(args.gpus)
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: the consensus path needs a CUDA GPU")
+    from hierarchical_sparse_kv_gb300 import build as B
+    from hierarchical_sparse_kv_gb300 import zoomr as Z
+
+    if rank == 0 or world == 1:
+        B.build()
+    barrier(world)
+    Z.load()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    st = W.make_consensus_structure(spec)
+    L = spec.layers if args.layers is None else max(1, min(args.layers, spec.layers))
+    Bn, H, Hq, d = st.batch, spec.num_kv_heads, spec.num_q_heads, spec.head_dim
+    G = Hq // H
+    eb = 2 if spec.dtype == "bf16" else 4
+    lts = [W.make_consensus_layer(st, l, dev) for l in range(L)]
+    bt = torch.from_numpy(st.block_tables.astype(np.int32)).to(dev)
+    # mean summary keys of every layer (zr_segment_summaries over the summary spans)
+    cfg = Z.cache_config(batch=Bn, num_kv_heads=H, head_dim=d, num_blocks=st.num_blocks,
+                         max_blocks_per_seq=st.max_blocks_per_seq, dtype=spec.dtype)
+    segs = torch.tensor([(b, s, e, int(st.seg_ptr[b]) + i) for b in range(Bn)
+                         for i, (s, e) in enumerate(st.summary_spans(b))], dtype=torch.int32, device=dev)
+    dt = W.torch_dtype(spec.dtype)
+    mks = []
+    for lt in lts:
+        mk = torch.empty((st.total_segments, H, d), dtype=dt, device=dev)
+        Z.zr_segment_summaries(cfg, segs, bt, lt.k_pool, lt.v_pool, mk, torch.empty_like(mk))
+        mks.append(mk)
+    plan = Z.ConsensusPlan.from_structure(st, device=dev)
+    q_all = torch.stack([lt.q for lt in lts])
+    for l, lt in enumerate(lts):
+        lt.q = q_all[l]
+    out_all = torch.empty((L, Bn, Hq, d), dtype=torch.float32, device=dev)
+    dbg = plan.new_debug_outputs()
+    for l in range(L):
+        plan.vote(lts[l].q, mks[l])
+    plan.select(dbg)
+    torch.cuda.synchronize()
+    _, _, rng, nr = (x.cpu().numpy() for x in dbg)
+    tok = [A.ranges_token_count(rng[b, :nr[b]]) for b in range(Bn)]
+    attend_bytes = sum(A.attend_bytes_per_unit(tok[b], 0, A.ranges_block_count(rng[b, :nr[b]]), G, d, eb) * H
+                       for b in range(Bn)) + Bn * Hq * d * 4
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(kind, s):
+        if kind in ("select", "full"):
+            for l in range(L):
+                plan.vote(lts[l].q, mks[l], stream=s)
+            plan.select(stream=s)
+        if kind in ("attend", "full"):
+            for l in range(L):
+                plan.attend(lts[l].q, lts[l].k_pool, lts[l].v_pool, bt, out_all[l], stream=s)
+
+    graphs = {}
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        step("full", stream)
+        for k in ("full", "attend", "select"):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                step(k, stream)
+            graphs[k] = g
+    torch.cuda.synchronize()
+
+    def timed(kind, steps):
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                graphs[kind].replay()
+        torch.cuda.synchronize()
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(steps):
+                graphs[kind].replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        return max_over_ranks(e0.elapsed_time(e1) / steps, world)
+
+    clocks = ClockSampler(dev.index) if rank == 0 else None
+    time.sleep(0.25 if clocks and clocks.proc else 0)
+    ms_attend = timed("attend", args.steps)
+    ms_full = timed("full", args.steps)
+    clk = clocks.stop() if clocks else None
+    ms_select = timed("select", args.steps)
+    assert plan.device_error() == 0, "device error word set"
+    # one selection step every SELECTION_INTERVAL steps, attention-only steps in between
+    ms_mixed = (ms_full + (SELECTION_INTERVAL - 1) * ms_attend) / SELECTION_INTERVAL
+
+    # e2e: every step's queries from pinned host memory, the step, every layer's output back
+    host_q = q_all.cpu().pin_memory()
+    host_out = torch.empty(out_all.shape, dtype=out_all.dtype).pin_memory()
+    e2e_steps = SELECTION_INTERVAL
+    with torch.cuda.stream(stream):
+        for i in range(2):
+            q_all.copy_(host_q, non_blocking=True)
+            graphs["full" if i == 0 else "attend"].replay()
+            host_out.copy_(out_all, non_blocking=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(e2e_steps):
+            q_all.copy_(host_q, non_blocking=True)
+            graphs["full" if i == 0 else "attend"].replay()
+            host_out.copy_(out_all, non_blocking=True)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
+
+    peak, peak_kind = read_peak()
+    attend_us = ms_attend * 1e3 / L
+    achieved = attend_bytes / (attend_us * 1e-6) / 1e9
+    line = {
+        "impl": "zoomr", "path": "consensus", "metric": CONSENSUS_METRIC, "value": world * 1e3 / ms_mixed,
+        "unit": "steps/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_mixed,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": spec.dtype,
+        "data": "synthetic (seeded N(0,1) K/V, queries near one summary segment's mean key)",
+        "config": {"workload": spec.name + ("" if L == spec.layers else f"_first{L}layers"), "batch": Bn,
+                   "prompt": spec.prompt_len, "generated": spec.gen_len, "layers": L, "q_heads": Hq, "kv_heads": H,
+                   "head_dim": d, "top_k": spec.topk, "consensus": spec.consensus, "window": spec.window,
+                   "regular_len": list(spec.reg_len_range), "summary_len": list(spec.sum_len_range),
+                   "selection_interval": SELECTION_INTERVAL, "graph": True,
+                   "l2": "each step reads the 32 layers' final sets (far beyond L2); no flush"},
+        "selection_step_ms": ms_full, "attention_step_ms": ms_attend, "selection_part_ms": ms_select,
+        "final_set_tokens": tok,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_kind": f"{peak_kind} copy bandwidth", "traffic": None,
+                     "kernel": f"zr_attend_mma_kernel<{d}>", "alg_bytes_per_launch": attend_bytes,
+                     "timing": "attention-only graph of 32 layers (gather-attention + merge), time / 32"},
+        "e2e": {"value": world * 1e3 / e2e_ms, "unit": "steps/s", "h2d_bytes_per_step": host_q.numel() * eb,
+                "d2h_bytes_per_step": host_out.numel() * 4},
+        "gpu_launches": int(round(args.steps * (2 * L + (L + 1) / SELECTION_INTERVAL))),
+        "clocks": clk,
+    }
+    if cpu_line is not None:
+        line["cpu_baseline"] = cpu_line
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    plan.close()
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -705,17 +903,20 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle work for cpu_baseline, once on one core and once on all cores")
     ap.add_argument("--ref-units", type=int, default=16, help="oracle units per reference-arm step")
-    ap.add_argument("--path", choices=["decode", "append"], default="decode",
-                    help="decode: the headline decode step; append: the cache-update path (appends and summaries)")
+    ap.add_argument("--path", choices=["decode", "append", "consensus"], default="decode",
+                    help="decode: the headline decode step; append: the cache-update path (appends and summaries); "
+                         "consensus: ZoomR's own consensus selection and attention over its final set")
     ap.add_argument("--layers", type=int, default=None,
-                    help="append path only: run the first N layers (a small case for profiling; the metric is "
-                         "defined on all 32)")
+                    help="append and consensus paths only: run the first N layers (a small case for profiling; "
+                         "the metrics are defined on all 32)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
-    return run_append(args) if args.path == "append" else run_zoomr(args)
+    if args.path == "append":
+        return run_append(args)
+    return run_consensus(args) if args.path == "consensus" else run_zoomr(args)
 
 
 if __name__ == "__main__":

@@ -43,36 +43,62 @@ __device__ __forceinline__ float elem<__nv_bfloat16>(const __nv_bfloat16* p, int
   return __bfloat162float(p[i]);
 }
 
-// Shared memory: q of one head [D] f32 | keys [n_max + 4] f32.
+// Element e (0 .. 16 / sizeof(T) - 1) of a 16-byte piece, as a float.
+template <typename T>
+__device__ __forceinline__ float piece_elem(const uint4& w, int e) {
+  constexpr int PER_WORD = 4 / static_cast<int>(sizeof(T));
+  const int wi = e / PER_WORD;
+  const uint32_t x = wi == 0 ? w.x : wi == 1 ? w.y : wi == 2 ? w.z : w.w;
+  if constexpr (sizeof(T) == 2)
+    return __uint_as_float((e & 1) ? (x & 0xFFFF0000u) : (x << 16));
+  else
+    return __uint_as_float(x);
+}
+
+// Shared memory: q of the group [G][D] f32 | keys [hc][n_max + 4] f32, hc heads at a time.
+// Thread pairs (summary i, head h) run one fp32 chain each, in ascending component order, over the
+// row loaded whole in 16-byte pieces (the hc threads of a row share it through L1).
 template <typename T, int D>
 __global__ void __launch_bounds__(kVoteThreads) zr_vote_kernel(StepArgs a, const T* __restrict__ mean_keys,
-                                                               int32_t* __restrict__ votes) {
+                                                               int32_t* __restrict__ votes, int hc) {
   extern __shared__ __align__(16) float vsmem[];
+  constexpr int EPP = 16 / static_cast<int>(sizeof(T));  // elements per 16-byte piece
+  constexpr int P = D / EPP;                              // pieces per row
   float* qs = vsmem;
-  float* keys = vsmem + D;
+  float* keys = vsmem + static_cast<size_t>(a.G) * D;
   const int g = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
   const int s0 = a.meta.seg_ptr[b];
   const int n = a.meta.seg_ptr[b + 1] - s0;
   const int k = a.meta.topk[b];  // clipped to n at plan time
-  const T* qb = static_cast<const T*>(a.q) + static_cast<size_t>(b) * a.Hq * D;
+  const int nk = a.n_max + 4;
+  const T* qg = static_cast<const T*>(a.q) + (static_cast<size_t>(b) * a.Hq + static_cast<size_t>(g) * a.G) * D;
   int32_t* vb = votes + static_cast<size_t>(b) * a.n_max;
-  for (int hh = 0; hh < a.G; ++hh) {
-    const int h = g * a.G + hh;
-    __syncthreads();  // the previous head's readers are done
-    for (int t = tid; t < D; t += kVoteThreads) qs[t] = elem<T>(qb + static_cast<size_t>(h) * D, t);
-    __syncthreads();
-    for (int i = tid; i < n; i += kVoteThreads) {
-      const T* kr = mean_keys + (static_cast<size_t>(s0 + i) * a.Hkv + g) * D;
+  for (int t = tid; t < a.G * D; t += kVoteThreads) qs[t] = elem<T>(qg, t);
+  for (int h0 = 0; h0 < a.G; h0 += hc) {
+    const int nh = min(hc, a.G - h0);
+    __syncthreads();  // q staged; the previous heads' readers are done
+    for (int pi = tid; pi < n * nh; pi += kVoteThreads) {
+      const int i = pi / nh, h = pi - i * nh;
+      const uint4* kr = reinterpret_cast<const uint4*>(mean_keys + (static_cast<size_t>(s0 + i) * a.Hkv + g) * D);
+      uint4 w[P];
+#pragma unroll
+      for (int pc = 0; pc < P; ++pc) w[pc] = __ldg(kr + pc);
+      const float* qh = qs + (h0 + h) * D;
       float acc = 0.0f;
-      for (int t = 0; t < D; ++t) acc = __fadd_rn(acc, __fmul_rn(qs[t], elem<T>(kr, t)));
-      keys[i] = acc;
+#pragma unroll
+      for (int pc = 0; pc < P; ++pc)
+#pragma unroll
+        for (int e = 0; e < EPP; ++e) acc = __fadd_rn(acc, __fmul_rn(qh[pc * EPP + e], piece_elem<T>(w[pc], e)));
+      keys[h * nk + i] = acc;
     }
     __syncthreads();
-    for (int i = tid; i < n; i += kVoteThreads) {
-      const float ki = keys[i];
+    for (int pi = tid; pi < nh * n; pi += kVoteThreads) {
+      const int h = pi / n, i = pi - h * n;
+      const float* kh = keys + h * nk;
+      const float ki = kh[i];
       int beat = 0;
       for (int j = 0; j < n; ++j) {
-        const float kj = keys[j];
+        const float kj = kh[j];
         beat += (kj > ki) | ((kj == ki) & (j < i));
       }
       if (beat < k) atomicAdd(vb + i, 1);
@@ -220,7 +246,16 @@ __global__ void __launch_bounds__(kConsensusThreads) zr_consensus_kernel(StepArg
 
 }  // namespace
 
-size_t vote_smem_bytes(int d, int n_max) { return (static_cast<size_t>(d) + n_max + 4) * sizeof(float); }
+// Heads whose keys fit the vote kernel's shared memory at once (at least 1, at most the group).
+int vote_heads(int G, int d, int n_max) {
+  const size_t budget = 96 * 1024 - static_cast<size_t>(G) * d * sizeof(float);
+  const int fit = static_cast<int>(budget / ((static_cast<size_t>(n_max) + 4) * sizeof(float)));
+  return fit < 1 ? 1 : (fit < G ? fit : G);
+}
+
+size_t vote_smem_bytes(int G, int d, int n_max) {
+  return (static_cast<size_t>(G) * d + static_cast<size_t>(vote_heads(G, d, n_max)) * (n_max + 4)) * sizeof(float);
+}
 size_t consensus_smem_bytes(int n_max) {
   return (static_cast<size_t>(n_max) + (n_max + 1) + (2 * n_max + 1) + 2 * (n_max + 2)) * sizeof(int);
 }
@@ -228,29 +263,30 @@ size_t consensus_smem_bytes(int n_max) {
 zr_status launch_vote(const Plan& p, const StepArgs& a, const void* mean_keys, int32_t* votes, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const dim3 grid(p.Hkv, p.B), block(kVoteThreads);
-  const size_t smem = vote_smem_bytes(p.d, p.n_max);
+  const size_t smem = vote_smem_bytes(p.G, p.d, p.n_max);
+  const int hc = vote_heads(p.G, p.d, p.n_max);
   cudaError_t e = cudaSuccess;
   if (p.cfg.dtype == ZR_BF16) {
     auto* mk = static_cast<const __nv_bfloat16*>(mean_keys);
     if (p.d == 64) {
       cudaFuncSetAttribute(zr_vote_kernel<__nv_bfloat16, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem));
-      zr_vote_kernel<__nv_bfloat16, 64><<<grid, block, smem, s>>>(a, mk, votes);
+      zr_vote_kernel<__nv_bfloat16, 64><<<grid, block, smem, s>>>(a, mk, votes, hc);
     } else {
       cudaFuncSetAttribute(zr_vote_kernel<__nv_bfloat16, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem));
-      zr_vote_kernel<__nv_bfloat16, 128><<<grid, block, smem, s>>>(a, mk, votes);
+      zr_vote_kernel<__nv_bfloat16, 128><<<grid, block, smem, s>>>(a, mk, votes, hc);
     }
   } else {
     auto* mk = static_cast<const float*>(mean_keys);
     if (p.d == 64) {
       cudaFuncSetAttribute(zr_vote_kernel<float, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem));
-      zr_vote_kernel<float, 64><<<grid, block, smem, s>>>(a, mk, votes);
+      zr_vote_kernel<float, 64><<<grid, block, smem, s>>>(a, mk, votes, hc);
     } else {
       cudaFuncSetAttribute(zr_vote_kernel<float, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem));
-      zr_vote_kernel<float, 128><<<grid, block, smem, s>>>(a, mk, votes);
+      zr_vote_kernel<float, 128><<<grid, block, smem, s>>>(a, mk, votes, hc);
     }
   }
   e = cudaGetLastError();

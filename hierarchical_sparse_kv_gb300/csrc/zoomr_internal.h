@@ -111,7 +111,7 @@ zr_status launch_step(const Plan& p, const StepArgs& a, void* stream, void* ev_s
 zr_status launch_attend_only(const Plan& p, const StepArgs& a, void* stream);
 
 // Implemented in zoomr_consensus.cu.
-size_t vote_smem_bytes(int d, int n_max);
+size_t vote_smem_bytes(int G, int d, int n_max);
 size_t consensus_smem_bytes(int n_max);
 zr_status launch_vote(const Plan& p, const StepArgs& a, const void* mean_keys, int32_t* votes, void* stream);
 zr_status launch_consensus(const Plan& p, const StepArgs& a, int32_t* votes, int32_t* votes_out, int32_t* ic_out,
