@@ -11,6 +11,7 @@ steps.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl zoomr|reference]
   python bench.py --path append      # the cache-update path: token appends and segment summaries
   python bench.py --path consensus   # ZoomR's consensus selection and attention over its final set
+  python bench.py --path offload     # the decode step with the K/V pools in pinned host memory
 
 Prints one JSON line (rank 0). Under torchrun each rank runs its own replica of
 the workload on its own GPU (weak scaling) and the reported time is the max over
@@ -286,6 +287,16 @@ def run_zoomr(args):
     dev = torch.device("cuda", torch.cuda.current_device())
     spec, st, lts = make_inputs(dev, args.workload)
     L = len(lts)
+    offload = args.path == "offload"
+    link_gbs = None
+    if offload:
+        # the pages' offloaded cache: every layer's K/V pools in pinned host memory, read by the kernels
+        # across the CPU-GPU link; only queries, summaries, block tables and scratch stay in HBM
+        for lt in lts:
+            lt.k_pool = lt.k_pool.cpu().pin_memory()
+            lt.v_pool = lt.v_pool.cpu().pin_memory()
+        torch.cuda.empty_cache()
+        link_gbs = measure_link_gbs(dev)
     plan = Z.DecodePlan.from_structure(st, device=dev)
     bt = torch.from_numpy(st.block_tables.astype(np.int32)).to(dev)
     # every layer's queries and outputs are slices of one buffer each, so the end-to-end leg moves a
@@ -432,14 +443,15 @@ def run_zoomr(args):
 
     peak, peak_kind = read_peak()
     achieved = attend_bytes_avg / (attend_ms * 1e-3) / 1e9
-    traffic = read_traffic() if args.workload == WORKLOAD_ID else None
+    traffic = read_traffic() if args.workload == WORKLOAD_ID and not offload else None
     mma = spec.dtype == "bf16" and G <= 8
     kernel = f"zr_attend_mma_kernel<{spec.head_dim}>" if mma else \
         f"zr_attend_fma_kernel<{'bf16' if spec.dtype == 'bf16' else 'float'}, {spec.head_dim}>"
     l2 = (f"inputs exceed L2 (each step reads ~{step_bytes / 1e9:.2f} GB of K/V; no flush)" if step_bytes > 129e6 else
           f"inputs fit in L2 (each step reads ~{step_bytes / 1e6:.1f} MB; no flush: L2-resident timing)")
     line = {
-        "impl": "zoomr", "metric": METRIC, "value": world * 1e3 / ms, "unit": "steps/s", "n_gpus": world,
+        "impl": "zoomr", "metric": OFFLOAD_METRIC if offload else METRIC, "value": world * 1e3 / ms, "unit": "steps/s",
+        "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": spec.dtype,
         "data": "synthetic (seeded N(0,1) K/V, segment-mean summaries + N(0,0.1), queries near segment means)",
@@ -462,6 +474,12 @@ def run_zoomr(args):
         "clocks": clk,
         "tokens_gathered_per_step": tok_total,
     }
+    if offload:
+        line["path"] = "offload"
+        line["roofline"].update({"bound": "link", "peak": link_gbs, "frac": achieved / link_gbs,
+                                 "peak_kind": "measured pinned-host-to-device copy bandwidth of this box (1 GiB "
+                                              "cudaMemcpyAsync, median of 5)"})
+        line["config"]["pools"] = "pinned host memory (every layer's K/V), read across the CPU-GPU link"
     if cpu_line is not None:
         line["cpu_baseline"] = cpu_line
     if rank == 0:
@@ -472,6 +490,30 @@ def run_zoomr(args):
 
         dist.destroy_process_group()
     return 0
+
+
+# ---------------------------------------------------------------------- offloaded pools
+OFFLOAD_METRIC = ("decode attention steps/s at 8B shape, 16K ctx, batch 8, 32 layers, K/V pools in pinned host memory "
+                  "read across the CPU-GPU link; link GB/s vs the measured copy bandwidth")
+
+
+def measure_link_gbs(dev) -> float:
+    """Pinned-host-to-device copy bandwidth of this machine: a 1 GiB cudaMemcpyAsync, median of 5."""
+    src = torch.empty(1 << 30, dtype=torch.uint8).pin_memory()
+    dst = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
+    dst.copy_(src, non_blocking=True)
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(5):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        dst.copy_(src, non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    del src, dst
+    torch.cuda.empty_cache()
+    return (1 << 30) / (float(np.median(ts)) * 1e-3) / 1e9
 
 
 # ---------------------------------------------------------------------- append path
@@ -903,9 +945,10 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle work for cpu_baseline, once on one core and once on all cores")
     ap.add_argument("--ref-units", type=int, default=16, help="oracle units per reference-arm step")
-    ap.add_argument("--path", choices=["decode", "append", "consensus"], default="decode",
+    ap.add_argument("--path", choices=["decode", "append", "consensus", "offload"], default="decode",
                     help="decode: the headline decode step; append: the cache-update path (appends and summaries); "
-                         "consensus: ZoomR's own consensus selection and attention over its final set")
+                         "consensus: ZoomR's own consensus selection and attention over its final set; offload: the "
+                         "decode step with the K/V pools in pinned host memory")
     ap.add_argument("--layers", type=int, default=None,
                     help="append and consensus paths only: run the first N layers (a small case for profiling; "
                          "the metrics are defined on all 32)")

@@ -112,6 +112,17 @@ def _dev(t: Optional[torch.Tensor]) -> Optional[int]:
     return t.data_ptr()
 
 
+def _pool(t: torch.Tensor) -> int:
+    """A K/V pool may live in HBM or in pinned host memory: with unified addressing a pinned host
+    allocation is mapped into the device's address space at the same address, and the kernels read
+    it across the CPU-GPU link (NVLink-C2C on a Grace system)."""
+    if t.is_cuda:
+        return _dev(t)
+    if t.device.type == "cpu" and t.is_pinned() and t.is_contiguous():
+        return t.data_ptr()
+    raise ValueError("zoomr: a K/V pool must be a contiguous CUDA tensor or a contiguous pinned host tensor")
+
+
 def _stream(stream) -> Optional[int]:
     if stream is None:
         return torch.cuda.current_stream().cuda_stream
@@ -158,7 +169,7 @@ def zr_decode_attend(plan: int, workspace: torch.Tensor, q: torch.Tensor, k_pool
                      out: torch.Tensor, sel_out: Optional[torch.Tensor] = None,
                      ranges_out: Optional[torch.Tensor] = None, nranges_out: Optional[torch.Tensor] = None,
                      stream=None) -> None:
-    st = load().zr_decode_attend(plan, _dev(workspace), _dev(q), _dev(k_pool), _dev(v_pool), _dev(block_tables),
+    st = load().zr_decode_attend(plan, _dev(workspace), _dev(q), _pool(k_pool), _pool(v_pool), _dev(block_tables),
                                  _dev(sum_k), _dev(sum_v), _dev(out), _dev(sel_out), _dev(ranges_out),
                                  _dev(nranges_out), _stream(stream))
     if st != ZR_OK:
@@ -174,7 +185,7 @@ def zr_decode_attend_timed(plan: int, workspace: torch.Tensor, q: torch.Tensor, 
             if torch.cuda.is_current_stream_capturing():
                 raise ValueError("zoomr: record timing events once before using them inside a stream capture")
             ev.record(torch.cuda.current_stream() if stream is None or isinstance(stream, int) else stream)
-    st = load().zr_decode_attend_timed(plan, _dev(workspace), _dev(q), _dev(k_pool), _dev(v_pool),
+    st = load().zr_decode_attend_timed(plan, _dev(workspace), _dev(q), _pool(k_pool), _pool(v_pool),
                                        _dev(block_tables), _dev(sum_k), _dev(sum_v), _dev(out),
                                        ev_start.cuda_event if ev_start is not None else None,
                                        ev_stop.cuda_event if ev_stop is not None else None, _stream(stream))
@@ -187,7 +198,7 @@ def zr_decode_attend_static(plan: int, q: torch.Tensor, k_pool: torch.Tensor, v_
                             out: torch.Tensor, stream=None) -> None:
     """The decode step with the library's static 16 MiB device scratch instead of a
     caller workspace, for callers that cannot allocate device memory."""
-    st = load().zr_decode_attend_static(plan, _dev(q), _dev(k_pool), _dev(v_pool), _dev(block_tables), _dev(sum_k),
+    st = load().zr_decode_attend_static(plan, _dev(q), _pool(k_pool), _pool(v_pool), _dev(block_tables), _dev(sum_k),
                                         _dev(sum_v), _dev(out), _stream(stream))
     if st != ZR_OK:
         raise ZoomrError(st, "zr_decode_attend_static")
@@ -240,7 +251,7 @@ def zr_append_kv(cfg: zr_config, positions: torch.Tensor, k_new: torch.Tensor, v
     for name, t in (("k_new", k_new), ("v_new", v_new)):
         _check_rows(name, t, (cfg.batch, cfg.num_kv_heads, cfg.head_dim), TORCH_DTYPES[cfg.dtype])
     st = load().zr_append_kv(ctypes.byref(cfg), _dev(positions), _dev(k_new), _dev(v_new), _dev(block_tables),
-                             _dev(k_pool), _dev(v_pool), _dev(err), _stream(stream))
+                             _pool(k_pool), _pool(v_pool), _dev(err), _stream(stream))
     if st != ZR_OK:
         raise ZoomrError(st, "zr_append_kv")
 
@@ -251,7 +262,7 @@ def zr_copy_blocks(cfg: zr_config, pairs: Optional[torch.Tensor], k_pool: torch.
     n = 0 if pairs is None else int(pairs.shape[0])
     _check_cache(cfg, k_pool, v_pool)
     _check_rows("pairs", pairs, (n, 2), torch.int32)
-    st = load().zr_copy_blocks(ctypes.byref(cfg), _dev(pairs) if n else None, n, _dev(k_pool), _dev(v_pool),
+    st = load().zr_copy_blocks(ctypes.byref(cfg), _dev(pairs) if n else None, n, _pool(k_pool), _pool(v_pool),
                                _dev(err), _stream(stream))
     if st != ZR_OK:
         raise ZoomrError(st, "zr_copy_blocks")
@@ -268,7 +279,7 @@ def zr_segment_summaries(cfg: zr_config, segs: Optional[torch.Tensor], block_tab
     _check_rows("sum_k", sum_k, rows, TORCH_DTYPES[cfg.dtype])
     _check_rows("sum_v", sum_v, rows, TORCH_DTYPES[cfg.dtype])
     st = load().zr_segment_summaries(ctypes.byref(cfg), _dev(segs) if n else None, n, _dev(block_tables),
-                                     _dev(k_pool), _dev(v_pool), _dev(sum_k), _dev(sum_v), int(sum_k.shape[0]),
+                                     _pool(k_pool), _pool(v_pool), _dev(sum_k), _dev(sum_v), int(sum_k.shape[0]),
                                      _dev(err), _stream(stream))
     if st != ZR_OK:
         raise ZoomrError(st, "zr_segment_summaries")
@@ -414,7 +425,7 @@ class ConsensusPlan:
             raise ZoomrError(st, "zr_consensus_select")
 
     def attend(self, q, k_pool, v_pool, block_tables, out, stream=None) -> None:
-        st = load().zr_consensus_attend(self.handle, _dev(self.ws), _dev(q), _dev(k_pool), _dev(v_pool),
+        st = load().zr_consensus_attend(self.handle, _dev(self.ws), _dev(q), _pool(k_pool), _pool(v_pool),
                                         _dev(block_tables), _dev(out), _stream(stream))
         if st != ZR_OK:
             raise ZoomrError(st, "zr_consensus_attend")
