@@ -115,6 +115,60 @@ __device__ __forceinline__ int warp_inclusive_sum(int x, int lane) {
   return x;
 }
 
+// The calling warp merges the runs [0, m) (ascending, disjoint, touching runs already joined; run r is
+// [rs[r * stride], re[r * stride])) with the window [W0, L) -- the first run that reaches W0 absorbs it
+// and every later run -- and writes the ranges and their prefix sums as the attend metadata of units
+// u0 .. u0 + nu - 1, each with n_sum summary rows; rout / nrout (optional) receive the ranges too.
+__device__ void emit_ranges(const StepArgs& a, const int* rs, const int* re, int stride, int m, int W0, int L,
+                            size_t u0, int nu, int n_sum, int32_t* rout, int32_t* nrout, int lane) {
+  int rstar = m;
+  for (int base = 0; base < m; base += 32) {
+    const int r = base + lane;
+    const unsigned hit = __ballot_sync(kFullMask, r < m && re[r * stride] >= W0);
+    if (hit) {
+      rstar = base + __ffs(hit) - 1;
+      break;
+    }
+  }
+  const int nr = rstar < m ? rstar + 1 : m + (W0 < L ? 1 : 0);
+  int carry = 0;
+  for (int base = 0; base < nr; base += 32) {
+    const int r = base + lane;
+    int s_ = 0, e_ = 0;
+    if (r < nr) {
+      if (r < rstar) {
+        s_ = rs[r * stride];
+        e_ = re[r * stride];
+      } else {
+        s_ = rstar < m ? min(W0, rs[rstar * stride]) : W0;
+        e_ = L;
+      }
+    }
+    const int len = e_ - s_;
+    const int incl = warp_inclusive_sum(len, lane);
+    if (r < nr) {
+      for (int j = 0; j < nu; ++j) {
+        const size_t u = u0 + j;
+        a.ranges[(u * (a.k_max + 1) + r) * 2] = s_;
+        a.ranges[(u * (a.k_max + 1) + r) * 2 + 1] = e_;
+        a.cum[u * (a.k_max + 2) + r] = carry + incl - len;
+      }
+      if (rout) {
+        rout[2 * r] = s_;
+        rout[2 * r + 1] = e_;
+      }
+    }
+    carry += __shfl_sync(kFullMask, incl, 31);
+  }
+  for (int j = lane; j < nu; j += 32) {
+    const size_t u = u0 + j;
+    a.cum[u * (a.k_max + 2) + nr] = carry;
+    a.unit_info[u] = make_int4(nr, carry, n_sum, 0);
+    a.unit_rows[u] = carry + n_sum;
+  }
+  if (lane == 0 && nrout) *nrout = nr;
+}
+
 // Shared memory: votes [n_max] | flag [n_max + 1] | bd [2 n_max + 1] | runs_s, runs_e [n_max + 2] each.
 __global__ void __launch_bounds__(kConsensusThreads) zr_consensus_kernel(StepArgs a, int32_t* __restrict__ votes,
                                                                          int32_t* votes_out, int32_t* ic_out,
@@ -126,7 +180,7 @@ __global__ void __launch_bounds__(kConsensusThreads) zr_consensus_kernel(StepArg
   int* bd = flag + nmax + 1;
   int* runs_s = bd + 2 * nmax + 1;
   int* runs_e = runs_s + nmax + 2;
-  __shared__ int s_cand, s_rstar;
+  __shared__ int s_cand;
   const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int s0 = a.meta.seg_ptr[b];
   const int n = a.meta.seg_ptr[b + 1] - s0;
@@ -192,56 +246,70 @@ __global__ void __launch_bounds__(kConsensusThreads) zr_consensus_kernel(StepArg
       if (last) runs_e[rid] = f == 1 ? bd[2 * i + 1] : bd[2 * i + 2];
       carry += __popc(m);
     }
-    if (lane == 0) s_rstar = prompt_runs + carry;  // run count, before the window search
-  }
-  __syncthreads();
-  const int m = s_rstar;
-  const int W0 = max(0, L - a.window);
-  __syncthreads();
-  for (int r = tid; r < m; r += kConsensusThreads)
-    if (runs_e[r] >= W0 && (r == 0 || runs_e[r - 1] < W0)) s_rstar = r;
-  __syncthreads();
-  const int rstar = s_rstar;
-  const int nr = rstar < m ? rstar + 1 : m + (W0 < L ? 1 : 0);
-  // final ranges and their prefix sums, written for every KV head of the sequence
-  if (warp == 0) {
-    int carry = 0;
-    for (int base = 0; base < nr; base += 32) {
-      const int r = base + lane;
-      int s_ = 0, e_ = 0;
-      if (r < nr) {
-        if (r < rstar) {
-          s_ = runs_s[r];
-          e_ = runs_e[r];
-        } else {
-          s_ = rstar < m ? min(W0, runs_s[rstar]) : W0;
-          e_ = L;
-        }
-      }
-      const int len = e_ - s_;
-      const int incl = warp_inclusive_sum(len, lane);
-      if (r < nr) {
-        for (int g = 0; g < a.Hkv; ++g) {
-          const size_t u = static_cast<size_t>(b) * a.Hkv + g;
-          a.ranges[(u * (a.k_max + 1) + r) * 2] = s_;
-          a.ranges[(u * (a.k_max + 1) + r) * 2 + 1] = e_;
-          a.cum[u * (a.k_max + 2) + r] = carry + incl - len;
-        }
-        if (a.ranges_out) {
-          a.ranges_out[(static_cast<size_t>(b) * (a.k_max + 1) + r) * 2] = s_;
-          a.ranges_out[(static_cast<size_t>(b) * (a.k_max + 1) + r) * 2 + 1] = e_;
-        }
-      }
-      carry += __shfl_sync(kFullMask, incl, 31);
+    __syncwarp();  // every lane's runs are written
+    const int m = prompt_runs + carry;
+    // keep the runs for the steps until the next selection, whose windows move on
+    int32_t* cr = a.cruns + static_cast<size_t>(b) * (nmax + 1) * 2;
+    for (int r = lane; r < m; r += 32) {
+      cr[2 * r] = runs_s[r];
+      cr[2 * r + 1] = runs_e[r];
     }
-    for (int g = lane; g < a.Hkv; g += 32) {
-      const size_t u = static_cast<size_t>(b) * a.Hkv + g;
-      a.cum[u * (a.k_max + 2) + nr] = carry;
-      a.unit_info[u] = make_int4(nr, carry, 0, 0);
-      a.unit_rows[u] = carry;
-    }
-    if (lane == 0 && a.nranges_out) a.nranges_out[b] = nr;
+    if (lane == 0) a.cnruns[b] = m;
+    __syncwarp();
+    emit_ranges(a, runs_s, runs_e, 1, m, max(0, L - a.window), L, static_cast<size_t>(b) * a.Hkv, a.Hkv, 0,
+                a.ranges_out ? a.ranges_out + static_cast<size_t>(b) * (a.k_max + 1) * 2 : nullptr,
+                a.nranges_out ? a.nranges_out + b : nullptr, lane);
   }
+}
+
+// Between selections (consensus plan): the stored runs of sequence b merged with the window of its new
+// length. One warp per sequence; a length below the selection's or past the block table sets the
+// error word and leaves the sequence unchanged.
+__global__ void __launch_bounds__(32) zr_consensus_advance_kernel(StepArgs a, const int32_t* __restrict__ seq_lens) {
+  const int b = blockIdx.x, lane = threadIdx.x;
+  const int L = seq_lens[b];
+  if (L < a.meta.seq_lens[b] || L > a.max_blocks * kBlockTokens) {
+    if (lane == 0) atomicOr(a.err, kErrBadIndex);
+    return;
+  }
+  const int32_t* cr = a.cruns + static_cast<size_t>(b) * (a.n_max + 1) * 2;
+  emit_ranges(a, cr, cr + 1, 2, a.cnruns[b], max(0, L - a.window), L, static_cast<size_t>(b) * a.Hkv, a.Hkv, 0,
+              nullptr, nullptr, lane);
+}
+
+// Between selections (decode plan): unit (b, g)'s runs of touching selected segments, rebuilt from the
+// selection the last decode step stored, merged with the window of the new length. One warp per unit;
+// the summary rows stay those of the selection step.
+__global__ void __launch_bounds__(32) zr_decode_advance_kernel(StepArgs a, const int32_t* __restrict__ seq_lens) {
+  extern __shared__ int asmem[];  // runs_s [k_max + 1] | runs_e [k_max + 1]
+  int* runs_s = asmem;
+  int* runs_e = asmem + a.k_max + 1;
+  const int g = blockIdx.x, b = blockIdx.y, lane = threadIdx.x;
+  const size_t u = static_cast<size_t>(b) * a.Hkv + g;
+  const int L = seq_lens[b];
+  if (L < a.meta.seq_lens[b] || L > a.max_blocks * kBlockTokens) {
+    if (lane == 0 && g == 0) atomicOr(a.err, kErrBadIndex);
+    return;
+  }
+  const int s0 = a.meta.seg_ptr[b];
+  const int n = a.meta.seg_ptr[b + 1] - s0;
+  const int k = a.meta.topk[b];
+  const int32_t* bnd = a.meta.seg_bounds + s0 + b;
+  const int32_t* sel = a.sel + u * a.k_max;
+  int carry = 0;
+  for (int base = 0; base < k; base += 32) {
+    const int j = base + lane;
+    const int seg = j < k ? sel[j] : -1;
+    const bool start = j < k && (j == 0 || sel[j - 1] != seg - 1);
+    const bool last = j < k && (j == k - 1 || sel[j + 1] != seg + 1);
+    const unsigned ms = __ballot_sync(kFullMask, start);
+    const int rid = carry + __popc(ms & ((2u << lane) - 1u)) - 1;
+    if (start) runs_s[rid] = bnd[seg];
+    if (last) runs_e[rid] = bnd[seg + 1];
+    carry += __popc(ms);
+  }
+  __syncwarp();
+  emit_ranges(a, runs_s, runs_e, 1, carry, max(0, L - a.window), L, u, 1, n - k, nullptr, nullptr, lane);
 }
 
 }  // namespace
@@ -299,6 +367,18 @@ zr_status launch_consensus(const Plan& p, const StepArgs& a, int32_t* votes, int
   cudaFuncSetAttribute(zr_consensus_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   zr_consensus_kernel<<<p.B, kConsensusThreads, smem, static_cast<cudaStream_t>(stream)>>>(a, votes, votes_out,
                                                                                            ic_out, p.c_max);
+  return cudaGetLastError() == cudaSuccess ? ZR_OK : ZR_ECUDA;
+}
+
+zr_status launch_decode_advance(const Plan& p, const StepArgs& a, const int32_t* seq_lens, void* stream) {
+  const size_t smem = 2 * static_cast<size_t>(p.k_max + 1) * sizeof(int);
+  cudaFuncSetAttribute(zr_decode_advance_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  zr_decode_advance_kernel<<<dim3(p.Hkv, p.B), 32, smem, static_cast<cudaStream_t>(stream)>>>(a, seq_lens);
+  return cudaGetLastError() == cudaSuccess ? ZR_OK : ZR_ECUDA;
+}
+
+zr_status launch_consensus_advance(const Plan& p, const StepArgs& a, const int32_t* seq_lens, void* stream) {
+  zr_consensus_advance_kernel<<<p.B, 32, 0, static_cast<cudaStream_t>(stream)>>>(a, seq_lens);
   return cudaGetLastError() == cudaSuccess ? ZR_OK : ZR_ECUDA;
 }
 

@@ -45,6 +45,8 @@ struct WsLayout {
   size_t part_o;      // float [U + attend_warps][G][d] unnormalised split outputs
   size_t part_ml;     // float [U + attend_warps][G][2] split (max, sum) in log2 units
   size_t votes;       // consensus only: int32 [B][n_max] vote counts, zero between selections
+  size_t cruns;       // consensus only: int32 [B][n_max + 1][2] the last selection's runs before the window
+  size_t cnruns;      // consensus only: int32 [B] their count
   size_t total;
 };
 
@@ -89,6 +91,8 @@ struct StepArgs {
   int32_t* sel;
   float* part_o;
   float2* part_ml;
+  int32_t* cruns;   // consensus only
+  int32_t* cnruns;  // consensus only
   int B, Hq, Hkv, G, window, num_blocks, max_blocks, k_max, n_max, attend_warps;
   float scale_log2;  // log2(e) / sqrt(d)
 };
@@ -116,6 +120,9 @@ size_t consensus_smem_bytes(int n_max);
 zr_status launch_vote(const Plan& p, const StepArgs& a, const void* mean_keys, int32_t* votes, void* stream);
 zr_status launch_consensus(const Plan& p, const StepArgs& a, int32_t* votes, int32_t* votes_out, int32_t* ic_out,
                            void* stream);
+// Between selections: rebuild every unit's token ranges for new sequence lengths (device int32 [B]).
+zr_status launch_decode_advance(const Plan& p, const StepArgs& a, const int32_t* seq_lens, void* stream);
+zr_status launch_consensus_advance(const Plan& p, const StepArgs& a, const int32_t* seq_lens, void* stream);
 
 }  // namespace zr
 

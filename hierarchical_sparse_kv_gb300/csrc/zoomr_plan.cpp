@@ -125,7 +125,10 @@ void layout_workspace(zr::Plan& p) {
   p.ws.sel = take(U * p.k_max * sizeof(int32_t));
   p.ws.part_o = take(slots * p.G * p.d * sizeof(float));
   p.ws.part_ml = take(slots * p.G * 2 * sizeof(float));
-  p.ws.votes = p.mode == zr::kConsensusPlan ? take(static_cast<size_t>(p.B) * p.n_max * sizeof(int32_t)) : 0;
+  const bool cons = p.mode == zr::kConsensusPlan;
+  p.ws.votes = cons ? take(static_cast<size_t>(p.B) * p.n_max * sizeof(int32_t)) : 0;
+  p.ws.cruns = cons ? take(static_cast<size_t>(p.B) * (p.n_max + 1) * 2 * sizeof(int32_t)) : 0;
+  p.ws.cnruns = cons ? take(static_cast<size_t>(p.B) * sizeof(int32_t)) : 0;
   p.ws.total = off;
 }
 
@@ -275,6 +278,8 @@ StepArgs step_args(const Plan& p, void* workspace) {
   a.sel = reinterpret_cast<int32_t*>(ws + p.ws.sel);
   a.part_o = reinterpret_cast<float*>(ws + p.ws.part_o);
   a.part_ml = reinterpret_cast<float2*>(ws + p.ws.part_ml);
+  a.cruns = p.mode == kConsensusPlan ? reinterpret_cast<int32_t*>(ws + p.ws.cruns) : nullptr;
+  a.cnruns = p.mode == kConsensusPlan ? reinterpret_cast<int32_t*>(ws + p.ws.cnruns) : nullptr;
   a.B = p.B;
   a.Hq = p.Hq;
   a.Hkv = p.Hkv;
@@ -498,6 +503,41 @@ zr_status zr_consensus_attend(zr_plan_t plan, void* workspace, const void* q, co
   a.sum_v = v_pool;
   a.out = out;
   return zr::launch_attend_only(plan->p, a, stream);
+}
+
+}  // extern "C"
+
+extern "C" {
+
+zr_status zr_decode_advance(zr_plan_t plan, void* workspace, const int32_t* seq_lens, void* stream) {
+  if (!plan || !workspace || !seq_lens || plan->p.mode != zr::kDecodePlan) return ZR_EINVAL;
+  if (!aligned(workspace, 256) || !aligned(seq_lens, 4)) return ZR_EINVAL;
+  return zr::launch_decode_advance(plan->p, zr::step_args(plan->p, workspace), seq_lens, stream);
+}
+
+zr_status zr_decode_attend_reuse(zr_plan_t plan, void* workspace, const void* q, const void* k_pool,
+                                 const void* v_pool, const int32_t* block_tables, const void* sum_k,
+                                 const void* sum_v, float* out, void* stream) {
+  if (!plan || !workspace || !q || !k_pool || !v_pool || !block_tables || !sum_k || !sum_v || !out) return ZR_EINVAL;
+  if (plan->p.mode != zr::kDecodePlan) return ZR_EINVAL;
+  if (!aligned(workspace, 256) || !aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) ||
+      !aligned(sum_k, 16) || !aligned(sum_v, 16) || !aligned(out, 16) || !aligned(block_tables, 4))
+    return ZR_EINVAL;
+  zr::StepArgs a = zr::step_args(plan->p, workspace);
+  a.q = q;
+  a.k_pool = k_pool;
+  a.v_pool = v_pool;
+  a.block_tables = block_tables;
+  a.sum_k = sum_k;
+  a.sum_v = sum_v;
+  a.out = out;
+  return zr::launch_attend_only(plan->p, a, stream);
+}
+
+zr_status zr_consensus_advance(zr_plan_t plan, void* workspace, const int32_t* seq_lens, void* stream) {
+  if (!plan || !workspace || !seq_lens || plan->p.mode != zr::kConsensusPlan) return ZR_EINVAL;
+  if (!aligned(workspace, 256) || !aligned(seq_lens, 4)) return ZR_EINVAL;
+  return zr::launch_consensus_advance(plan->p, zr::step_args(plan->p, workspace), seq_lens, stream);
 }
 
 }  // extern "C"

@@ -84,6 +84,12 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.zr_consensus_select.restype = ctypes.c_int
     lib.zr_consensus_attend.argtypes = [_P] * 8
     lib.zr_consensus_attend.restype = ctypes.c_int
+    lib.zr_decode_advance.argtypes = [_P] * 4
+    lib.zr_decode_advance.restype = ctypes.c_int
+    lib.zr_decode_attend_reuse.argtypes = [_P] * 10
+    lib.zr_decode_attend_reuse.restype = ctypes.c_int
+    lib.zr_consensus_advance.argtypes = [_P] * 4
+    lib.zr_consensus_advance.restype = ctypes.c_int
     lib.zr_free.argtypes = [_P]
     lib.zr_free.restype = None
     lib.zr_status_string.argtypes = [ctypes.c_int]
@@ -335,6 +341,20 @@ class DecodePlan:
         zr_decode_attend_timed(self.handle, self.ws, q, k_pool, v_pool, block_tables, sum_k, sum_v, out, ev_start,
                                ev_stop, stream)
 
+    def advance(self, seq_lens: torch.Tensor, stream=None) -> None:
+        """Move every unit's window to the new lengths (device int32 [B]), the selection held fixed."""
+        _check_rows("seq_lens", seq_lens, (self.batch,), torch.int32)
+        st = load().zr_decode_advance(self.handle, _dev(self.ws), _dev(seq_lens), _stream(stream))
+        if st != ZR_OK:
+            raise ZoomrError(st, "zr_decode_advance")
+
+    def run_reuse(self, q, k_pool, v_pool, block_tables, sum_k, sum_v, out, stream=None) -> None:
+        """Gather-attention and merge over the ranges in the workspace (no scoring or selection)."""
+        st = load().zr_decode_attend_reuse(self.handle, _dev(self.ws), _dev(q), _pool(k_pool), _pool(v_pool),
+                                           _dev(block_tables), _dev(sum_k), _dev(sum_v), _dev(out), _stream(stream))
+        if st != ZR_OK:
+            raise ZoomrError(st, "zr_decode_attend_reuse")
+
     def device_error(self, stream=None) -> int:
         return zr_get_device_error(self.handle, self.ws, stream)
 
@@ -429,6 +449,13 @@ class ConsensusPlan:
                                         _dev(block_tables), _dev(out), _stream(stream))
         if st != ZR_OK:
             raise ZoomrError(st, "zr_consensus_attend")
+
+    def advance(self, seq_lens: torch.Tensor, stream=None) -> None:
+        """Move every sequence's window to the new lengths (device int32 [B]), I_c and I_s held fixed."""
+        _check_rows("seq_lens", seq_lens, (self.batch,), torch.int32)
+        st = load().zr_consensus_advance(self.handle, _dev(self.ws), _dev(seq_lens), _stream(stream))
+        if st != ZR_OK:
+            raise ZoomrError(st, "zr_consensus_advance")
 
     def device_error(self, stream=None) -> int:
         return zr_get_device_error(self.handle, self.ws, stream)

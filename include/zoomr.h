@@ -331,6 +331,46 @@ ZR_API zr_status zr_consensus_select(zr_plan_t plan, void* workspace, int32_t* v
 ZR_API zr_status zr_consensus_attend(zr_plan_t plan, void* workspace, const void* q, const void* k_pool,
                                      const void* v_pool, const int32_t* block_tables, float* out, void* stream);
 
+/*
+ * ------------------------------------------- steps between selections (amortisation)
+ * ZoomR page, 3.4 "Decoding Stage" and appendix A.3 "Semantic Boundaries": the
+ * selection is recomputed only at semantic boundaries (about every 35 tokens)
+ * and reused for the steps in between. Between two selections the selected parts
+ * stay fixed and the recent window follows the newest token: with L' cached
+ * tokens it is [max(0, L' - w), L'). Tokens appended since the selection belong to
+ * no segment and are reached only through the window.
+ *
+ * seq_lens is a DEVICE int32 array [B] of the new lengths L'_b. Each must lie in
+ * [L_b of the plan, 16 * max_blocks_per_seq]; otherwise bit 2 of the workspace
+ * error word is set and that sequence keeps its previous token ranges. The calls
+ * are asynchronous on `stream` and allocate nothing.
+ */
+
+/*
+ * zr_decode_advance -- rebuild every unit's token ranges from the selection the
+ * last zr_decode_attend stored in the workspace (its selected segments) and the
+ * window of the new lengths; the summary rows stay those of that selection.
+ */
+ZR_API zr_status zr_decode_advance(zr_plan_t plan, void* workspace, const int32_t* seq_lens, void* stream);
+
+/*
+ * zr_decode_attend_reuse -- the gather-attention and merge of zr_decode_attend
+ * over the token ranges and summary rows currently in the workspace (from the
+ * last zr_decode_attend or zr_decode_advance); no scoring or selection. Same
+ * arguments as zr_decode_attend without the debug outputs.
+ */
+ZR_API zr_status zr_decode_attend_reuse(zr_plan_t plan, void* workspace, const void* q, const void* k_pool,
+                                        const void* v_pool, const int32_t* block_tables, const void* sum_k,
+                                        const void* sum_v, float* out, void* stream);
+
+/*
+ * zr_consensus_advance -- the consensus path's final sets for the new lengths:
+ * the prompt, zoomed regular segments and candidate summary segments of the last
+ * zr_consensus_select, with the window of the new lengths. zr_consensus_attend
+ * then attends over them.
+ */
+ZR_API zr_status zr_consensus_advance(zr_plan_t plan, void* workspace, const int32_t* seq_lens, void* stream);
+
 /* zr_free -- release the plan and its small device metadata (NULL is a no-op). */
 ZR_API void zr_free(zr_plan_t plan);
 
