@@ -12,6 +12,7 @@ steps.
   python bench.py --path append      # the cache-update path: token appends and segment summaries
   python bench.py --path consensus   # ZoomR's consensus selection and attention over its final set
   python bench.py --path offload     # the decode step with the K/V pools in pinned host memory
+  python bench.py --path generate    # the consensus path as a decode loop (appends, advance, periodic selection)
 
 Prints one JSON line (rank 0). Under torchrun each rank runs its own replica of
 the workload on its own GPU (weak scaling) and the reported time is the max over
@@ -931,6 +932,157 @@ def run_consensus(args):
     return 0
 
 
+# ---------------------------------------------------------------------- generation loop
+GENERATE_METRIC = ("ZoomR generation steps/s at 8B shape, 512-token prompt + 16K generated, batch 8, 32 layers: every "
+                   "step appends each layer's K/V and moves the window, every 35th step also votes and selects")
+
+
+def run_generate(args):
+    """The consensus path as a decode loop: each step appends every layer's new K/V row (zr_append_kv), moves
+    the windows to the new lengths (zr_consensus_advance) and attends every layer (zr_consensus_attend); every
+    35th step first votes in every layer and selects (zr_consensus_vote, zr_consensus_select). The lengths live
+    on the device and grow by one per step inside the captured graphs, so consecutive replays are consecutive
+    steps."""
+    spec = W.CONSENSUS_WORKLOADS[1]
+    world, rank, local = dist_setup(args.gpus)
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: the generation loop needs a CUDA GPU")
+    from hierarchical_sparse_kv_gb300 import build as B
+    from hierarchical_sparse_kv_gb300 import zoomr as Z
+
+    if rank == 0 or world == 1:
+        B.build()
+    barrier(world)
+    Z.load()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    T = SELECTION_INTERVAL
+    rounds_total = args.steps + args.warmup + 2
+    room = T * rounds_total + 1
+    st0 = W.make_consensus_structure(spec, spare_blocks=spec.batch * (room // 16 + 2))
+    Lg = st0.seq_lens.astype(np.int64) + room
+    cols = int(((Lg + 15) // 16).max())
+    tables = np.full((st0.batch, cols), -1, np.int32)
+    tables[:, :st0.max_blocks_per_seq] = st0.block_tables
+    used = set(st0.block_tables.ravel().tolist())
+    free = [x for x in range(st0.num_blocks) if x not in used]
+    for b in range(st0.batch):
+        for j in range(int((Lg[b] + 15) // 16)):
+            if tables[b, j] < 0:
+                tables[b, j] = free.pop(0)
+    import dataclasses
+    st = dataclasses.replace(st0, block_tables=tables)
+    L = spec.layers if args.layers is None else max(1, min(args.layers, spec.layers))
+    Bn, H, Hq, d = st.batch, spec.num_kv_heads, spec.num_q_heads, spec.head_dim
+    dt = W.torch_dtype(spec.dtype)
+    lts = [W.make_consensus_layer(st, l, dev) for l in range(L)]
+    bt = torch.from_numpy(st.block_tables).to(dev)
+    cfg = Z.cache_config(batch=Bn, num_kv_heads=H, head_dim=d, num_blocks=st.num_blocks,
+                         max_blocks_per_seq=st.max_blocks_per_seq, dtype=spec.dtype)
+    segs = torch.tensor([(b, s, e, int(st.seg_ptr[b]) + i) for b in range(Bn)
+                         for i, (s, e) in enumerate(st.summary_spans(b))], dtype=torch.int32, device=dev)
+    mks = []
+    for lt in lts:
+        mk = torch.empty((st.total_segments, H, d), dtype=dt, device=dev)
+        Z.zr_segment_summaries(cfg, segs, bt, lt.k_pool, lt.v_pool, mk, torch.empty_like(mk))
+        mks.append(mk)
+    plan = Z.ConsensusPlan.from_structure(st, device=dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(spec.seed + 1)
+    kn = torch.randn((L, Bn, H, d), generator=gen, device=dev).to(dt)
+    vn = torch.randn((L, Bn, H, d), generator=gen, device=dev).to(dt)
+    q_all = torch.stack([lt.q for lt in lts])
+    out_all = torch.empty((L, Bn, Hq, d), dtype=torch.float32, device=dev)
+    lens = torch.from_numpy(st.seq_lens.astype(np.int32)).to(dev)
+    pos = torch.empty_like(lens)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(boundary, s):
+        lens.add_(1)
+        torch.sub(lens, 1, out=pos)
+        for l in range(L):
+            Z.zr_append_kv(cfg, pos, kn[l], vn[l], bt, lts[l].k_pool, lts[l].v_pool, stream=s)
+        if boundary:
+            for l in range(L):
+                plan.vote(q_all[l], mks[l], stream=s)
+            plan.select(stream=s)
+        plan.advance(lens, stream=s)
+        for l in range(L):
+            plan.attend(q_all[l], lts[l].k_pool, lts[l].v_pool, bt, out_all[l], stream=s)
+
+    stream.wait_stream(torch.cuda.current_stream())
+    graphs = {}
+    with torch.cuda.stream(stream):
+        step(True, stream)  # eager: the first selection, and warm-up
+        for kind in (True, False):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                step(kind, stream)
+            graphs[kind] = g
+    torch.cuda.synchronize()
+    # the captures ran nothing: the lengths moved once (the eager step)
+
+    def rounds(n, e2e=False, host_q=None, host_out=None):
+        with torch.cuda.stream(stream):
+            for _ in range(n):
+                for i in range(T):
+                    if e2e:
+                        q_all.copy_(host_q, non_blocking=True)
+                    graphs[i == 0].replay()
+                    if e2e:
+                        host_out.copy_(out_all, non_blocking=True)
+
+    rounds(args.warmup)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = ClockSampler(dev.index) if rank == 0 else None
+    time.sleep(0.25 if clocks and clocks.proc else 0)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    rounds(args.steps)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop() if clocks else None
+    ms = max_over_ranks(e0.elapsed_time(e1) / (args.steps * T), world)
+    host_q = q_all.cpu().pin_memory()
+    host_out = torch.empty(out_all.shape, dtype=out_all.dtype).pin_memory()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    rounds(1, True, host_q, host_out)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / T, world)
+    final_len = lens.cpu().numpy()
+    assert int(final_len[0]) <= int(st.seq_lens[0]) + room, "ran past the block tables' room"
+    assert plan.device_error() == 0, "device error word set"
+    launches_regular = 3 + 3 * L
+    launches_boundary = launches_regular + L + 1
+    line = {
+        "impl": "zoomr", "path": "generate", "metric": GENERATE_METRIC, "value": world * 1e3 / ms, "unit": "steps/s",
+        "n_gpus": world, "steps": args.steps * T, "warmup": args.warmup * T, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": spec.dtype,
+        "data": "synthetic (seeded N(0,1) K/V and new rows, queries near one summary segment's mean key)",
+        "config": {"workload": spec.name + ("" if L == spec.layers else f"_first{L}layers") + "_generate",
+                   "batch": Bn, "prompt": spec.prompt_len, "generated_at_start": spec.gen_len, "layers": L,
+                   "q_heads": Hq, "kv_heads": H, "head_dim": d, "top_k": spec.topk, "consensus": spec.consensus,
+                   "window": spec.window, "selection_interval": T, "graph": True,
+                   "tokens_appended": int(final_len[0] - st.seq_lens[0]),
+                   "l2": "each step reads the 32 layers' final sets (far beyond L2); no flush"},
+        "e2e": {"value": world * 1e3 / e2e_ms, "unit": "steps/s", "h2d_bytes_per_step": host_q.numel() * 2,
+                "d2h_bytes_per_step": host_out.numel() * 4},
+        "gpu_launches": int(args.steps * ((T - 1) * launches_regular + launches_boundary)),
+        "clocks": clk,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    plan.close()
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -945,10 +1097,11 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle work for cpu_baseline, once on one core and once on all cores")
     ap.add_argument("--ref-units", type=int, default=16, help="oracle units per reference-arm step")
-    ap.add_argument("--path", choices=["decode", "append", "consensus", "offload"], default="decode",
+    ap.add_argument("--path", choices=["decode", "append", "consensus", "offload", "generate"], default="decode",
                     help="decode: the headline decode step; append: the cache-update path (appends and summaries); "
                          "consensus: ZoomR's own consensus selection and attention over its final set; offload: the "
-                         "decode step with the K/V pools in pinned host memory")
+                         "decode step with the K/V pools in pinned host memory; generate: the consensus path as a "
+                         "decode loop (appends, window advance, a selection every 35 steps)")
     ap.add_argument("--layers", type=int, default=None,
                     help="append and consensus paths only: run the first N layers (a small case for profiling; "
                          "the metrics are defined on all 32)")
@@ -959,6 +1112,8 @@ def main(argv=None):
         return run_reference(args)
     if args.path == "append":
         return run_append(args)
+    if args.path == "generate":
+        return run_generate(args)
     return run_consensus(args) if args.path == "consensus" else run_zoomr(args)
 
 
