@@ -27,19 +27,13 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+zr_status validate_shape(const zr_config* c);
+
 zr_status validate(const zr_config* c, const int32_t* seq_lens, const int32_t* seg_ptr, const int32_t* seg_bounds,
                    const int32_t* topk) {
   if (!c || !seq_lens || !seg_ptr || !seg_bounds || !topk) return ZR_EINVAL;
-  if (c->batch < 1 || c->num_q_heads < 1 || c->num_kv_heads < 1) return ZR_EINVAL;
-  if (c->num_q_heads % c->num_kv_heads != 0) return ZR_EINVAL;
-  if (c->block_size != zr::kBlockTokens) return ZR_EINVAL;
-  if (c->num_blocks < 1 || c->max_blocks_per_seq < 1 || c->window < 0) return ZR_EINVAL;
-  if (c->dtype != ZR_F32 && c->dtype != ZR_BF16) return ZR_EINVAL;
-  if (c->head_dim != 64 && c->head_dim != 128) return c->head_dim < 1 ? ZR_EINVAL : ZR_EUNSUPPORTED;
-  if (c->num_q_heads / c->num_kv_heads > zr::kMaxGroup) return ZR_EUNSUPPORTED;
-  // Row ids of the pool are (block * Hkv + head) * 16 + slot and must stay below 2^31.
-  if (static_cast<int64_t>(c->num_blocks) * c->num_kv_heads * zr::kBlockTokens >= (int64_t(1) << 31))
-    return ZR_EUNSUPPORTED;
+  const zr_status st = validate_shape(c);
+  if (st != ZR_OK) return st;
   if (seg_ptr[0] != 0) return ZR_EINVAL;
   for (int b = 0; b < c->batch; ++b) {
     const int32_t L = seq_lens[b];
@@ -62,7 +56,8 @@ zr_status validate(const zr_config* c, const int32_t* seq_lens, const int32_t* s
   return ZR_OK;
 }
 
-// The shape checks shared by both plan kinds.
+// The shape checks shared by both plan kinds. Row ids of the pool are (block * Hkv + head) * 16 + slot
+// and must stay below 2^31.
 zr_status validate_shape(const zr_config* c) {
   if (c->batch < 1 || c->num_q_heads < 1 || c->num_kv_heads < 1) return ZR_EINVAL;
   if (c->num_q_heads % c->num_kv_heads != 0) return ZR_EINVAL;

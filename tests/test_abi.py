@@ -182,3 +182,9 @@ def test_consensus_entry_points_reject_null_arguments(lib):
     assert lib.zr_consensus_select(None, None, None, None, None, None, None) == Z.ZR_EINVAL
     assert lib.zr_consensus_attend(*([None] * 8)) == Z.ZR_EINVAL
     assert lib.zr_consensus_dims(None, None, None) == Z.ZR_EINVAL
+
+
+def test_steps_between_selections_reject_null_arguments(lib):
+    assert lib.zr_decode_advance(None, None, None, None) == Z.ZR_EINVAL
+    assert lib.zr_decode_attend_reuse(*([None] * 10)) == Z.ZR_EINVAL
+    assert lib.zr_consensus_advance(None, None, None, None) == Z.ZR_EINVAL
