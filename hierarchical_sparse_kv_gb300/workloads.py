@@ -124,6 +124,7 @@ class WorkloadSpec:
     shared_prefix_tokens: int = 0
     peaky_query: bool = False
     seed: int = 0
+    sink_tokens: int = 0  # prompt tokens kept as an attention sink; the segments partition [sink, L)
 
 
 WORKLOADS: Dict[int, WorkloadSpec] = {
@@ -151,6 +152,7 @@ class Structure:
     num_blocks: int
     block_tables: np.ndarray  # int32 [B, max_blocks_per_seq], unused entries -1
     ref_count: np.ndarray  # int64 [num_blocks] after construction
+    sink_lens: Optional[np.ndarray] = None  # int32 [B] attention-sink tokens, or None (no sink)
 
     @property
     def batch(self) -> int:
@@ -199,9 +201,10 @@ def make_structure(spec: WorkloadSpec, *, seq_lens: Optional[Sequence[int]] = No
     lens = np.maximum(lens, spec.shared_prefix_tokens + 1) if spec.shared_prefix_tokens else lens
 
     bounds_list = []
+    sink = int(spec.sink_tokens)
     for b in range(B):
         lo, hi = spec.seg_len_range
-        bounds_list.append(_draw_segments(rng, int(lens[b]), lo, hi))
+        bounds_list.append(_draw_segments(rng, int(lens[b]) - sink, lo, hi) + sink)
     n_seg = np.array([len(x) - 1 for x in bounds_list], dtype=np.int64)
     seg_ptr = np.concatenate([[0], np.cumsum(n_seg)]).astype(np.int32)
     seg_bounds = np.concatenate(bounds_list).astype(np.int32)
@@ -225,7 +228,7 @@ def make_structure(spec: WorkloadSpec, *, seq_lens: Optional[Sequence[int]] = No
         own = own + alloc.alloc(int(nblk[b]) - P)
         tables[b, :len(own)] = own
     return Structure(spec, lens.astype(np.int32), seg_ptr, seg_bounds, topk, spec.window, num_blocks, tables,
-                     alloc.ref_count.copy())
+                     alloc.ref_count.copy(), np.full(B, sink, np.int32) if sink else None)
 
 
 # --------------------------------------------------------------------------
@@ -248,11 +251,10 @@ class LayerTensors:
 
 def _segment_means(x: torch.Tensor, bounds: np.ndarray) -> torch.Tensor:
     """fp64 mean over each segment [bounds[i], bounds[i+1]) of rows of x [L, H, d]."""
-    L = x.shape[0]
     lens = np.diff(bounds)
     seg_id = torch.from_numpy(np.repeat(np.arange(len(lens)), lens)).to(x.device)
     acc = torch.zeros((len(lens),) + tuple(x.shape[1:]), dtype=torch.float64, device=x.device)
-    acc.index_add_(0, seg_id, x[:L].to(torch.float64))
+    acc.index_add_(0, seg_id, x[int(bounds[0]):int(bounds[-1])].to(torch.float64))
     return acc / torch.from_numpy(lens.astype(np.float64)).to(x.device).view(-1, 1, 1)
 
 
