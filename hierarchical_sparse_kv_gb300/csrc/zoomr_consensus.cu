@@ -278,8 +278,8 @@ __global__ void __launch_bounds__(32) zr_consensus_advance_kernel(StepArgs a, co
 }
 
 // Between selections (decode plan): unit (b, g)'s runs of touching selected segments, rebuilt from the
-// selection the last decode step stored, merged with the window of the new length. One warp per unit;
-// the summary rows stay those of the selection step.
+// selection the last decode step stored (with the sink's run first, for plans with a sink), merged with
+// the window of the new length. One warp per unit; the summary rows stay those of the selection step.
 __global__ void __launch_bounds__(32) zr_decode_advance_kernel(StepArgs a, const int32_t* __restrict__ seq_lens) {
   extern __shared__ int asmem[];  // runs_s [k_max + 1] | runs_e [k_max + 1]
   int* runs_s = asmem;
@@ -309,7 +309,35 @@ __global__ void __launch_bounds__(32) zr_decode_advance_kernel(StepArgs a, const
     carry += __popc(ms);
   }
   __syncwarp();
-  emit_ranges(a, runs_s, runs_e, 1, carry, max(0, L - a.window), L, u, 1, n - k, nullptr, nullptr, lane);
+  int m = carry;
+  const int Ns = a.meta.prompt_lens[b];  // the sink of a plan with one, else 0
+  if (Ns > 0) {
+    if (m > 0 && runs_s[0] <= Ns) {
+      if (lane == 0) runs_s[0] = 0;  // the first segment (it begins at Ns) is selected: one run
+    } else {
+      for (int base = (m / 32) * 32; base >= 0; base -= 32) {
+        const int r = base + lane;
+        int s_ = 0, e_ = 0;
+        if (r < m) {
+          s_ = runs_s[r];
+          e_ = runs_e[r];
+        }
+        __syncwarp();
+        if (r < m) {
+          runs_s[r + 1] = s_;
+          runs_e[r + 1] = e_;
+        }
+        __syncwarp();
+      }
+      if (lane == 0) {
+        runs_s[0] = 0;
+        runs_e[0] = Ns;
+      }
+      ++m;
+    }
+    __syncwarp();
+  }
+  emit_ranges(a, runs_s, runs_e, 1, m, max(0, L - a.window), L, u, 1, n - k, nullptr, nullptr, lane);
 }
 
 }  // namespace

@@ -148,6 +148,59 @@ __device__ int block_exclusive_scan(int v, int* total) {
 }
 
 // ------------------------------------------------------------------ select
+// One warp: unit u's ranges [0, nr) and prefix sums (global, written by this CTA) gain the sink
+// [0, Ns), which lies before every segment: it merges into range 0 if that starts at or before
+// Ns, else every range moves up one slot (the plan reserves it) and the sink becomes range 0.
+__device__ void add_sink_range(const StepArgs& a, int u, int Ns, int32_t* rg, int32_t* cum, int32_t* rout, int lane) {
+  int4 info = a.unit_info[u];
+  const int nr = info.x;
+  int added;
+  if (nr > 0 && rg[0] <= Ns) {
+    added = rg[0];
+    __syncwarp();
+    if (lane == 0) rg[0] = 0;
+    for (int r = 1 + lane; r <= nr; r += 32) cum[r] += added;
+  } else {
+    added = Ns;
+    // move ranges and prefix sums up one slot, highest chunk first
+    for (int base = (nr / 32) * 32; base >= 0; base -= 32) {
+      const int r = base + lane;
+      int s_ = 0, e_ = 0, c_ = 0;
+      if (r < nr) {
+        s_ = rg[2 * r];
+        e_ = rg[2 * r + 1];
+      }
+      if (r <= nr) c_ = cum[r];
+      __syncwarp();
+      if (r < nr) {
+        rg[2 * (r + 1)] = s_;
+        rg[2 * (r + 1) + 1] = e_;
+      }
+      if (r <= nr) cum[r + 1] = c_ + Ns;
+      __syncwarp();
+    }
+    if (lane == 0) {
+      rg[0] = 0;
+      rg[1] = Ns;
+      cum[0] = 0;
+    }
+    info.x = nr + 1;
+  }
+  __syncwarp();
+  const int nr2 = info.x;
+  if (rout)
+    for (int r = lane; r < nr2; r += 32) {
+      rout[2 * r] = rg[2 * r];
+      rout[2 * r + 1] = rg[2 * r + 1];
+    }
+  if (lane == 0) {
+    info.y += added;
+    a.unit_info[u] = info;
+    a.unit_rows[u] += added;
+    if (a.nranges_out) a.nranges_out[u] = nr2;
+  }
+}
+
 // Shared memory: q [kMaxGroup][D+4] f32 | staged summary-key rows, raw, kStageRows x (D*sizeof(T)+16)
 //   | pair values [kStageRows][kMaxGroup] | keys [n_max+4] | flag [n_max+2] | bounds [n_max+1] | list [n_max] | runs_s [n_max] | runs_e [n_max]
 // The 16-byte row pad keeps the threads' row reads in different banks.
@@ -444,6 +497,14 @@ __global__ void __launch_bounds__(kSelectThreads) zr_select_kernel(StepArgs a) {
       a.unit_rows[u] = n_tok + n - k;
       if (a.nranges_out) a.nranges_out[u] = nr;
     }
+  }
+  // 4. the prompt kept as an attention sink (sequences planned with one): [0, Ns) joins the token
+  //    ranges -- merged into the first range when that one starts at or before Ns (the first
+  //    segment, which begins at Ns, is selected, or the window reaches the prompt), else prepended.
+  const int Ns = a.meta.prompt_lens[b];
+  if (Ns > 0) {
+    __syncthreads();  // this CTA's ranges, prefix sums and unit sizes are written
+    if (tid < 32) add_sink_range(a, u, Ns, rg, cum, rout, tid);
   }
   if (a.sel_out) {
     int* so = a.sel_out + static_cast<size_t>(u) * a.k_max;

@@ -30,7 +30,7 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 zr_status validate_shape(const zr_config* c);
 
 zr_status validate(const zr_config* c, const int32_t* seq_lens, const int32_t* seg_ptr, const int32_t* seg_bounds,
-                   const int32_t* topk) {
+                   const int32_t* topk, const int32_t* sink_lens) {
   if (!c || !seq_lens || !seg_ptr || !seg_bounds || !topk) return ZR_EINVAL;
   const zr_status st = validate_shape(c);
   if (st != ZR_OK) return st;
@@ -49,7 +49,8 @@ zr_status validate(const zr_config* c, const int32_t* seq_lens, const int32_t* s
   for (int b = 0; b < c->batch; ++b) {
     const int32_t* bd = seg_bounds + seg_ptr[b] + b;
     const int n = seg_ptr[b + 1] - seg_ptr[b];
-    if (bd[0] != 0 || bd[n] != seq_lens[b]) return ZR_EINVAL;
+    const int32_t sink = sink_lens ? sink_lens[b] : 0;
+    if (sink < 0 || bd[0] != sink || bd[n] != seq_lens[b]) return ZR_EINVAL;
     for (int i = 0; i < n; ++i)
       if (bd[i + 1] <= bd[i]) return ZR_EINVAL;
   }
@@ -127,16 +128,37 @@ void layout_workspace(zr::Plan& p) {
   p.ws.total = off;
 }
 
+zr_status make_decode_plan(const zr_config* cfg, const int32_t* seq_lens, const int32_t* seg_ptr,
+                           const int32_t* seg_bounds, const int32_t* topk, const int32_t* sink_lens,
+                           zr_plan_t* out_plan, size_t* workspace_bytes);
+
 }  // namespace
 
 extern "C" {
 
 zr_status zr_plan(const zr_config* cfg, const int32_t* seq_lens, const int32_t* seg_ptr, const int32_t* seg_bounds,
                   const int32_t* topk, zr_plan_t* out_plan, size_t* workspace_bytes) {
+  return make_decode_plan(cfg, seq_lens, seg_ptr, seg_bounds, topk, nullptr, out_plan, workspace_bytes);
+}
+
+zr_status zr_plan_sink(const zr_config* cfg, const int32_t* seq_lens, const int32_t* sink_lens,
+                       const int32_t* seg_ptr, const int32_t* seg_bounds, const int32_t* topk, zr_plan_t* out_plan,
+                       size_t* workspace_bytes) {
+  if (!sink_lens) return ZR_EINVAL;
+  return make_decode_plan(cfg, seq_lens, seg_ptr, seg_bounds, topk, sink_lens, out_plan, workspace_bytes);
+}
+
+}  // extern "C"
+
+namespace {
+
+zr_status make_decode_plan(const zr_config* cfg, const int32_t* seq_lens, const int32_t* seg_ptr,
+                           const int32_t* seg_bounds, const int32_t* topk, const int32_t* sink_lens,
+                           zr_plan_t* out_plan, size_t* workspace_bytes) {
   if (!out_plan || !workspace_bytes) return ZR_EINVAL;
   *out_plan = nullptr;
   *workspace_bytes = 0;
-  zr_status st = validate(cfg, seq_lens, seg_ptr, seg_bounds, topk);
+  zr_status st = validate(cfg, seq_lens, seg_ptr, seg_bounds, topk, sink_lens);
   if (st != ZR_OK) return st;
 
   struct zr_plan* P = new (std::nothrow) struct zr_plan();
@@ -160,6 +182,7 @@ zr_status zr_plan(const zr_config* cfg, const int32_t* seq_lens, const int32_t* 
   p.k_max = 1;
   p.n_max = 1;
   int64_t rows_bound = 0;
+  bool any_sink = false;
   for (int b = 0; b < p.B; ++b) {
     const int n = seg_ptr[b + 1] - seg_ptr[b];
     const int32_t* bd = seg_bounds + seg_ptr[b] + b;
@@ -172,9 +195,12 @@ zr_status zr_plan(const zr_config* cfg, const int32_t* seq_lens, const int32_t* 
     std::sort(lens.begin(), lens.end(), std::greater<int32_t>());
     int64_t top = 0;
     for (int i = 0; i < kclip[b]; ++i) top += lens[i];
-    const int64_t tok_bound = std::min<int64_t>(L, std::min<int64_t>(p.window, L) + top);
+    const int32_t sink = sink_lens ? sink_lens[b] : 0;
+    const int64_t tok_bound = std::min<int64_t>(L, sink + std::min<int64_t>(p.window, L) + top);
     rows_bound += (tok_bound + (n - kclip[b])) * p.Hkv;
+    any_sink = any_sink || sink > 0;
   }
+  if (any_sink) ++p.k_max;  // one more range slot per unit for the sink's range
   if (cudaGetDevice(&p.device) != cudaSuccess) {
     cudaGetLastError();
     delete P;
@@ -197,7 +223,8 @@ zr_status zr_plan(const zr_config* cfg, const int32_t* seq_lens, const int32_t* 
     moff = align_up(moff + count * sizeof(int32_t), 256);
     return at;
   };
-  const size_t o_len = mtake(nb), o_ptr = mtake(nb + 1), o_bnd = mtake(n_bounds), o_topk = mtake(nb);
+  const size_t o_len = mtake(nb), o_ptr = mtake(nb + 1), o_bnd = mtake(n_bounds), o_topk = mtake(nb),
+               o_sink = mtake(nb);
   void* base = nullptr;
   cudaError_t ce = cudaMalloc(&base, moff);
   if (ce != cudaSuccess) {
@@ -211,10 +238,14 @@ zr_status zr_plan(const zr_config* cfg, const int32_t* seq_lens, const int32_t* 
   p.meta.seg_ptr = reinterpret_cast<int32_t*>(cb + o_ptr);
   p.meta.seg_bounds = reinterpret_cast<int32_t*>(cb + o_bnd);
   p.meta.topk = reinterpret_cast<int32_t*>(cb + o_topk);
+  p.meta.prompt_lens = reinterpret_cast<int32_t*>(cb + o_sink);  // the sink lengths (0 without a sink)
+  std::vector<int32_t> sinks(p.B, 0);
+  if (sink_lens) std::copy(sink_lens, sink_lens + p.B, sinks.begin());
   bool ok = cudaMemcpy(p.meta.seq_lens, seq_lens, nb * 4, cudaMemcpyHostToDevice) == cudaSuccess &&
             cudaMemcpy(p.meta.seg_ptr, seg_ptr, (nb + 1) * 4, cudaMemcpyHostToDevice) == cudaSuccess &&
             cudaMemcpy(p.meta.seg_bounds, seg_bounds, n_bounds * 4, cudaMemcpyHostToDevice) == cudaSuccess &&
-            cudaMemcpy(p.meta.topk, kclip.data(), nb * 4, cudaMemcpyHostToDevice) == cudaSuccess;
+            cudaMemcpy(p.meta.topk, kclip.data(), nb * 4, cudaMemcpyHostToDevice) == cudaSuccess &&
+            cudaMemcpy(p.meta.prompt_lens, sinks.data(), nb * 4, cudaMemcpyHostToDevice) == cudaSuccess;
   if (!ok) {
     cudaGetLastError();
     cudaFree(base);
@@ -225,6 +256,10 @@ zr_status zr_plan(const zr_config* cfg, const int32_t* seq_lens, const int32_t* 
   *workspace_bytes = p.ws.total;
   return ZR_OK;
 }
+
+}  // namespace
+
+extern "C" {
 
 zr_status zr_plan_dims(zr_plan_t plan, int32_t* k_max, int32_t* n_max) {
   if (!plan || !k_max || !n_max || plan->p.mode != zr::kDecodePlan) return ZR_EINVAL;

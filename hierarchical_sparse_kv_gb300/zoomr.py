@@ -56,6 +56,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.zr_plan.argtypes = [ctypes.POINTER(zr_config), _I32P, _I32P, _I32P, _I32P, ctypes.POINTER(_P),
                             ctypes.POINTER(ctypes.c_size_t)]
     lib.zr_plan.restype = ctypes.c_int
+    lib.zr_plan_sink.argtypes = [ctypes.POINTER(zr_config), _I32P, _I32P, _I32P, _I32P, _I32P, ctypes.POINTER(_P),
+                                 ctypes.POINTER(ctypes.c_size_t)]
+    lib.zr_plan_sink.restype = ctypes.c_int
     lib.zr_plan_dims.argtypes = [_P, _I32P, _I32P]
     lib.zr_plan_dims.restype = ctypes.c_int
     lib.zr_decode_attend.argtypes = [_P] * 13
@@ -137,15 +140,21 @@ def _stream(stream) -> Optional[int]:
     return stream.cuda_stream
 
 
-def zr_plan(cfg: zr_config, seq_lens, seg_ptr, seg_bounds, topk) -> Tuple[int, int]:
-    """Returns (plan handle, workspace bytes). Raises ZoomrError on a non-OK status."""
+def zr_plan(cfg: zr_config, seq_lens, seg_ptr, seg_bounds, topk, sink_lens=None) -> Tuple[int, int]:
+    """Returns (plan handle, workspace bytes); with ``sink_lens``, zr_plan_sink. Raises ZoomrError on a
+    non-OK status."""
     lib = load()
     a = [_i32(x) for x in (seq_lens, seg_ptr, seg_bounds, topk)]
     plan = _P()
     ws = ctypes.c_size_t()
-    st = lib.zr_plan(ctypes.byref(cfg), *[_ptr32(x) for x in a], ctypes.byref(plan), ctypes.byref(ws))
+    if sink_lens is None:
+        st = lib.zr_plan(ctypes.byref(cfg), *[_ptr32(x) for x in a], ctypes.byref(plan), ctypes.byref(ws))
+    else:
+        sk = _i32(sink_lens)
+        st = lib.zr_plan_sink(ctypes.byref(cfg), _ptr32(a[0]), _ptr32(sk), *[_ptr32(x) for x in a[1:]],
+                              ctypes.byref(plan), ctypes.byref(ws))
     if st != ZR_OK:
-        raise ZoomrError(st, "zr_plan")
+        raise ZoomrError(st, "zr_plan_sink" if sink_lens is not None else "zr_plan")
     return plan.value, ws.value
 
 
@@ -301,12 +310,12 @@ class DecodePlan:
 
     def __init__(self, *, batch: int, num_q_heads: int, num_kv_heads: int, head_dim: int, num_blocks: int,
                  max_blocks_per_seq: int, window: int, dtype: str, seq_lens: Sequence[int], seg_ptr: Sequence[int],
-                 seg_bounds: Sequence[int], topk: Sequence[int], device=None):
+                 seg_bounds: Sequence[int], topk: Sequence[int], device=None, sink_lens=None):
         self.cfg = zr_config(batch, num_q_heads, num_kv_heads, head_dim, 16, num_blocks, max_blocks_per_seq, window,
                              DTYPES[dtype])
         self.device = torch.device(device if device is not None else "cuda")
         with torch.cuda.device(self.device):
-            self.handle, self.workspace_bytes = zr_plan(self.cfg, seq_lens, seg_ptr, seg_bounds, topk)
+            self.handle, self.workspace_bytes = zr_plan(self.cfg, seq_lens, seg_ptr, seg_bounds, topk, sink_lens)
             self.k_max, self.n_max = zr_plan_dims(self.handle)
             self.workspace = torch.zeros(max(self.workspace_bytes, 256) // 4 + 64, dtype=torch.int32,
                                          device=self.device)
@@ -323,7 +332,7 @@ class DecodePlan:
         return cls(batch=st.batch, num_q_heads=sp.num_q_heads, num_kv_heads=sp.num_kv_heads, head_dim=sp.head_dim,
                    num_blocks=st.num_blocks, max_blocks_per_seq=st.max_blocks_per_seq, window=st.window,
                    dtype=sp.dtype, seq_lens=st.seq_lens, seg_ptr=st.seg_ptr, seg_bounds=st.seg_bounds, topk=st.topk,
-                   device=device)
+                   device=device, sink_lens=getattr(st, "sink_lens", None))
 
     def new_debug_outputs(self):
         B, H = self.batch, self.num_kv_heads

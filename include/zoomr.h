@@ -104,6 +104,21 @@ ZR_API zr_status zr_plan(const zr_config* cfg, const int32_t* seq_lens, const in
                   size_t* workspace_bytes);
 
 /*
+ * zr_plan_sink -- zr_plan with the prompt kept as an attention sink (ZoomR page,
+ * 3.3 "Constructing the Final Multi-Granularity Context": the prompt tokens I_p
+ * are in every final set; 3.4 "Prefill Stage": their cache is kept in full).
+ *   sink_lens  [B]  N_s >= 0 prompt tokens of sequence b, always attended; the
+ *                   segments then partition [N_s, L_b): the first bound of each
+ *                   sequence is N_s instead of 0 (N_s < L_b).
+ * Every unit's token set gains [0, N_s). The plan reserves one more range slot
+ * per unit: zr_plan_dims reports k_max one larger than zr_plan would (the
+ * selection output keeps its -1 padding). Everything else is as zr_plan.
+ */
+ZR_API zr_status zr_plan_sink(const zr_config* cfg, const int32_t* seq_lens, const int32_t* sink_lens,
+                              const int32_t* seg_ptr, const int32_t* seg_bounds, const int32_t* topk,
+                              zr_plan_t* out_plan, size_t* workspace_bytes);
+
+/*
  * zr_plan_dims -- sizes of the optional debug outputs of a plan.
  *   *k_max = max_b min(topk[b], n_b) (at least 1), *n_max = max_b n_b.
  */

@@ -188,3 +188,17 @@ def test_steps_between_selections_reject_null_arguments(lib):
     assert lib.zr_decode_advance(None, None, None, None) == Z.ZR_EINVAL
     assert lib.zr_decode_attend_reuse(*([None] * 10)) == Z.ZR_EINVAL
     assert lib.zr_consensus_advance(None, None, None, None) == Z.ZR_EINVAL
+
+
+def test_sink_plan_checks_the_first_bound_on_the_host(lib):
+    cfg, L, P, Bd, K = _good()
+
+    def status(sink, bounds):
+        a = [Z._i32(x) for x in (L, sink, P, bounds, K)]
+        plan, ws = Z._P(), ctypes.c_size_t()
+        return lib.zr_plan_sink(ctypes.byref(cfg), *[Z._ptr32(x) for x in a], ctypes.byref(plan), ctypes.byref(ws))
+
+    assert status([3, 0], Bd) == Z.ZR_EINVAL                       # first bound 0, sink 3
+    assert status([-1, 0], Bd) == Z.ZR_EINVAL
+    assert status([10, 17], [10, 25, 40, 17, 17]) == Z.ZR_EINVAL   # a sequence with its whole length as sink: empty segment
+    assert lib.zr_plan_sink(ctypes.byref(cfg), None, None, None, None, None, None, None) == Z.ZR_EINVAL
