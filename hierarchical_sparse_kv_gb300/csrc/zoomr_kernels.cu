@@ -240,6 +240,7 @@ __global__ void __launch_bounds__(kSelectThreads) zr_select_kernel(StepArgs a) {
   const int n = a.meta.seg_ptr[b + 1] - s0;
   const int L = a.meta.seq_lens[b];
   const int k = a.meta.topk[b];
+  const int Ns = a.meta.prompt_lens[b];
   for (int i = tid; i <= n; i += blockDim.x) bnd[i] = a.meta.seg_bounds[s0 + b + i];
   pdl_wait();
 
@@ -501,7 +502,6 @@ __global__ void __launch_bounds__(kSelectThreads) zr_select_kernel(StepArgs a) {
   // 4. the prompt kept as an attention sink (sequences planned with one): [0, Ns) joins the token
   //    ranges -- merged into the first range when that one starts at or before Ns (the first
   //    segment, which begins at Ns, is selected, or the window reaches the prompt), else prepended.
-  const int Ns = a.meta.prompt_lens[b];
   if (Ns > 0) {
     __syncthreads();  // this CTA's ranges, prefix sums and unit sizes are written
     if (tid < 32) add_sink_range(a, u, Ns, rg, cum, rout, tid);
@@ -522,6 +522,22 @@ __global__ void __launch_bounds__(kSelectThreads) zr_select_kernel(StepArgs a) {
 
 __device__ __forceinline__ int unit_rows(const StepArgs& a, int u) { return a.unit_rows[u]; }
 
+// Every attend warp needs the unit sizes to find its rows. Up to kStagedUnits of them are read
+// once per CTA into shared memory (all threads, one round trip) rather than once per warp: the
+// grid's warps would otherwise all hit the same few L2 lines at the same moment.
+constexpr int kStagedUnits = 256;
+struct UnitRows {
+  const int32_t* p;  // shared copy, or the workspace array
+  __device__ __forceinline__ int operator()(int u) const { return p[u]; }
+};
+__device__ __forceinline__ UnitRows stage_unit_rows(const StepArgs& a, int32_t* s_rows) {
+  const int U = a.B * a.Hkv;
+  if (U > kStagedUnits) return UnitRows{a.unit_rows};
+  for (int i = threadIdx.x; i < U; i += blockDim.x) s_rows[i] = a.unit_rows[i];
+  __syncthreads();
+  return UnitRows{s_rows};
+}
+
 struct WarpRange {
   long long s, e;  // this warp's global rows [s, e)
   long long R;     // rows of all units
@@ -532,7 +548,7 @@ struct WarpRange {
 };
 
 // This warp's share of the rows and the unit where it starts; false when it gets no rows.
-__device__ bool locate_range(const StepArgs& a, int w, int nwarps, int lane, WarpRange& wr) {
+__device__ bool locate_range(const StepArgs& a, const UnitRows& rows, int w, int nwarps, int lane, WarpRange& wr) {
   const int U = a.B * a.Hkv;
   constexpr int K = 8;  // units kept in registers per lane: one memory round trip when U <= 256
   const bool fast = U <= 32 * K;
@@ -542,11 +558,11 @@ __device__ bool locate_range(const StepArgs& a, int w, int nwarps, int lane, War
 #pragma unroll
     for (int k = 0; k < K; ++k) {
       const int u = 32 * k + lane;
-      v[k] = u < U ? unit_rows(a, u) : 0;
+      v[k] = u < U ? rows(u) : 0;
       tot += v[k];
     }
   } else {
-    for (int u = lane; u < U; u += 32) tot += unit_rows(a, u);
+    for (int u = lane; u < U; u += 32) tot += rows(u);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(kFull, tot, o);
@@ -578,7 +594,7 @@ __device__ bool locate_range(const StepArgs& a, int w, int nwarps, int lane, War
     }
   } else {
     for (int base = 0; base < U; base += 32) {
-      const int r = base + lane < U ? unit_rows(a, base + lane) : 0;
+      const int r = base + lane < U ? rows(base + lane) : 0;
       const int incl = warp_incl_scan(r, lane);
       const int ctot = __shfl_sync(kFull, incl, 31);
       if (carry + ctot > wr.s) {
@@ -643,10 +659,11 @@ __device__ void build_row_table(const StepArgs& a, int b, int g, int u, int4 inf
 // One warp's walk over its rows: for every unit its range touches, begin_unit, run over row
 // tables of up to kChunkRows rows, and end_unit into slot u + w.
 template <class Worker>
-__device__ void attend_balanced(const StepArgs& a, Worker& wk, uint32_t* tab, int warp, int lane) {
+__device__ void attend_balanced(const StepArgs& a, const UnitRows& rows, Worker& wk, uint32_t* tab, int warp,
+                                int lane) {
   const int w = blockIdx.x * kAttendWarps + warp;
   WarpRange wr;
-  if (!locate_range(a, w, a.attend_warps, lane, wr)) return;
+  if (!locate_range(a, rows, w, a.attend_warps, lane, wr)) return;
   int u = wr.u;
   long long P = wr.P;
   int Ru = wr.Ru;
@@ -667,7 +684,7 @@ __device__ void attend_balanced(const StepArgs& a, Worker& wk, uint32_t* tab, in
     if (pos >= wr.e) break;
     P += Ru;
     ++u;
-    Ru = unit_rows(a, u);
+    Ru = rows(u);
   }
 }
 
@@ -896,6 +913,7 @@ template <int D>
 __global__ void __launch_bounds__(kAttendWarps * 32, 3) zr_attend_mma_kernel(StepArgs a) {
   extern __shared__ __align__(16) unsigned char attend_smem[];
   __shared__ uint32_t rowtab[kAttendWarps][kChunkRows];
+  __shared__ int32_t s_rows[kStagedUnits];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   pdl_wait();
   pdl_trigger();  // after the wait: the merge kernel may read the select kernel's unit sizes at once
@@ -904,7 +922,7 @@ __global__ void __launch_bounds__(kAttendWarps * 32, 3) zr_attend_mma_kernel(Ste
   const int chunk_off = (lane % (D / 8)) * 16;
   wk.lb = LoadBases{static_cast<const char*>(a.k_pool) + chunk_off, static_cast<const char*>(a.v_pool) + chunk_off,
                     static_cast<const char*>(a.sum_k) + chunk_off, static_cast<const char*>(a.sum_v) + chunk_off};
-  attend_balanced(a, wk, rowtab[warp], warp, lane);
+  attend_balanced(a, stage_unit_rows(a, s_rows), wk, rowtab[warp], warp, lane);
 }
 
 // ------------------------------------------------------------------ attend: CUDA cores (f32, or any G)
@@ -983,11 +1001,12 @@ struct FmaWorker {
 template <typename T, int D>
 __global__ void __launch_bounds__(kAttendWarps * 32) zr_attend_fma_kernel(StepArgs a) {
   __shared__ uint32_t rowtab[kAttendWarps][kChunkRows];
+  __shared__ int32_t s_rows[kStagedUnits];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   pdl_wait();
   pdl_trigger();  // after the wait: the merge kernel may read the select kernel's unit sizes at once
   FmaWorker<T, D> wk;
-  attend_balanced(a, wk, rowtab[warp], warp, lane);
+  attend_balanced(a, stage_unit_rows(a, s_rows), wk, rowtab[warp], warp, lane);
 }
 
 // ------------------------------------------------------------------ merge
