@@ -42,6 +42,16 @@ constexpr unsigned kFull = 0xFFFFFFFFu;
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// An L2 prefetch: a hint only (a later load still reads the current value), so kernels issue it for
+// their inputs before waiting on the previous kernel, which cannot make it read anything stale.
+__device__ __forceinline__ void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
+
+// Prefetch `bytes` at `base` into L2, one 128-byte line per thread of the grid slice [t0, t0 + nt).
+__device__ __forceinline__ void prefetch_span(const void* base, size_t bytes, size_t t, size_t nt) {
+  const char* c = static_cast<const char*>(base);
+  for (size_t off = t * 128; off < bytes; off += nt * 128) prefetch_l2(c + off);
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -210,9 +220,13 @@ struct SelectLayout {
   static constexpr int kRowBytes = D * static_cast<int>(sizeof(T)) + 16;
   static constexpr int kStageRows = D * sizeof(T) >= 512 ? 128 : 256;
   static constexpr int kPieces = D * static_cast<int>(sizeof(T)) / 16;  // 16-byte pieces per row
-  static constexpr size_t kPairBytes = static_cast<size_t>(kStageRows) * kMaxGroup * 4;
-  static constexpr size_t kFixedBytes =
-      static_cast<size_t>(kMaxGroup) * DP * 4 + static_cast<size_t>(kStageRows) * kRowBytes + kPairBytes;
+  // Rows staged per batch: the plan's largest segment count, at most kStageRows (so that a small
+  // plan's select CTA leaves room for the attend CTAs that wait beside it on the same SM).
+  __host__ __device__ static constexpr int stage_rows(int n_max) { return n_max < kStageRows ? (n_max > 0 ? n_max : 1) : kStageRows; }
+  __host__ __device__ static constexpr size_t fixed_bytes(int n_max) {
+    return static_cast<size_t>(kMaxGroup) * DP * 4 +
+           static_cast<size_t>(stage_rows(n_max)) * (kRowBytes + static_cast<size_t>(kMaxGroup) * 4);
+  }
 };
 
 template <typename T, int D>
@@ -225,8 +239,9 @@ __global__ void __launch_bounds__(kSelectThreads) zr_select_kernel(StepArgs a) {
   const int G = a.G, nmax = a.n_max;
   float* qs = reinterpret_cast<float*>(smem_raw);
   unsigned char* stage = smem_raw + static_cast<size_t>(kMaxGroup) * DP * 4;
-  float* pairv = reinterpret_cast<float*>(stage + static_cast<size_t>(LY::kStageRows) * LY::kRowBytes);
-  float* keys = reinterpret_cast<float*>(smem_raw + LY::kFixedBytes);
+  const int SR = LY::stage_rows(nmax);
+  float* pairv = reinterpret_cast<float*>(stage + static_cast<size_t>(SR) * LY::kRowBytes);
+  float* keys = reinterpret_cast<float*>(smem_raw + LY::fixed_bytes(nmax));
   int* flag = reinterpret_cast<int*>(keys + nmax + 4);
   int* bnd = flag + nmax + 2;
   int* list = bnd + nmax + 1;
@@ -242,19 +257,30 @@ __global__ void __launch_bounds__(kSelectThreads) zr_select_kernel(StepArgs a) {
   const int k = a.meta.topk[b];
   const int Ns = a.meta.prompt_lens[b];
   for (int i = tid; i <= n; i += blockDim.x) bnd[i] = a.meta.seg_bounds[s0 + b + i];
+  const T* qg = static_cast<const T*>(a.q) + (static_cast<size_t>(b) * a.Hq + static_cast<size_t>(g) * G) * D;
+  {
+    // the group's queries and the first batch of its summary-key rows, into L2 before the wait
+    constexpr size_t RB = D * sizeof(T);
+    if (tid < kSelectThreads / 2) {
+      prefetch_span(qg, G * RB, tid, kSelectThreads / 2);
+    } else {
+      const char* sk = static_cast<const char*>(a.sum_k);
+      const int rows = min(SR, n);
+      for (int i = tid - kSelectThreads / 2; i < rows; i += kSelectThreads / 2)
+        prefetch_span(sk + (static_cast<size_t>(s0 + i) * a.Hkv + g) * RB, RB, 0, 1);
+    }
+  }
   pdl_wait();
 
-  const T* qg = static_cast<const T*>(a.q) + (static_cast<size_t>(b) * a.Hq + static_cast<size_t>(g) * G) * D;
-
   // 1. ranking key: max over the group of the fp32 dot, products and sums rounded, ascending order.
-  //    Up to kStageRows summary-key rows are staged raw in one memory round trip (the first batch
+  //    Up to SR summary-key rows are staged raw in one memory round trip (the first batch
   //    together with the queries); then every (segment, head) pair runs its own sequential chain.
   const char* sk = static_cast<const char*>(a.sum_k);
   constexpr int PER = LY::kStageRows * LY::kPieces / kSelectThreads;
   static_assert(LY::kStageRows * LY::kPieces % kSelectThreads == 0, "staging split");
   constexpr int EPP = 16 / static_cast<int>(sizeof(T));  // elements per 16-byte piece
-  for (int c0 = 0; c0 < n; c0 += LY::kStageRows) {
-    const int rows = min(LY::kStageRows, n - c0);
+  for (int c0 = 0; c0 < n; c0 += SR) {
+    const int rows = min(SR, n - c0);
     __syncthreads();  // the previous batch's readers are done
     uint4 v[PER];
     float qv[8];
@@ -656,6 +682,15 @@ __device__ void build_row_table(const StepArgs& a, int b, int g, int u, int4 inf
   __syncwarp();
 }
 
+// Before its wait on the select kernel an attend CTA prefetches its slice of the block tables and
+// of the queries (inputs, not written by the select kernel) into L2.
+__device__ __forceinline__ void prefetch_attend_inputs(const StepArgs& a, size_t q_row_bytes) {
+  const size_t t = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const size_t nt = static_cast<size_t>(gridDim.x) * blockDim.x;
+  prefetch_span(a.block_tables, static_cast<size_t>(a.B) * a.max_blocks * sizeof(int32_t), t, nt);
+  prefetch_span(a.q, static_cast<size_t>(a.B) * a.Hq * q_row_bytes, t, nt);
+}
+
 // One warp's walk over its rows: for every unit its range touches, begin_unit, run over row
 // tables of up to kChunkRows rows, and end_unit into slot u + w.
 template <class Worker>
@@ -915,6 +950,7 @@ __global__ void __launch_bounds__(kAttendWarps * 32, 3) zr_attend_mma_kernel(Ste
   __shared__ uint32_t rowtab[kAttendWarps][kChunkRows];
   __shared__ int32_t s_rows[kStagedUnits];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  prefetch_attend_inputs(a, sizeof(__nv_bfloat16) * D);
   pdl_wait();
   pdl_trigger();  // after the wait: the merge kernel may read the select kernel's unit sizes at once
   MmaWorker<D> wk;
@@ -1003,6 +1039,7 @@ __global__ void __launch_bounds__(kAttendWarps * 32) zr_attend_fma_kernel(StepAr
   __shared__ uint32_t rowtab[kAttendWarps][kChunkRows];
   __shared__ int32_t s_rows[kStagedUnits];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  prefetch_attend_inputs(a, sizeof(T) * D);
   pdl_wait();
   pdl_trigger();  // after the wait: the merge kernel may read the select kernel's unit sizes at once
   FmaWorker<T, D> wk;
@@ -1206,7 +1243,7 @@ cudaError_t launch_pdl(Kern kernel, dim3 grid, dim3 block, size_t smem, cudaStre
 
 template <typename T, int D>
 size_t select_smem_bytes(int n_max) {
-  return SelectLayout<T, D>::kFixedBytes + (static_cast<size_t>(n_max) * 6 + 7) * 4;
+  return SelectLayout<T, D>::fixed_bytes(n_max) + (static_cast<size_t>(n_max) * 6 + 7) * 4;
 }
 
 template <typename T, int D>
