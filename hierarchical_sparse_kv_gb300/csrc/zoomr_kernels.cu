@@ -645,15 +645,22 @@ __device__ void build_row_table(const StepArgs& a, int b, int g, int u, int4 inf
   const int32_t* sl = a.sumlist + static_cast<size_t>(u) * a.n_max;
   const int32_t* bt = a.block_tables + static_cast<size_t>(b) * a.max_blocks;
   const int seg0 = a.meta.seg_ptr[b];
+  // The first 32 ranges' bounds are read before anything uses `info` (whatever nr is, they lie
+  // within the unit's arrays; masked below), so this load overlaps the caller's load of `info`.
+  const bool in0 = lane <= a.k_max;
+  const int cs0 = in0 ? cum[lane] : 0, ce0 = in0 ? cum[lane + 1] : 0, st0 = in0 ? rg[2 * lane] : 0;
   __syncwarp();  // the previous table's readers are done
   for (int e = lane; e < kChunkRows; e += 32) tab[e] = kInvalidRow;
   const int tok_end = min(r0 + n, n_tok);
   for (int base = 0; base < nr && r0 < tok_end; base += 32) {
     const int i = base + lane;
-    // read within the unit's arrays whatever nr is, then mask: the loads need not wait for info
-    const bool in_region = i <= a.k_max;
-    const int cs_raw = in_region ? cum[i] : 0, ce_raw = in_region ? cum[i + 1] : 0;
-    const int st_raw = in_region ? rg[2 * i] : 0;
+    int cs_raw = cs0, ce_raw = ce0, st_raw = st0;
+    if (base > 0) {
+      const bool in_region = i <= a.k_max;
+      cs_raw = in_region ? cum[i] : 0;
+      ce_raw = in_region ? cum[i + 1] : 0;
+      st_raw = in_region ? rg[2 * i] : 0;
+    }
     const int cs = i < nr ? cs_raw : 0x7fffffff;
     const int ce = i < nr ? ce_raw : 0x7fffffff;
     const int st = i < nr ? st_raw : 0;
