@@ -540,11 +540,12 @@ __global__ void __launch_bounds__(kSelectThreads) zr_select_kernel(StepArgs a) {
 
 // ------------------------------------------------------------------ attend: shared pieces
 // The rows every unit gathers (its tokens through the block table, then its summary rows) are
-// laid end to end in unit order, R rows in all, and the attend grid's warps split them evenly:
-// warp w takes global rows [w*R/N, (w+1)*R/N) with N = min(warps, R), so every warp streams
-// the same number of bytes whatever the units' sizes. A warp writes one partial per unit its
-// range touches, into slot u + w: the (unit, warp) pairs that intersect form a monotone
-// staircase, so u + w is unique and the slots never exceed U + N.
+// laid end to end in unit order, each unit preceded by a fixed start cost (below), C in all, and
+// the attend grid's warps split that evenly: warp w takes [w*C/N, (w+1)*C/N) with N = min(warps,
+// C), so every warp streams about the same number of bytes whatever the units' sizes. A warp
+// writes one partial per unit whose rows its share touches, into slot u + w: the (unit, warp)
+// pairs that intersect form a monotone staircase, so u + w is unique and the slots never exceed
+// U + N.
 
 __device__ __forceinline__ int unit_rows(const StepArgs& a, int u) { return a.unit_rows[u]; }
 
@@ -564,16 +565,26 @@ __device__ __forceinline__ UnitRows stage_unit_rows(const StepArgs& a, int32_t* 
   return UnitRows{s_rows};
 }
 
+// The split runs over a cost coordinate: unit u costs kUnitStartCost + its rows, the start cost
+// first (a virtual stretch that holds no row). A warp whose share reaches into a second unit pays a
+// second start (query fragments, two table round trips, a pipeline refill), measured at about 3 us
+// on GB300: such warps were the last to finish. The virtual stretch takes rows off their shares;
+// 48 rows measured best on the 16K-token workload (swept from 0 to 128).
+#ifndef ZR_UNIT_START_ROWS
+#define ZR_UNIT_START_ROWS 48
+#endif
+constexpr int kUnitStartCost = ZR_UNIT_START_ROWS;
+
 struct WarpRange {
-  long long s, e;  // this warp's global rows [s, e)
-  long long R;     // rows of all units
-  long long N;     // warps that get rows
-  int u;           // unit containing row s
-  long long P;     // first global row of unit u
+  long long s, e;  // this warp's share [s, e) of the cost coordinate
+  long long R;     // cost of all units
+  long long N;     // warps that get a share
+  int u;           // unit whose cost stretch contains s
+  long long P;     // cost position where unit u starts (its rows start at P + kUnitStartCost)
   int Ru;          // rows of unit u
 };
 
-// This warp's share of the rows and the unit where it starts; false when it gets no rows.
+// This warp's share of the cost coordinate and the unit where it starts; false when it gets none.
 __device__ bool locate_range(const StepArgs& a, const UnitRows& rows, int w, int nwarps, int lane, WarpRange& wr) {
   const int U = a.B * a.Hkv;
   constexpr int K = 8;  // units kept in registers per lane: one memory round trip when U <= 256
@@ -585,10 +596,10 @@ __device__ bool locate_range(const StepArgs& a, const UnitRows& rows, int w, int
     for (int k = 0; k < K; ++k) {
       const int u = 32 * k + lane;
       v[k] = u < U ? rows(u) : 0;
-      tot += v[k];
+      tot += u < U ? v[k] + kUnitStartCost : 0;
     }
   } else {
-    for (int u = lane; u < U; u += 32) tot += rows(u);
+    for (int u = lane; u < U; u += 32) tot += rows(u) + kUnitStartCost;
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(kFull, tot, o);
@@ -603,13 +614,14 @@ __device__ bool locate_range(const StepArgs& a, const UnitRows& rows, int w, int
     const int l = __ffs(m) - 1;
     wr.u = base + l;
     wr.Ru = __shfl_sync(kFull, r, l);
-    wr.P = carry + __shfl_sync(kFull, incl, l) - wr.Ru;
+    wr.P = carry + __shfl_sync(kFull, incl, l) - (wr.Ru + kUnitStartCost);
   };
   if (fast) {
 #pragma unroll
     for (int k = 0; k < K; ++k) {
       if (32 * k < U) {
-        const int incl = warp_incl_scan(v[k], lane);
+        const int c = 32 * k + lane < U ? v[k] + kUnitStartCost : 0;
+        const int incl = warp_incl_scan(c, lane);
         const int ctot = __shfl_sync(kFull, incl, 31);
         if (carry + ctot > wr.s) {
           found(32 * k, v[k], incl);
@@ -621,7 +633,7 @@ __device__ bool locate_range(const StepArgs& a, const UnitRows& rows, int w, int
   } else {
     for (int base = 0; base < U; base += 32) {
       const int r = base + lane < U ? rows(base + lane) : 0;
-      const int incl = warp_incl_scan(r, lane);
+      const int incl = warp_incl_scan(base + lane < U ? r + kUnitStartCost : 0, lane);
       const int ctot = __shfl_sync(kFull, incl, 31);
       if (carry + ctot > wr.s) {
         found(base, r, incl);
@@ -630,7 +642,7 @@ __device__ bool locate_range(const StepArgs& a, const UnitRows& rows, int w, int
       carry += ctot;
     }
   }
-  return false;  // not reached: row s < R lies in some unit
+  return false;  // not reached: position s < R lies in some unit
 }
 
 // Fill tab[0, kChunkRows) for the unit-local rows [r0, r0 + n) of unit u: the pool row id
@@ -709,22 +721,24 @@ __device__ void attend_balanced(const StepArgs& a, const UnitRows& rows, Worker&
   int u = wr.u;
   long long P = wr.P;
   int Ru = wr.Ru;
-  long long pos = wr.s;
   while (true) {
-    const int b = u / a.Hkv, g = u - b * a.Hkv;
-    const int4 info = a.unit_info[u];
-    const long long end = min(wr.e, P + Ru);
-    const int lo = static_cast<int>(pos - P), hi = static_cast<int>(end - P);
-    wk.begin_unit(a, b, g, lane);
-    for (int r0 = lo; r0 < hi; r0 += kChunkRows) {
-      const int nrow = min(kChunkRows, hi - r0);
-      build_row_table(a, b, g, u, info, r0, nrow, tab, lane);
-      wk.run(a, tab, nrow, lane);
+    // unit u's rows occupy [P + kUnitStartCost, P + kUnitStartCost + Ru) of the cost coordinate
+    const long long first = P + kUnitStartCost;
+    const int lo = static_cast<int>(min(max(wr.s - first, 0LL), static_cast<long long>(Ru)));
+    const int hi = static_cast<int>(min(max(wr.e - first, 0LL), static_cast<long long>(Ru)));
+    if (lo < hi) {
+      const int b = u / a.Hkv, g = u - b * a.Hkv;
+      const int4 info = a.unit_info[u];
+      wk.begin_unit(a, b, g, lane);
+      for (int r0 = lo; r0 < hi; r0 += kChunkRows) {
+        const int nrow = min(kChunkRows, hi - r0);
+        build_row_table(a, b, g, u, info, r0, nrow, tab, lane);
+        wk.run(a, tab, nrow, lane);
+      }
+      wk.end_unit(a, u + w, lane);
     }
-    wk.end_unit(a, u + w, lane);
-    pos = end;
-    if (pos >= wr.e) break;
-    P += Ru;
+    if (first + Ru >= wr.e) break;
+    P = first + Ru;
     ++u;
     Ru = rows(u);
   }
@@ -1092,9 +1106,12 @@ __global__ void __launch_bounds__(kAttendWarps * 32) zr_merge_comp_kernel(StepAr
     Pu += __shfl_xor_sync(kFull, Pu, o);
     Ru += __shfl_xor_sync(kFull, Ru, o);
   }
-  const long long N = min(static_cast<long long>(a.attend_warps), R);
-  // warp holding global row r of the even split: ceil((r + 1) N / R) - 1
-  const long long wf = ((Pu + 1) * N + R - 1) / R - 1, wl = ((Pu + Ru) * N + R - 1) / R - 1;
+  // the split's cost coordinate: unit u's rows at [Pu + (u + 1) X, Pu + (u + 1) X + Ru), C = R + U X
+  const long long X = kUnitStartCost, C = R + static_cast<long long>(U) * X;
+  const long long N = min(static_cast<long long>(a.attend_warps), C);
+  const long long c0 = Pu + (u + 1) * X, c1 = c0 + Ru - 1;  // the unit's first and last row
+  // warp whose share holds cost position c: ceil((c + 1) N / C) - 1
+  const long long wf = ((c0 + 1) * N + C - 1) / C - 1, wl = ((c1 + 1) * N + C - 1) / C - 1;
   const size_t first = static_cast<size_t>(u) + wf;
   const int cnt = static_cast<int>(wl - wf + 1);
   pdl_wait();
@@ -1169,9 +1186,12 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 8) zr_merge_part_kernel(Step
       Pu += __shfl_xor_sync(kFull, Pu, o);
       Ru += __shfl_xor_sync(kFull, Ru, o);
     }
-    const long long N = min(static_cast<long long>(a.attend_warps), R);
-    // warp holding global row r of the even split: ceil((r + 1) N / R) - 1
-    const long long wf = ((Pu + 1) * N + R - 1) / R - 1, wl = ((Pu + Ru) * N + R - 1) / R - 1;
+    // the split's cost coordinate: unit u's rows at [Pu + (u + 1) X, Pu + (u + 1) X + Ru), C = R + U X
+    const long long X = kUnitStartCost, C = R + static_cast<long long>(U) * X;
+    const long long N = min(static_cast<long long>(a.attend_warps), C);
+    const long long c0 = Pu + (u + 1) * X, c1 = c0 + Ru - 1;  // the unit's first and last row
+    // warp whose share holds cost position c: ceil((c + 1) N / C) - 1
+    const long long wf = ((c0 + 1) * N + C - 1) / C - 1, wl = ((c1 + 1) * N + C - 1) / C - 1;
     if (lane == 0) {
       s_first = u + wf;
       s_cnt = static_cast<int>(wl - wf + 1);
