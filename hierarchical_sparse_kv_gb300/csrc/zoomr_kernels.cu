@@ -387,15 +387,13 @@ __global__ void __launch_bounds__(kSelectThreads) zr_select_kernel(StepArgs a) {
       s_cnt[2][wi] = __popc(bbe);
     }
     __syncthreads();
-    int off_s = 0, off_r = 0, m = 0, rstar = 0;
-    for (int w = 0; w < nwarps; ++w) {
-      if (w < wi) {
-        off_s += s_cnt[0][w];
-        off_r += s_cnt[1][w];
-      }
-      m += s_cnt[1][w];
-      rstar += s_cnt[2][w];  // runs that end before the window starts
-    }
+    // every warp scans the per-warp counts itself: lane w holds warp w's (nwarps <= 32)
+    const int c0w = lane < nwarps ? s_cnt[0][lane] : 0, c1w = lane < nwarps ? s_cnt[1][lane] : 0;
+    const int c2w = lane < nwarps ? s_cnt[2][lane] : 0;
+    const int i0 = warp_incl_scan(c0w, lane), i1 = warp_incl_scan(c1w, lane), i2 = warp_incl_scan(c2w, lane);
+    const int off_s = wi > 0 ? __shfl_sync(kFull, i0, wi - 1) : 0;
+    const int off_r = wi > 0 ? __shfl_sync(kFull, i1, wi - 1) : 0;
+    const int m = __shfl_sync(kFull, i1, 31), rstar = __shfl_sync(kFull, i2, 31);  // rstar: runs ending before W0
     const unsigned lt = (1u << lane) - 1u;
     const int pos = off_s + __popc(bs & lt);
     if (in) {
