@@ -18,6 +18,12 @@ constexpr int kChunkRows = 256;       // rows of one attend warp's row table (a 
 #endif
 constexpr int kAttendWarps = ZR_ATTEND_WARPS;  // warps per attend CTA
 constexpr int kSelectThreads = 512;   // threads per select CTA
+// Virtual rows in front of each unit in the attend kernels' split of a decode plan (measured best
+// on the 16K-token workload in a sweep of 0 to 128; consensus plans use 0).
+#ifndef ZR_UNIT_START_ROWS
+#define ZR_UNIT_START_ROWS 48
+#endif
+constexpr int kUnitStartRows = ZR_UNIT_START_ROWS;
 constexpr uint32_t kSummaryFlag = 0x80000000u;  // row id refers to the summary tensors
 constexpr uint32_t kInvalidRow = 0xFFFFFFFFu;   // masked row (past the chunk end, or a bad block id)
 
@@ -94,6 +100,7 @@ struct StepArgs {
   int32_t* cruns;   // consensus only
   int32_t* cnruns;  // consensus only
   int B, Hq, Hkv, G, window, num_blocks, max_blocks, k_max, n_max, attend_warps;
+  int unit_cost;  // virtual rows in front of every unit in the attend kernels' even split (see kernels)
   float scale_log2;  // log2(e) / sqrt(d)
 };
 

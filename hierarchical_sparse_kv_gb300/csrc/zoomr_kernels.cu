@@ -563,22 +563,18 @@ __device__ __forceinline__ UnitRows stage_unit_rows(const StepArgs& a, int32_t* 
   return UnitRows{s_rows};
 }
 
-// The split runs over a cost coordinate: unit u costs kUnitStartCost + its rows, the start cost
-// first (a virtual stretch that holds no row). A warp whose share reaches into a second unit pays a
+// The split runs over a cost coordinate: unit u costs a.unit_cost + its rows, the start cost first
+// (a virtual stretch that holds no row). A warp whose share reaches into a second unit pays a
 // second start (query fragments, two table round trips, a pipeline refill), measured at about 3 us
-// on GB300: such warps were the last to finish. The virtual stretch takes rows off their shares;
-// 48 rows measured best on the 16K-token workload (swept from 0 to 128).
-#ifndef ZR_UNIT_START_ROWS
-#define ZR_UNIT_START_ROWS 48
-#endif
-constexpr int kUnitStartCost = ZR_UNIT_START_ROWS;
+// on GB300 for decode units: such warps were the last to finish. The virtual stretch takes rows off
+// their shares.
 
 struct WarpRange {
   long long s, e;  // this warp's share [s, e) of the cost coordinate
   long long R;     // cost of all units
   long long N;     // warps that get a share
   int u;           // unit whose cost stretch contains s
-  long long P;     // cost position where unit u starts (its rows start at P + kUnitStartCost)
+  long long P;     // cost position where unit u starts (its rows start at P + a.unit_cost)
   int Ru;          // rows of unit u
 };
 
@@ -594,10 +590,10 @@ __device__ bool locate_range(const StepArgs& a, const UnitRows& rows, int w, int
     for (int k = 0; k < K; ++k) {
       const int u = 32 * k + lane;
       v[k] = u < U ? rows(u) : 0;
-      tot += u < U ? v[k] + kUnitStartCost : 0;
+      tot += u < U ? v[k] + a.unit_cost : 0;
     }
   } else {
-    for (int u = lane; u < U; u += 32) tot += rows(u) + kUnitStartCost;
+    for (int u = lane; u < U; u += 32) tot += rows(u) + a.unit_cost;
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(kFull, tot, o);
@@ -612,13 +608,13 @@ __device__ bool locate_range(const StepArgs& a, const UnitRows& rows, int w, int
     const int l = __ffs(m) - 1;
     wr.u = base + l;
     wr.Ru = __shfl_sync(kFull, r, l);
-    wr.P = carry + __shfl_sync(kFull, incl, l) - (wr.Ru + kUnitStartCost);
+    wr.P = carry + __shfl_sync(kFull, incl, l) - (wr.Ru + a.unit_cost);
   };
   if (fast) {
 #pragma unroll
     for (int k = 0; k < K; ++k) {
       if (32 * k < U) {
-        const int c = 32 * k + lane < U ? v[k] + kUnitStartCost : 0;
+        const int c = 32 * k + lane < U ? v[k] + a.unit_cost : 0;
         const int incl = warp_incl_scan(c, lane);
         const int ctot = __shfl_sync(kFull, incl, 31);
         if (carry + ctot > wr.s) {
@@ -631,7 +627,7 @@ __device__ bool locate_range(const StepArgs& a, const UnitRows& rows, int w, int
   } else {
     for (int base = 0; base < U; base += 32) {
       const int r = base + lane < U ? rows(base + lane) : 0;
-      const int incl = warp_incl_scan(base + lane < U ? r + kUnitStartCost : 0, lane);
+      const int incl = warp_incl_scan(base + lane < U ? r + a.unit_cost : 0, lane);
       const int ctot = __shfl_sync(kFull, incl, 31);
       if (carry + ctot > wr.s) {
         found(base, r, incl);
@@ -720,8 +716,8 @@ __device__ void attend_balanced(const StepArgs& a, const UnitRows& rows, Worker&
   long long P = wr.P;
   int Ru = wr.Ru;
   while (true) {
-    // unit u's rows occupy [P + kUnitStartCost, P + kUnitStartCost + Ru) of the cost coordinate
-    const long long first = P + kUnitStartCost;
+    // unit u's rows occupy [P + a.unit_cost, P + a.unit_cost + Ru) of the cost coordinate
+    const long long first = P + a.unit_cost;
     const int lo = static_cast<int>(min(max(wr.s - first, 0LL), static_cast<long long>(Ru)));
     const int hi = static_cast<int>(min(max(wr.e - first, 0LL), static_cast<long long>(Ru)));
     if (lo < hi) {
@@ -1105,7 +1101,7 @@ __global__ void __launch_bounds__(kAttendWarps * 32) zr_merge_comp_kernel(StepAr
     Ru += __shfl_xor_sync(kFull, Ru, o);
   }
   // the split's cost coordinate: unit u's rows at [Pu + (u + 1) X, Pu + (u + 1) X + Ru), C = R + U X
-  const long long X = kUnitStartCost, C = R + static_cast<long long>(U) * X;
+  const long long X = a.unit_cost, C = R + static_cast<long long>(U) * X;
   const long long N = min(static_cast<long long>(a.attend_warps), C);
   const long long c0 = Pu + (u + 1) * X, c1 = c0 + Ru - 1;  // the unit's first and last row
   // warp whose share holds cost position c: ceil((c + 1) N / C) - 1
@@ -1185,7 +1181,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 8) zr_merge_part_kernel(Step
       Ru += __shfl_xor_sync(kFull, Ru, o);
     }
     // the split's cost coordinate: unit u's rows at [Pu + (u + 1) X, Pu + (u + 1) X + Ru), C = R + U X
-    const long long X = kUnitStartCost, C = R + static_cast<long long>(U) * X;
+    const long long X = a.unit_cost, C = R + static_cast<long long>(U) * X;
     const long long N = min(static_cast<long long>(a.attend_warps), C);
     const long long c0 = Pu + (u + 1) * X, c1 = c0 + Ru - 1;  // the unit's first and last row
     // warp whose share holds cost position c: ceil((c + 1) N / C) - 1

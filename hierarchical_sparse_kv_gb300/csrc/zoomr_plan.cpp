@@ -320,6 +320,10 @@ StepArgs step_args(const Plan& p, void* workspace) {
   a.k_max = p.k_max;
   a.n_max = p.n_max;
   a.attend_warps = p.attend_warps;
+  // A second unit in a warp's share costs a second start. Decode units of one sequence gather
+  // different tokens (each KV head selects its own segments); consensus units share one token set,
+  // whose block-table entries the next unit finds cached, and a start there costs little.
+  a.unit_cost = p.mode == kConsensusPlan ? 0 : kUnitStartRows;
   a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(p.d)));
   return a;
 }
