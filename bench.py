@@ -24,6 +24,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import statistics
 import os
 import subprocess
 import sys
@@ -405,18 +406,17 @@ def run_zoomr(args):
     ms = max_over_ranks(ms, world)
     # attend kernel: the timed layer of each capture (its last replay in the timed region)
     timed = [i for i in range(min(n_graphs, args.steps)) if modes[i] == 0]
-    attend_ms_sum = sum(evs[i][0].elapsed_time(evs[i][1]) for i in timed)
-    attend_bytes_sum = sum(attend_bytes[i % L] for i in timed)
-    attend_ms = attend_ms_sum / len(timed)
-    attend_bytes_avg = attend_bytes_sum / len(timed)
+    # medians over the timed captures (the event pair: bytes over time per launch, median over launches)
+    attend_ms = statistics.median(evs[i][0].elapsed_time(evs[i][1]) for i in timed)
+    attend_bytes_avg = sum(attend_bytes[i % L] for i in timed) / len(timed)
     in_step = None
     sa = [pev[i].elapsed_time(evs[i][1]) for i in range(min(n_graphs, args.steps)) if modes[i] == 1]
     so = [pev[i].elapsed_time(evs[i][0]) for i in range(min(n_graphs, args.steps)) if modes[i] == 2]
     if sa and so:
-        in_step_ms = sum(sa) / len(sa) - sum(so) / len(so)
+        in_step_ms = statistics.median(sa) - statistics.median(so)
         mean_bytes = sum(attend_bytes) / L
         in_step = {"attend_us": in_step_ms * 1e3, "achieved": mean_bytes / (in_step_ms * 1e-3) / 1e9,
-                   "select_us": sum(so) / len(so) * 1e3, "select_attend_us": sum(sa) / len(sa) * 1e3}
+                   "select_us": statistics.median(so) * 1e3, "select_attend_us": statistics.median(sa) * 1e3}
 
     # e2e through the public API with host buffers: one H2D of all layers' queries from pinned
     # memory, the step, one D2H of all layers' outputs into pinned memory.
@@ -468,7 +468,7 @@ def run_zoomr(args):
         "gpu_launches": 3 * L * args.steps,
         "attend_in_step": None if in_step is None else dict(
             in_step, frac=in_step["achieved"] / peak,
-            method="mean(select+attend) - mean(select), events before the call and after attend or select, "
+            method="median(select+attend) - median(select), events before the call and after attend or select, "
                    "launch overlap between the two kernels intact"),
         "timing": "CUDA events on the launching stream around the graph replays; the attend kernel is timed with "
                   "an event pair around one layer per captured step, rotating over the layers",
@@ -484,9 +484,9 @@ def run_zoomr(args):
         raw = {k: line["roofline"][k] for k in ("achieved", "frac", "attend_us", "alg_bytes_per_launch", "timing")}
         line["roofline"].update({"achieved": in_step["achieved"], "frac": in_step["achieved"] / peak,
                                  "attend_us": in_step["attend_us"], "alg_bytes_per_launch": sum(attend_bytes) / L,
-                                 "timing": "attend kernel's time in the captured step: mean(select + attend) - "
-                                           "mean(select), CUDA events on the launching stream, launch overlap "
-                                           "intact",
+                                 "timing": "attend kernel's time in the captured step: median(select + attend) - "
+                                           "median(select) over the timed replays, CUDA events on the launching stream, "
+                                           "launch overlap intact",
                                  "event_pair": raw})
     if offload:
         line["path"] = "offload"
