@@ -379,7 +379,7 @@ const char* zr_status_string(zr_status s) {
     case ZR_EINVAL: return "ZR_EINVAL: invalid argument";
     case ZR_ENOMEM: return "ZR_ENOMEM: allocation failed";
     case ZR_ECUDA: return "ZR_ECUDA: CUDA runtime error";
-    case ZR_EUNSUPPORTED: return "ZR_EUNSUPPORTED: outside this build's limits";
+    case ZR_EUNSUPPORTED: return "ZR_EUNSUPPORTED: outside the library's supported limits";
     case ZR_EDEVICE: return "ZR_EDEVICE: the device reported a bad index";
   }
   return "unknown zr_status";

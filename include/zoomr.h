@@ -62,7 +62,7 @@ typedef enum {
   ZR_EINVAL = 1,        /* bad argument: a null pointer, a shape or a metadata array out of its contract */
   ZR_ENOMEM = 2,        /* a host or device allocation of the plan failed */
   ZR_ECUDA = 3,         /* a CUDA runtime call failed (no device, bad stream, launch failure) */
-  ZR_EUNSUPPORTED = 4,  /* valid but outside this build's limits (head_dim, group size, segment count) */
+  ZR_EUNSUPPORTED = 4,  /* valid but outside the library's supported limits (head_dim, group size, segment count) */
   ZR_EDEVICE = 5        /* the device reported a bad index (see zr_get_device_error) */
 } zr_status;
 

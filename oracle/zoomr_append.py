@@ -1,6 +1,6 @@
 """CPU oracle for the append path of a paged KV cache and the mean summary keys.
 
-TEST INFRASTRUCTURE. This module is the checker, not the product: only the
+TEST INFRASTRUCTURE. This module is the oracle, not the product: only the
 tests and the benchmark may import it. It shares no code with the CUDA path and
 imports nothing from it.
 

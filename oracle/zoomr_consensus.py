@@ -1,6 +1,6 @@
 """CPU oracle for ZoomR's consensus selection and the attention over its final set.
 
-TEST INFRASTRUCTURE. This module is the checker, not the product: only the
+TEST INFRASTRUCTURE. This module is the oracle, not the product: only the
 tests and the benchmark may import it. It shares no code with the CUDA path and
 imports nothing from it (it reuses the decode oracle's fp32 key, top-k, paged
 row and fp64 attention steps).

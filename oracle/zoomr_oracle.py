@@ -1,6 +1,6 @@
 """CPU oracle for one ZoomR decode step over a paged KV cache.
 
-TEST INFRASTRUCTURE. This module is the checker, not the product: only the
+TEST INFRASTRUCTURE. This module is the oracle, not the product: only the
 tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline leg may
 import it. It shares no code with the CUDA path and imports nothing from it.
 

@@ -1,6 +1,6 @@
 """CPU oracle for the decode step with the prompt kept as an attention sink.
 
-TEST INFRASTRUCTURE. This module is the checker, not the product: only the
+TEST INFRASTRUCTURE. This module is the oracle, not the product: only the
 tests and the benchmark may import it. It shares no code with the CUDA path and
 imports nothing from it (it reuses the decode oracle's steps).
 
