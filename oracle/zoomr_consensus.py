@@ -2,7 +2,7 @@
 
 TEST INFRASTRUCTURE. This module is the oracle, not the product: only the
 tests and the benchmark may import it. It shares no code with the CUDA path and
-imports nothing from it (it reuses the decode oracle's fp32 key, top-k, paged
+imports nothing from it (it reuses the decode oracle's exact key, top-k, paged
 row and fp64 attention steps).
 
 It follows the ZoomR page ("ZoomR: Memory Efficient Reasoning through
@@ -18,8 +18,8 @@ bd[2n] <= L): R_i = [bd[2i], bd[2i+1]) and S_i = [bd[2i+1], bd[2i+2]).
    l and query head h, alpha_i = q^(l,h) . kbar_i^(l,h) over the n summaries and
    the indices of the k largest (ties to the lower index). kbar_i is the mean
    summary key of S_i for the KV head that query head h reads (GQA). The key is
-   the decode oracle's fp32 dot (each product and partial sum rounded, ascending
-   components); k >= n gives every index.
+   the decode oracle's exact dot product (fp64 where that sum is exact, Fraction
+   elsewhere); k >= n gives every index.
 2. ``consensus``   3.3 "Global Aggregation and Consensus": I_all is the union of
    all (layer, head) top-k sets; v_i counts the sets that contain i; I_c is the
    c members of I_all with the most votes (ties to the lower index; c >= |I_all|
@@ -51,7 +51,7 @@ from oracle import zoomr_oracle as O
 def head_top_k(q_head: np.ndarray, kbar: np.ndarray, k: int) -> np.ndarray:
     """Top-k summary indices of one (layer, query head): q_head [d], kbar [n, d] (its KV head's mean
     summary keys). Ascending index order."""
-    keys = O.summary_keys(np.asarray(q_head)[None, :], kbar)  # a group of one head: its own fp32 key
+    keys = O.summary_keys(np.asarray(q_head)[None, :], kbar)  # a group of one head: its own exact key
     return O.select_top_k(keys, k)
 
 

@@ -14,9 +14,11 @@ states:
    the equation alpha_i = q_t^T kbar_i: the inner product of the query with
    every mean summary key. Readings: per KV head the score is the maximum over
    the GQA group's query heads; the division by sqrt(d) is dropped from the
-   ranking key (a positive scale does not change an order); the decision is
-   taken in the kernel's precision, fp32, with each product and each partial
-   sum rounded to nearest-even and the components summed in ascending order.
+   ranking key (a positive scale does not change an order). The key is the
+   exact real value of that inner product on the stored inputs: every product
+   of two stored values (bf16 or fp32) is exact in fp64, the d products are
+   summed in fp64 with a TwoSum error term after every add, and any sum whose
+   error terms are not all zero is recomputed with ``fractions.Fraction``.
 2. ``select_top_k``   ZoomR 3.3, the equation I_top-k = argtop-k(alpha):
    the k largest keys; ties go to the lower segment index; the result is
    returned in ascending index order. k >= n selects every segment.
@@ -32,7 +34,7 @@ states:
 
 Every step above is pinned from outside the oracle (closed forms checked
 against a library attention routine, exact rational scores, a pure-Python
-brute force, hand-computed rounding cases and invariants) in
+brute force, hand-computed cancellation cases and invariants) in
 ``tests/test_oracle_pins.py``; no step is left unpinned.
 """
 
@@ -40,6 +42,7 @@ from __future__ import annotations
 
 import math
 from dataclasses import dataclass
+from fractions import Fraction
 from typing import List, Sequence
 
 import numpy as np
@@ -47,29 +50,57 @@ import numpy as np
 BLOCK_SIZE = 16
 
 
-def summary_keys(q_group: np.ndarray, sum_k: np.ndarray) -> np.ndarray:
-    """Ranking key of every segment for one KV head.
+def _two_sum(a: np.ndarray, b: np.ndarray):
+    """fp64 a + b and its exact rounding error (Knuth's TwoSum, round to nearest)."""
+    s = a + b
+    bb = s - a
+    return s, (a - (s - bb)) + (b - bb)
 
-    q_group: [G, d] stored query values of the group's query heads (exact
-    float32 values of the stored dtype). sum_k: [n, d] stored summary keys.
-    Returns float32 [n]: max over the G heads of the fp32 dot product, each
-    product rounded to fp32 and the d products summed one at a time in
-    ascending component order (t = 0 .. d-1) with fp32 rounding after each add.
+
+def exact_dots(q_group: np.ndarray, sum_k: np.ndarray):
+    """Exact q_h . s_i for every segment i and group head h.
+
+    q_group: [G, d], sum_k: [n, d], holding the exact stored values. Returns
+    (dots, inexact): dots is an object array [n, G] of Python floats (where the
+    fp64 sum was exact) or Fractions (where it was not), inexact the bool [n, G]
+    flags of the entries that took the Fraction route.
     """
-    q32 = np.asarray(q_group, dtype=np.float32)
-    s32 = np.asarray(sum_k, dtype=np.float32)
-    n, d = s32.shape
-    acc = np.zeros((n, q32.shape[0]), dtype=np.float32)
+    q = np.asarray(q_group, dtype=np.float64)  # bf16 and fp32 widen exactly
+    s = np.asarray(sum_k, dtype=np.float64)
+    assert np.all(np.isfinite(q)) and np.all(np.isfinite(s)), "non-finite ranking inputs are unsupported"
+    n, d = s.shape
+    G = q.shape[0]
+    acc = np.zeros((n, G), dtype=np.float64)
+    inexact = np.zeros((n, G), dtype=bool)
     for t in range(d):
-        prod = s32[:, t:t + 1] * q32[None, :, t]  # float32 product, rounded
-        acc = acc + prod  # float32 add, rounded
-    return acc.max(axis=1)
+        prod = s[:, t:t + 1] * q[None, :, t]  # two <= 24-bit significands: exact in fp64
+        acc, err = _two_sum(acc, prod)
+        inexact |= err != 0
+    dots = np.empty((n, G), dtype=object)
+    for i in range(n):
+        for h in range(G):
+            if inexact[i, h]:
+                dots[i, h] = sum((Fraction(float(s[i, t])) * Fraction(float(q[h, t])) for t in range(d)), Fraction(0))
+            else:
+                dots[i, h] = float(acc[i, h])
+    return dots, inexact
+
+
+def summary_keys(q_group: np.ndarray, sum_k: np.ndarray) -> np.ndarray:
+    """Ranking key of every segment for one KV head: max over the G heads of the
+    exact dot product (object array [n] of Python floats or Fractions; Python
+    compares the two kinds exactly)."""
+    dots, _ = exact_dots(q_group, sum_k)
+    keys = np.empty(dots.shape[0], dtype=object)
+    for i in range(dots.shape[0]):
+        keys[i] = max(dots[i])
+    return keys
 
 
 def select_top_k(keys: np.ndarray, k: int) -> np.ndarray:
     """Indices of the k largest keys, ties to the lower index, ascending order."""
     n = len(keys)
-    order = sorted(range(n), key=lambda i: (-float(keys[i]), i))
+    order = sorted(range(n), key=lambda i: (-keys[i], i))
     chosen = order[:max(0, min(int(k), n))]
     return np.array(sorted(chosen), dtype=np.int64)
 
@@ -123,7 +154,7 @@ def paged_rows(pool: np.ndarray, block_table_row: np.ndarray, g: int, tokens: np
 
 @dataclass
 class UnitResult:
-    keys: np.ndarray  # float32 [n]
+    keys: np.ndarray  # object [n]: exact keys (Python float or Fraction)
     sel: np.ndarray  # int64 ascending
     tokens: np.ndarray  # int64 sorted
     summaries: np.ndarray  # int64 ascending

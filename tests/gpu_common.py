@@ -83,7 +83,7 @@ def parity(st: W.Structure, lt: W.LayerTensors, plan: Optional[Z.DecodePlan] = N
 
 
 def min_score_margin(res, units, topk) -> float:
-    """Smallest gap s_(k) - s_(k+1) of the fp32 keys at the top-k boundary over ``units``."""
+    """Smallest gap s_(k) - s_(k+1) of the exact keys (as floats) at the top-k boundary over ``units``."""
     m = float("inf")
     for (b, g) in units:
         keys = np.sort(res.units[b][g].keys.astype(np.float64))[::-1]

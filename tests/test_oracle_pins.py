@@ -20,6 +20,7 @@ import torch
 from hierarchical_sparse_kv_gb300 import workloads as W
 from oracle import zoomr_oracle as O
 from tests import brute_force as BF
+from tests import near_ties as NT
 from tests.helpers import oracle_args, unit_args
 
 
@@ -92,9 +93,8 @@ def test_matches_pure_python_brute_force(seed, topk, window, dtype):
     for g in range(2):
         q, kl, vl, bounds, sk, sv = unit_args(st, lt, 0, g)
         exact = BF.exact_scores(q, sk)
-        # The oracle ranks on fp32 keys; the brute force ranks on exact scores. They agree
-        # whenever the gap at the k boundary exceeds both keys' rounding error; check that here.
         ex_sel = BF.dominant_subset(exact, topk)
+        assert [Fraction(x) for x in res.units[0][g].keys] == exact
         out, sel, nrows = BF.brute_unit(q, kl, vl, bounds, sk, sv, topk, window, selected=ex_sel)
         u = res.units[0][g]
         assert list(u.sel) == sel
@@ -155,41 +155,73 @@ def test_negative_zero_and_positive_zero_keys_tie():
     assert list(O.select_top_k(keys, 1)) == [0]
 
 
-def test_key_rounding_order_hand_case():
-    """Ascending-order fp32 sum with rounding after every add: 2^24 + 1 rounds to
-    2^24 (tie to even) and the following -2^24 leaves 0, while the exact sum is 1."""
+def test_key_is_exact_where_an_fp32_chain_cancels():
+    """Hand cases: 2^24 + 1 - 2^24 is 1 exactly (an fp32 chain in ascending order
+    gives 0), in any order of the components; a product is not rounded before the
+    add: (1 + 2^-12)^2 = 1 + 2^-11 + 2^-24 exactly."""
     q = np.array([[1.0, 1.0, 1.0, 0.0]], dtype=np.float32)
-    s = np.array([[2.0 ** 24, 1.0, -(2.0 ** 24), 5.0]], dtype=np.float32)
-    assert O.summary_keys(q, s)[0] == 0.0
-    s2 = np.array([[1.0, 2.0 ** 24, -(2.0 ** 24), 5.0]], dtype=np.float32)  # 1 + 2^24 rounds to 2^24 too
-    assert O.summary_keys(q, s2)[0] == 0.0
-    s3 = np.array([[2.0 ** 24, -(2.0 ** 24), 1.0, 5.0]], dtype=np.float32)  # exact all the way
-    assert O.summary_keys(q, s3)[0] == 1.0
-    # the product is rounded to fp32 before the add: (1 + 2^-12)^2 = 1 + 2^-11 + 2^-24 -> 1 + 2^-11 (tie to even)
+    for s in ([2.0 ** 24, 1.0, -(2.0 ** 24), 5.0], [1.0, 2.0 ** 24, -(2.0 ** 24), 5.0],
+              [2.0 ** 24, -(2.0 ** 24), 1.0, 5.0]):
+        assert O.summary_keys(q, np.array([s], dtype=np.float32))[0] == 1
     a = np.float32(1.0 + 2.0 ** -12)
-    assert O.summary_keys(np.array([[a]], np.float32), np.array([[a]], np.float32))[0] == np.float32(1 + 2.0 ** -11)
+    key = O.summary_keys(np.array([[a]], np.float32), np.array([[a]], np.float32))[0]
+    assert Fraction(key) == Fraction(1) + Fraction(1, 2 ** 11) + Fraction(1, 2 ** 24)
 
 
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_keys_within_the_recursive_summation_bound_of_the_exact_score(dtype):
-    """|fp32 key - exact max_h q.s| <= gamma_{d+1} * sum_t |q_t s_t| (Higham's bound for
-    d rounded products summed recursively), and exact for integer-valued inputs."""
-    st, lt = _tiny(seed=12, dtype=dtype, head_dim=32, num_q_heads=4, num_kv_heads=1)
-    q = W.to_numpy32(lt.q)[0]
-    sk = W.to_numpy32(lt.sum_k)[:, 0]
-    keys = O.summary_keys(q, sk)
-    u = 2.0 ** -24
-    d = q.shape[1]
-    gamma = (d + 1) * u / (1 - (d + 1) * u)
-    for i in range(sk.shape[0]):
-        exact = [BF.exact_dot(q[h], sk[i]) for h in range(q.shape[0])]
-        bound = max(gamma * math.fsum(abs(float(a) * float(b)) for a, b in zip(q[h], sk[i])) for h in range(4))
-        assert abs(Fraction(float(keys[i])) - max(exact)) <= Fraction(bound)
-    qi = np.round(q * 4).astype(np.float32)
-    si = np.round(sk * 4).astype(np.float32)
-    keys_i = O.summary_keys(qi, si)
-    for i in range(si.shape[0]):
-        assert Fraction(float(keys_i[i])) == max(BF.exact_dot(qi[h], si[i]) for h in range(4))
+def test_inexact_fp64_sum_takes_the_fraction_route():
+    """2^60 + 1 - 2^60: the fp64 sum loses the 1 (TwoSum flags it) and the key
+    comes from exact rational arithmetic; a clean sum stays on the fp64 route."""
+    q = np.array([[1.0, 1.0, 1.0], [0.5, 0.0, 0.0]], dtype=np.float32)
+    s = np.array([[2.0 ** 60, 1.0, -(2.0 ** 60)], [3.0, 1.0, 2.0]], dtype=np.float32)
+    dots, inexact = O.exact_dots(q, s)
+    assert inexact[0, 0] and not inexact[1, 0] and not inexact[0, 1]
+    assert isinstance(dots[0, 0], Fraction) and dots[0, 0] == 1
+    assert dots[0, 1] == 2.0 ** 59 and dots[1, 0] == 6.0 and dots[1, 1] == 1.5
+    assert list(O.summary_keys(q, s)) == [2.0 ** 59, 6.0]
+
+
+@pytest.mark.parametrize("dtype,scale", [("f32", 1.0), ("bf16", 1.0), ("bf16", 1e-30), ("f32", 1e20)])
+def test_keys_equal_the_exact_rational_score(dtype, scale):
+    """Full-width (d = 128) random inputs, with a few values planted far below the
+    rest (tiny and subnormal magnitudes) so that some fp64 sums are inexact: every
+    key equals max over the group of the exact Fraction dot product."""
+    rng = np.random.default_rng(31)
+    G, n, d = 4, 12, 128
+    q = rng.standard_normal((G, d)) * 3.0
+    s = rng.standard_normal((n, d)) * 0.12 * scale
+    s[2, 5] = 1e-30 * scale
+    s[3, 7] = 3e-39  # subnormal in fp32 and bf16
+    q[1, 9] = 2.0 ** -70
+    s[4, :] = s[5, :]  # an exact tie
+    q32 = torch.from_numpy(q).to(torch.float32).to(W.torch_dtype(dtype)).to(torch.float32).numpy()
+    s32 = torch.from_numpy(s).to(torch.float32).to(W.torch_dtype(dtype)).to(torch.float32).numpy()
+    dots, inexact = O.exact_dots(q32, s32)
+    keys = O.summary_keys(q32, s32)
+    exact = BF.exact_scores(q32, s32)
+    for i in range(n):
+        for h in range(G):
+            assert Fraction(dots[i, h]) == BF.exact_dot(q32[h], s32[i])
+        assert Fraction(keys[i]) == exact[i]
+    assert keys[4] == keys[5]
+
+
+def test_fp32_chain_and_exact_orders_disagree_on_planted_near_ties():
+    """bf16 near-ties planted at the top-k boundary (two one-ulp nudges of a
+    summary key) where an ascending fp32 chain ranks the pair the other way: the
+    oracle's selection follows the exact scores."""
+    st, lt = _tiny(seed=17, dtype="bf16", head_dim=128, seq_len=1024, seg_len_range=(32, 64), topk=4, window=0,
+                   num_q_heads=8, num_kv_heads=2)
+    flips = NT.plant_near_ties(st, lt)
+    assert flips, "no near-tie planted"
+    res = O.decode_step(**oracle_args(st, lt))
+    for (b, g, i, j) in flips:
+        q, _, _, _, sk, _ = unit_args(st, lt, b, g)
+        exact = BF.exact_scores(q, sk)
+        f32 = NT.fp32_chain_keys(q, sk)
+        assert (exact[i] > exact[j]) != (f32[i] > f32[j] or (f32[i] == f32[j] and i < j))
+        k = int(st.topk[b])
+        assert list(res.units[b][g].sel) == sorted(sorted(range(len(exact)), key=lambda m: (-exact[m], m))[:k])
+        assert list(res.units[b][g].sel) != list(O.select_top_k(f32, k))
 
 
 def test_group_of_one_is_per_head_selection_and_mqa_shares_one():
@@ -275,3 +307,9 @@ def test_planted_mistakes_are_caught():
     keys = np.array([1.0, 3.0, 3.0, 0.5], dtype=np.float32)
     wrong = sorted(sorted(range(4), key=lambda i: (-keys[i], -i))[:1])
     assert wrong != list(O.select_top_k(keys, 1)) == BF.dominant_subset(list(keys), 1)
+
+    # a key taken as an ascending fp32 chain (rounded products and adds) picks the wrong segment
+    q1 = np.ones((1, 3), np.float32)
+    s2 = np.array([[2.0 ** 24, 1.0, -(2.0 ** 24)], [0.5, 0.0, 0.0]], np.float32)
+    assert list(O.select_top_k(O.summary_keys(q1, s2), 1)) == [0]
+    assert list(O.select_top_k(NT.fp32_chain_keys(q1, s2), 1)) == [1]
