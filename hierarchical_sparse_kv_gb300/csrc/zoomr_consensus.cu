@@ -23,6 +23,7 @@
 
 #include <cstdint>
 
+#include "zoomr_exact_key.cuh"
 #include "zoomr_internal.h"
 
 namespace zr {
@@ -32,77 +33,93 @@ constexpr unsigned kFullMask = 0xFFFFFFFFu;
 constexpr int kVoteThreads = 256;
 constexpr int kConsensusThreads = 256;
 
-template <typename T>
-__device__ __forceinline__ float elem(const T* p, int i);
-template <>
-__device__ __forceinline__ float elem<float>(const float* p, int i) {
-  return p[i];
-}
-template <>
-__device__ __forceinline__ float elem<__nv_bfloat16>(const __nv_bfloat16* p, int i) {
-  return __bfloat162float(p[i]);
-}
-
-// Element e (0 .. 16 / sizeof(T) - 1) of a 16-byte piece, as a float.
-template <typename T>
-__device__ __forceinline__ float piece_elem(const uint4& w, int e) {
-  constexpr int PER_WORD = 4 / static_cast<int>(sizeof(T));
-  const int wi = e / PER_WORD;
-  const uint32_t x = wi == 0 ? w.x : wi == 1 ? w.y : wi == 2 ? w.z : w.w;
-  if constexpr (sizeof(T) == 2)
-    return __uint_as_float((e & 1) ? (x & 0xFFFF0000u) : (x << 16));
-  else
-    return __uint_as_float(x);
-}
-
-// Shared memory: q of the group [G][D] f32 | keys [hc][n_max + 4] f32, hc heads at a time.
-// Thread pairs (summary i, head h) run one fp32 chain each, in ascending component order, over the
-// row loaded whole in 16-byte pieces (the hc threads of a row share it through L1).
+// Shared memory: the exact-key scorer's query limb tables | key high words [n_max + 4] u64 | key low words
+// [n_max + 4] u64 | flag [n_max + 2] | fp32 enclosures lo, hi [n_max] each.
 template <typename T, int D>
-__global__ void __launch_bounds__(kVoteThreads) zr_vote_kernel(StepArgs a, const T* __restrict__ mean_keys,
-                                                               int32_t* __restrict__ votes, int hc) {
-  extern __shared__ __align__(16) float vsmem[];
-  constexpr int EPP = 16 / static_cast<int>(sizeof(T));  // elements per 16-byte piece
-  constexpr int P = D / EPP;                              // pieces per row
-  float* qs = vsmem;
-  float* keys = vsmem + static_cast<size_t>(a.G) * D;
+struct VoteLayout {
+  using SC = xk::Scorer<T, D, kVoteThreads>;
+  __host__ __device__ static constexpr size_t q_bytes(int G) { return (SC::smem_bytes(G) + 15) / 16 * 16; }
+  __host__ __device__ static constexpr size_t bytes(int G, int n_max) {
+    return q_bytes(G) + 2 * sizeof(uint64_t) * (static_cast<size_t>(n_max) + 4) +
+           sizeof(int) * (static_cast<size_t>(n_max) + 2) + 2 * sizeof(float) * static_cast<size_t>(n_max);
+  }
+};
+
+// For every query head of the group, one at a time: the top-k of the summaries by the exact key
+// alpha_i = q_h . kbar_i on the stored values (ties to the lower index) and one vote per selected summary.
+// The fp32 estimates decide where their enclosures separate at the k boundary; otherwise the keys are
+// computed exactly (the integer limbs, or the general 640-bit path), the limb tables built once per unit.
+template <typename T, int D>
+__global__ void __maxnreg__(96) zr_vote_kernel(StepArgs a, const T* __restrict__ mean_keys,
+                                               int32_t* __restrict__ votes) {
+  using LY = VoteLayout<T, D>;
+  using SC = typename LY::SC;
+  extern __shared__ __align__(16) unsigned char vsmem[];
+  const int G = a.G, nmax = a.n_max;
+  int* qh = reinterpret_cast<int*>(vsmem);
+  int* ql = qh + G * SC::kQRow;
+  int* qtail = ql + G * SC::kQRow;
+  uint64_t* kh = reinterpret_cast<uint64_t*>(vsmem + LY::q_bytes(G));
+  uint64_t* kl = kh + nmax + 4;
+  int* flag = reinterpret_cast<int*>(kl + nmax + 4);
+  float* elo = reinterpret_cast<float*>(flag + nmax + 2);
+  float* ehi = elo + nmax;
+  __shared__ int s_flags;
+  __shared__ uint32_t s_red[4 * kVoteThreads / 32];
+  __shared__ uint32_t s_cert[3 * kVoteThreads / 32];
   const int g = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+  const int u = b * a.Hkv + g;
   const int s0 = a.meta.seg_ptr[b];
   const int n = a.meta.seg_ptr[b + 1] - s0;
   const int k = a.meta.topk[b];  // clipped to n at plan time
-  const int nk = a.n_max + 4;
-  const T* qg = static_cast<const T*>(a.q) + (static_cast<size_t>(b) * a.Hq + static_cast<size_t>(g) * a.G) * D;
-  int32_t* vb = votes + static_cast<size_t>(b) * a.n_max;
-  for (int t = tid; t < a.G * D; t += kVoteThreads) qs[t] = elem<T>(qg, t);
-  for (int h0 = 0; h0 < a.G; h0 += hc) {
-    const int nh = min(hc, a.G - h0);
-    __syncthreads();  // q staged; the previous heads' readers are done
-    for (int pi = tid; pi < n * nh; pi += kVoteThreads) {
-      const int i = pi / nh, h = pi - i * nh;
-      const uint4* kr = reinterpret_cast<const uint4*>(mean_keys + (static_cast<size_t>(s0 + i) * a.Hkv + g) * D);
-      uint4 w[P];
-#pragma unroll
-      for (int pc = 0; pc < P; ++pc) w[pc] = __ldg(kr + pc);
-      const float* qh = qs + (h0 + h) * D;
-      float acc = 0.0f;
-#pragma unroll
-      for (int pc = 0; pc < P; ++pc)
-#pragma unroll
-        for (int e = 0; e < EPP; ++e) acc = __fadd_rn(acc, __fmul_rn(qh[pc * EPP + e], piece_elem<T>(w[pc], e)));
-      keys[h * nk + i] = acc;
+  const T* qg = static_cast<const T*>(a.q) + (static_cast<size_t>(b) * a.Hq + static_cast<size_t>(g) * G) * D;
+  const T* rows = mean_keys + (static_cast<size_t>(s0) * a.Hkv + g) * D;
+  const size_t stride = static_cast<size_t>(a.Hkv) * D;
+  int32_t* vb = votes + static_cast<size_t>(b) * nmax;
+  if (tid == 0) s_flags = 0;
+  bool exact_ready = false;  // CTA-uniform
+  xk::Frame fr{};
+  uint4 cache[SC::kVPS];
+  for (int h = 0; h < G; ++h) {
+    xk::estimate_rows<T, D, kVoteThreads, false>(qg, h, 1, rows, stride, n,
+                                                  [&](int r, int, float mid, float lo, float hi) {
+                                                    kh[r] = 0;
+                                                    kl[r] = xk::order_bits(mid);
+                                                    elo[r] = lo;
+                                                    ehi[r] = hi;
+                                                  });
+    __syncthreads();
+    if (!xk::certify_top_k<kVoteThreads>(elo, ehi, n, k, kh, kl, flag, s_cert)) {
+      int fl = 0;
+      if (!exact_ready) {
+        fr = xk::unit_frame<T, D, kVoteThreads>(qg, G, rows, stride, n, s_red, qtail, fl, cache);
+        if (!fr.general) xk::load_q_limbs<T, D, kVoteThreads>(qg, G, fr, qh, ql, qtail, fl);
+        exact_ready = true;
+      }
+      if (!fr.general)
+        xk::score_rows<T, D, kVoteThreads, false>(rows, stride, n, fr, qh, ql, qtail, h, 1, fl, cache,
+                                                   [&](int r, int, uint64_t uh, uint64_t ul) {
+                                                     kh[r] = uh;
+                                                     kl[r] = ul;
+                                                   });
+      if (fl) atomicOr(&s_flags, fl);
+      __syncthreads();
+      const int uflags = s_flags;
+      if ((uflags & xk::kFlagNonFinite) && tid == 0) atomicOr(a.err, kErrNonFinite);
+      if (fr.general || (uflags & xk::kFlagDeep)) {
+        // a value far below its side's largest (or a non-finite one): the general 640-bit path, keys in
+        // the workspace
+        uint32_t* big = a.bigkeys + static_cast<size_t>(u) * nmax * xk::kBigDigits;
+        xk::big_keys<T, D, kVoteThreads>(qg, h, 1, rows, stride, n, big);
+        xk::big_rank_select<kVoteThreads>(big, n, k, flag);
+      } else {
+        xk::rank_select<kVoteThreads>(kh, kl, n, k, !fr.narrow, flag);
+      }
     }
     __syncthreads();
-    for (int pi = tid; pi < nh * n; pi += kVoteThreads) {
-      const int h = pi / n, i = pi - h * n;
-      const float* kh = keys + h * nk;
-      const float ki = kh[i];
-      int beat = 0;
-      for (int j = 0; j < n; ++j) {
-        const float kj = kh[j];
-        beat += (kj > ki) | ((kj == ki) & (j < i));
-      }
-      if (beat < k) atomicAdd(vb + i, 1);
-    }
+    for (int i = tid; i < n; i += kVoteThreads)
+      if (flag[i]) atomicAdd(vb + i, 1);
+    __syncthreads();  // flag, the estimates and the keys are reused by the next head
   }
 }
 
@@ -342,15 +359,8 @@ __global__ void __launch_bounds__(32) zr_decode_advance_kernel(StepArgs a, const
 
 }  // namespace
 
-// Heads whose keys fit the vote kernel's shared memory at once (at least 1, at most the group).
-int vote_heads(int G, int d, int n_max) {
-  const size_t budget = 96 * 1024 - static_cast<size_t>(G) * d * sizeof(float);
-  const int fit = static_cast<int>(budget / ((static_cast<size_t>(n_max) + 4) * sizeof(float)));
-  return fit < 1 ? 1 : (fit < G ? fit : G);
-}
-
 size_t vote_smem_bytes(int G, int d, int n_max) {
-  return (static_cast<size_t>(G) * d + static_cast<size_t>(vote_heads(G, d, n_max)) * (n_max + 4)) * sizeof(float);
+  return d == 64 ? VoteLayout<float, 64>::bytes(G, n_max) : VoteLayout<float, 128>::bytes(G, n_max);
 }
 size_t consensus_smem_bytes(int n_max) {
   return (static_cast<size_t>(n_max) + (n_max + 1) + (2 * n_max + 1) + 2 * (n_max + 2)) * sizeof(int);
@@ -360,29 +370,28 @@ zr_status launch_vote(const Plan& p, const StepArgs& a, const void* mean_keys, i
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const dim3 grid(p.Hkv, p.B), block(kVoteThreads);
   const size_t smem = vote_smem_bytes(p.G, p.d, p.n_max);
-  const int hc = vote_heads(p.G, p.d, p.n_max);
   cudaError_t e = cudaSuccess;
   if (p.cfg.dtype == ZR_BF16) {
     auto* mk = static_cast<const __nv_bfloat16*>(mean_keys);
     if (p.d == 64) {
       cudaFuncSetAttribute(zr_vote_kernel<__nv_bfloat16, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem));
-      zr_vote_kernel<__nv_bfloat16, 64><<<grid, block, smem, s>>>(a, mk, votes, hc);
+      zr_vote_kernel<__nv_bfloat16, 64><<<grid, block, smem, s>>>(a, mk, votes);
     } else {
       cudaFuncSetAttribute(zr_vote_kernel<__nv_bfloat16, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem));
-      zr_vote_kernel<__nv_bfloat16, 128><<<grid, block, smem, s>>>(a, mk, votes, hc);
+      zr_vote_kernel<__nv_bfloat16, 128><<<grid, block, smem, s>>>(a, mk, votes);
     }
   } else {
     auto* mk = static_cast<const float*>(mean_keys);
     if (p.d == 64) {
       cudaFuncSetAttribute(zr_vote_kernel<float, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem));
-      zr_vote_kernel<float, 64><<<grid, block, smem, s>>>(a, mk, votes, hc);
+      zr_vote_kernel<float, 64><<<grid, block, smem, s>>>(a, mk, votes);
     } else {
       cudaFuncSetAttribute(zr_vote_kernel<float, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem));
-      zr_vote_kernel<float, 128><<<grid, block, smem, s>>>(a, mk, votes, hc);
+      zr_vote_kernel<float, 128><<<grid, block, smem, s>>>(a, mk, votes);
     }
   }
   e = cudaGetLastError();

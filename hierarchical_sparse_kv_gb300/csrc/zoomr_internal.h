@@ -27,7 +27,7 @@ constexpr int kUnitStartRows = ZR_UNIT_START_ROWS;
 constexpr uint32_t kSummaryFlag = 0x80000000u;  // row id refers to the summary tensors
 constexpr uint32_t kInvalidRow = 0xFFFFFFFFu;   // masked row (past the chunk end, or a bad block id)
 
-enum : int32_t { kErrBadBlock = 1, kErrBadIndex = 2 };
+enum : int32_t { kErrBadBlock = 1, kErrBadIndex = 2, kErrNonFinite = 4 };
 
 // Small device metadata copied from the host at plan time (one allocation).
 struct DeviceMeta {
@@ -50,6 +50,7 @@ struct WsLayout {
   size_t sel;         // int32 [U][k_max] selected segments, ascending
   size_t part_o;      // float [U + attend_warps][G][d] unnormalised split outputs
   size_t part_ml;     // float [U + attend_warps][G][2] split (max, sum) in log2 units
+  size_t bigkeys;     // uint32 [U][n_max][20] exact keys of units that take the general (640-bit) path
   size_t votes;       // consensus only: int32 [B][n_max] vote counts, zero between selections
   size_t cruns;       // consensus only: int32 [B][n_max + 1][2] the last selection's runs before the window
   size_t cnruns;      // consensus only: int32 [B] their count
@@ -97,6 +98,7 @@ struct StepArgs {
   int32_t* sel;
   float* part_o;
   float2* part_ml;
+  uint32_t* bigkeys;
   int32_t* cruns;   // consensus only
   int32_t* cnruns;  // consensus only
   int B, Hq, Hkv, G, window, num_blocks, max_blocks, k_max, n_max, attend_warps;

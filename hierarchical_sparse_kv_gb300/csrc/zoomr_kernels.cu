@@ -31,6 +31,7 @@
 #include <cstdlib>
 #include <cstring>
 
+#include "zoomr_exact_key.cuh"
 #include "zoomr_internal.h"
 
 namespace zr {
@@ -64,29 +65,6 @@ __device__ __forceinline__ float bf16_hi(uint32_t x) { return __uint_as_float(x 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
-}
-
-template <typename T>
-__device__ __forceinline__ float to_float(T x);
-template <>
-__device__ __forceinline__ float to_float<float>(float x) { return x; }
-template <>
-__device__ __forceinline__ float to_float<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
-
-// Load 8 consecutive elements (16 B for bf16, 32 B for f32) as floats.
-template <typename T>
-__device__ __forceinline__ void load8(const T* p, float (&v)[8]);
-template <>
-__device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16* p, float (&v)[8]) {
-  const uint4 w = *reinterpret_cast<const uint4*>(p);
-  v[0] = bf16_lo(w.x); v[1] = bf16_hi(w.x); v[2] = bf16_lo(w.y); v[3] = bf16_hi(w.y);
-  v[4] = bf16_lo(w.z); v[5] = bf16_hi(w.z); v[6] = bf16_lo(w.w); v[7] = bf16_hi(w.w);
-}
-template <>
-__device__ __forceinline__ void load8<float>(const float* p, float (&v)[8]) {
-  const float4 a = *reinterpret_cast<const float4*>(p);
-  const float4 b = *reinterpret_cast<const float4*>(p + 4);
-  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
 
 // Load E (= 2 or 4) consecutive elements as floats.
@@ -211,43 +189,79 @@ __device__ void add_sink_range(const StepArgs& a, int u, int Ns, int32_t* rg, in
   }
 }
 
-// Shared memory: q [kMaxGroup][D+4] f32 | staged summary-key rows, raw, kStageRows x (D*sizeof(T)+16)
-//   | pair values [kStageRows][kMaxGroup] | keys [n_max+4] | flag [n_max+2] | bounds [n_max+1] | list [n_max] | runs_s [n_max] | runs_e [n_max]
-// The 16-byte row pad keeps the threads' row reads in different banks.
+// Shared memory: the exact-key scorer's query limb tables | key high words [n_max + 4] u64 | key low
+//   words [n_max + 4] u64 | flag [n_max + 2] | bounds [n_max + 1] | list [n_max] | runs_s [n_max] | runs_e [n_max]
+//   | fp32 enclosures lo, hi [n_max] each
 template <typename T, int D>
 struct SelectLayout {
-  static constexpr int DP = D + 4;
-  static constexpr int kRowBytes = D * static_cast<int>(sizeof(T)) + 16;
-  static constexpr int kStageRows = D * sizeof(T) >= 512 ? 128 : 256;
-  static constexpr int kPieces = D * static_cast<int>(sizeof(T)) / 16;  // 16-byte pieces per row
-  // Rows staged per batch: the plan's largest segment count, at most kStageRows (so that a small
-  // plan's select CTA leaves room for the attend CTAs that wait beside it on the same SM).
-  __host__ __device__ static constexpr int stage_rows(int n_max) { return n_max < kStageRows ? (n_max > 0 ? n_max : 1) : kStageRows; }
-  __host__ __device__ static constexpr size_t fixed_bytes(int n_max) {
-    return static_cast<size_t>(kMaxGroup) * DP * 4 +
-           static_cast<size_t>(stage_rows(n_max)) * (kRowBytes + static_cast<size_t>(kMaxGroup) * 4);
+  using SC = xk::Scorer<T, D, kSelectThreads>;
+  __host__ __device__ static constexpr size_t q_bytes(int G) { return (SC::smem_bytes(G) + 15) / 16 * 16; }
+  __host__ __device__ static constexpr size_t bytes(int G, int n_max) {
+    return q_bytes(G) + 2 * sizeof(uint64_t) * (static_cast<size_t>(n_max) + 4) +
+           sizeof(int) * (5 * static_cast<size_t>(n_max) + 3) + 2 * sizeof(float) * static_cast<size_t>(n_max);
   }
 };
 
+// The exact top-k of one unit (every thread of the select CTA calls it), for units whose fp32 enclosures
+// do not separate at the k boundary: exact integer keys (the general 640-bit path where a value lies far
+// below its side's largest or is not finite), then the exact ranking into flag. Shared-memory scratch:
+// the query limb tables qh, ql, qtail, the keys kh, kl, the unit flags word and red.
 template <typename T, int D>
-__global__ void __launch_bounds__(kSelectThreads) zr_select_kernel(StepArgs a) {
+__device__ __noinline__ void exact_select(const StepArgs& a, int u, const T* qg, const T* rows, size_t stride,
+                                          int n, int k, int* qh, int* ql, int* qtail, uint64_t* kh, uint64_t* kl,
+                                          int* flag, int* s_flags, uint32_t* s_red) {
+  using SC = xk::Scorer<T, D, kSelectThreads>;
+  const int G = a.G;
+  int fl = 0;
+  uint4 cache[SC::kVPS];
+  const xk::Frame fr = xk::unit_frame<T, D, kSelectThreads>(qg, G, rows, stride, n, s_red, qtail, fl, cache);
+  if (!fr.general) {
+    xk::load_q_limbs<T, D, kSelectThreads>(qg, G, fr, qh, ql, qtail, fl);
+    xk::score_rows<T, D, kSelectThreads, true>(rows, stride, n, fr, qh, ql, qtail, 0, G, fl, cache,
+                                                 [&](int r, int, uint64_t uh, uint64_t ul) {
+                                                   kh[r] = uh;
+                                                   kl[r] = ul;
+                                                 });
+  }
+  if (fl) atomicOr(s_flags, fl);
+  __syncthreads();
+  const int uflags = *s_flags;
+  if ((uflags & xk::kFlagNonFinite) && threadIdx.x == 0) atomicOr(a.err, kErrNonFinite);
+  if (fr.general || (uflags & xk::kFlagDeep)) {
+    uint32_t* big = a.bigkeys + static_cast<size_t>(u) * a.n_max * xk::kBigDigits;
+    xk::big_keys<T, D, kSelectThreads>(qg, 0, G, rows, stride, n, big);
+    xk::big_rank_select<kSelectThreads>(big, n, k, flag);
+  } else {
+    xk::rank_select<kSelectThreads>(kh, kl, n, k, !fr.narrow, flag);
+  }
+}
+
+// 80 registers per thread (no spills): a select CTA then leaves room on its SM for an attend CTA of
+// the same layer, which launches early and waits (programmatic dependent launch).
+template <typename T, int D>
+__global__ void __maxnreg__(80) zr_select_kernel(StepArgs a) {
   using LY = SelectLayout<T, D>;
-  constexpr int DP = LY::DP;
+  using SC = typename LY::SC;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const int g = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
   const int u = b * a.Hkv + g;
   const int G = a.G, nmax = a.n_max;
-  float* qs = reinterpret_cast<float*>(smem_raw);
-  unsigned char* stage = smem_raw + static_cast<size_t>(kMaxGroup) * DP * 4;
-  const int SR = LY::stage_rows(nmax);
-  float* pairv = reinterpret_cast<float*>(stage + static_cast<size_t>(SR) * LY::kRowBytes);
-  float* keys = reinterpret_cast<float*>(smem_raw + LY::fixed_bytes(nmax));
-  int* flag = reinterpret_cast<int*>(keys + nmax + 4);
+  int* qh = reinterpret_cast<int*>(smem_raw);
+  int* ql = qh + G * SC::kQRow;
+  int* qtail = ql + G * SC::kQRow;
+  uint64_t* kh = reinterpret_cast<uint64_t*>(smem_raw + LY::q_bytes(G));
+  uint64_t* kl = kh + nmax + 4;
+  int* flag = reinterpret_cast<int*>(kl + nmax + 4);
   int* bnd = flag + nmax + 2;
   int* list = bnd + nmax + 1;
   int* runs_s = list + nmax;
   int* runs_e = runs_s + nmax;
+  float* elo = reinterpret_cast<float*>(runs_e + nmax);
+  float* ehi = elo + nmax;
   __shared__ int s_rstar;
+  __shared__ int s_flags;
+  __shared__ uint32_t s_red[4 * kSelectThreads / 32];
+  __shared__ uint32_t s_cert[3 * kSelectThreads / 32];
 
   pdl_trigger();
   // Plan metadata is never written by a kernel: read it before waiting on the previous kernel.
@@ -257,108 +271,39 @@ __global__ void __launch_bounds__(kSelectThreads) zr_select_kernel(StepArgs a) {
   const int k = a.meta.topk[b];
   const int Ns = a.meta.prompt_lens[b];
   for (int i = tid; i <= n; i += blockDim.x) bnd[i] = a.meta.seg_bounds[s0 + b + i];
+  if (tid == 0) s_flags = 0;
   const T* qg = static_cast<const T*>(a.q) + (static_cast<size_t>(b) * a.Hq + static_cast<size_t>(g) * G) * D;
+  const T* rows = static_cast<const T*>(a.sum_k) + (static_cast<size_t>(s0) * a.Hkv + g) * D;
+  const size_t stride = static_cast<size_t>(a.Hkv) * D;
   {
-    // the group's queries and the first batch of its summary-key rows, into L2 before the wait
+    // the group's queries and the unit's summary-key rows, into L2 before the wait
     constexpr size_t RB = D * sizeof(T);
     if (tid < kSelectThreads / 2) {
       prefetch_span(qg, G * RB, tid, kSelectThreads / 2);
     } else {
-      const char* sk = static_cast<const char*>(a.sum_k);
-      const int rows = min(SR, n);
-      for (int i = tid - kSelectThreads / 2; i < rows; i += kSelectThreads / 2)
-        prefetch_span(sk + (static_cast<size_t>(s0 + i) * a.Hkv + g) * RB, RB, 0, 1);
+      const int rows_pf = min(n, kSelectThreads);
+      for (int i = tid - kSelectThreads / 2; i < rows_pf; i += kSelectThreads / 2)
+        prefetch_span(rows + i * stride, RB, 0, 1);
     }
   }
   pdl_wait();
 
-  // 1. ranking key: max over the group of the fp32 dot, products and sums rounded, ascending order.
-  //    Up to SR summary-key rows are staged raw in one memory round trip (the first batch
-  //    together with the queries); then every (segment, head) pair runs its own sequential chain.
-  const char* sk = static_cast<const char*>(a.sum_k);
-  constexpr int PER = LY::kStageRows * LY::kPieces / kSelectThreads;
-  static_assert(LY::kStageRows * LY::kPieces % kSelectThreads == 0, "staging split");
-  constexpr int EPP = 16 / static_cast<int>(sizeof(T));  // elements per 16-byte piece
-  for (int c0 = 0; c0 < n; c0 += SR) {
-    const int rows = min(SR, n - c0);
-    __syncthreads();  // the previous batch's readers are done
-    uint4 v[PER];
-    float qv[8];
-    const bool q_here = c0 == 0 && tid < G * (D / 8);
-    if (q_here) load8<T>(qg + tid * 8, qv);
-#pragma unroll
-    for (int j = 0; j < PER; ++j) {
-      const int e = tid + j * kSelectThreads;
-      if (e < rows * LY::kPieces)
-        v[j] = *reinterpret_cast<const uint4*>(
-            sk + ((static_cast<size_t>(s0 + c0 + e / LY::kPieces) * a.Hkv + g) * D) * sizeof(T) +
-            (e % LY::kPieces) * 16);
-    }
-    if (q_here) {
-      float4* dst = reinterpret_cast<float4*>(qs + (tid / (D / 8)) * DP + (tid % (D / 8)) * 8);
-      dst[0] = make_float4(qv[0], qv[1], qv[2], qv[3]);
-      dst[1] = make_float4(qv[4], qv[5], qv[6], qv[7]);
-    }
-#pragma unroll
-    for (int j = 0; j < PER; ++j) {
-      const int e = tid + j * kSelectThreads;
-      if (e < rows * LY::kPieces)
-        *reinterpret_cast<uint4*>(stage + (e / LY::kPieces) * LY::kRowBytes + (e % LY::kPieces) * 16) = v[j];
-    }
-    __syncthreads();
-    // One sequential chain per (segment, head) pair, 16-byte shared-memory reads of both operands.
-    const int npairs = rows * G;
-    for (int pi = tid; pi < npairs; pi += blockDim.x) {
-      const unsigned char* srow = stage + (pi / G) * LY::kRowBytes;
-      const float4* q4 = reinterpret_cast<const float4*>(qs + (pi % G) * DP);
-      float acc = 0.f;
-#pragma unroll 4
-      for (int pc = 0; pc < LY::kPieces; ++pc) {
-        const uint4 w = *reinterpret_cast<const uint4*>(srow + 16 * pc);
-        float sv[EPP], qv[EPP];
-        if constexpr (sizeof(T) == 2) {
-          sv[0] = bf16_lo(w.x); sv[1] = bf16_hi(w.x); sv[2] = bf16_lo(w.y); sv[3] = bf16_hi(w.y);
-          sv[4] = bf16_lo(w.z); sv[5] = bf16_hi(w.z); sv[6] = bf16_lo(w.w); sv[7] = bf16_hi(w.w);
-          const float4 qa = q4[2 * pc], qb = q4[2 * pc + 1];
-          qv[0] = qa.x; qv[1] = qa.y; qv[2] = qa.z; qv[3] = qa.w; qv[4] = qb.x; qv[5] = qb.y; qv[6] = qb.z; qv[7] = qb.w;
-        } else {
-          sv[0] = __uint_as_float(w.x); sv[1] = __uint_as_float(w.y);
-          sv[2] = __uint_as_float(w.z); sv[3] = __uint_as_float(w.w);
-          const float4 qa = q4[pc];
-          qv[0] = qa.x; qv[1] = qa.y; qv[2] = qa.z; qv[3] = qa.w;
-        }
-#pragma unroll
-        for (int e = 0; e < EPP; ++e) acc = __fadd_rn(acc, __fmul_rn(qv[e], sv[e]));
-      }
-      pairv[pi] = acc;
-    }
-    __syncthreads();
-    for (int i = tid; i < rows; i += blockDim.x) {
-      float key = pairv[i * G];
-      for (int h = 1; h < G; ++h) key = fmaxf(key, pairv[i * G + h]);
-      keys[c0 + i] = key;
-    }
-  }
-  if (tid < 4) keys[n + tid] = -INFINITY;  // pad for the 4-wide reads below
+  // 1. ranking key: max over the group of the exact dot q_h . s_i. First an fp32 estimate of every key
+  //    with an enclosure of the exact value (lane-parallel fused multiply-adds).
+  xk::estimate_rows<T, D, kSelectThreads, true>(qg, 0, G, rows, stride, n,
+                                                [&](int r, int, float mid, float lo, float hi) {
+                                                  kh[r] = 0;
+                                                  kl[r] = xk::order_bits(mid);
+                                                  elo[r] = lo;
+                                                  ehi[r] = hi;
+                                                });
   __syncthreads();
 
-  // 2. top-k: segment i is selected iff fewer than k segments beat it (a greater key, or an equal
-  //    key and a lower index). Branch-free count over 4-wide reads; the pad never beats a key.
-  const float4* keys4 = reinterpret_cast<const float4*>(keys);
-  for (int i = tid; i < n; i += blockDim.x) {
-    const float ki = keys[i];
-    int cnt = 0;
-#pragma unroll 4
-    for (int j4 = 0; j4 < (n + 3) >> 2; ++j4) {
-      const float4 kv = keys4[j4];
-      const int j = 4 * j4;
-      cnt += (kv.x > ki) | ((kv.x == ki) & (j < i));
-      cnt += (kv.y > ki) | ((kv.y == ki) & (j + 1 < i));
-      cnt += (kv.z > ki) | ((kv.z == ki) & (j + 2 < i));
-      cnt += (kv.w > ki) | ((kv.w == ki) & (j + 3 < i));
-    }
-    flag[i] = cnt < k ? 1 : 0;
-  }
+  // 2. top-k: segment i is selected iff fewer than k segments beat it (a greater exact key, or an equal
+  //    key and a lower index). The top-k of the estimates is the exact one when its certificate holds
+  //    (the enclosures separate at the k boundary); otherwise the keys are computed exactly.
+  if (!xk::certify_top_k<kSelectThreads>(elo, ehi, n, k, kh, kl, flag, s_cert))
+    exact_select<T, D>(a, u, qg, rows, stride, n, k, qh, ql, qtail, kh, kl, flag, &s_flags, s_red);
   __syncthreads();
 
   // 3. the selected list (ascending), the summary list (the rest, ascending), the maximal runs of
@@ -1263,8 +1208,8 @@ cudaError_t launch_pdl(Kern kernel, dim3 grid, dim3 block, size_t smem, cudaStre
 }
 
 template <typename T, int D>
-size_t select_smem_bytes(int n_max) {
-  return SelectLayout<T, D>::fixed_bytes(n_max) + (static_cast<size_t>(n_max) * 6 + 7) * 4;
+size_t select_smem_bytes(int G, int n_max) {
+  return SelectLayout<T, D>::bytes(G, n_max);
 }
 
 template <typename T, int D>
@@ -1325,13 +1270,12 @@ zr_status configure_for(Plan& p, int64_t useful_warps) {
   if constexpr (sizeof(T) == 2)
     cudaFuncSetAttribute(zr_attend_mma_kernel<D>, cudaFuncAttributePreferredSharedMemoryCarveout, carve);
   cudaGetLastError();
-  p.select_smem = select_smem_bytes<T, D>(p.n_max);
-  if (p.select_smem > 48 * 1024) {
-    if (cudaFuncSetAttribute(zr_select_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(p.select_smem)) != cudaSuccess) {
-      cudaGetLastError();
-      return ZR_ECUDA;
-    }
+  // Set for every plan: the kernel's static shared memory counts against the 48 KB default too.
+  p.select_smem = select_smem_bytes<T, D>(p.G, p.n_max);
+  if (cudaFuncSetAttribute(zr_select_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(p.select_smem)) != cudaSuccess) {
+    cudaGetLastError();
+    return ZR_ECUDA;
   }
   return ZR_OK;
 }

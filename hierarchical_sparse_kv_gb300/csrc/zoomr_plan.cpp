@@ -121,6 +121,7 @@ void layout_workspace(zr::Plan& p) {
   p.ws.sel = take(U * p.k_max * sizeof(int32_t));
   p.ws.part_o = take(slots * p.G * p.d * sizeof(float));
   p.ws.part_ml = take(slots * p.G * 2 * sizeof(float));
+  p.ws.bigkeys = take(U * p.n_max * 20 * sizeof(uint32_t));
   const bool cons = p.mode == zr::kConsensusPlan;
   p.ws.votes = cons ? take(static_cast<size_t>(p.B) * p.n_max * sizeof(int32_t)) : 0;
   p.ws.cruns = cons ? take(static_cast<size_t>(p.B) * (p.n_max + 1) * 2 * sizeof(int32_t)) : 0;
@@ -308,6 +309,7 @@ StepArgs step_args(const Plan& p, void* workspace) {
   a.sel = reinterpret_cast<int32_t*>(ws + p.ws.sel);
   a.part_o = reinterpret_cast<float*>(ws + p.ws.part_o);
   a.part_ml = reinterpret_cast<float2*>(ws + p.ws.part_ml);
+  a.bigkeys = reinterpret_cast<uint32_t*>(ws + p.ws.bigkeys);
   a.cruns = p.mode == kConsensusPlan ? reinterpret_cast<int32_t*>(ws + p.ws.cruns) : nullptr;
   a.cnruns = p.mode == kConsensusPlan ? reinterpret_cast<int32_t*>(ws + p.ws.cnruns) : nullptr;
   a.B = p.B;

@@ -7,10 +7,10 @@
  *   1. score    ZoomR page, 3.3 "Per-Head Importance Scoring and Voting", the
  *               equation alpha_i = q_t^T kbar_i: every segment's summary key is
  *               scored against the query. Per KV head the score is the maximum
- *               over the group's query heads. The ranking key is the fp32 dot
- *               product with each product and each partial sum rounded to
- *               nearest-even, summed in ascending component order (the 1/sqrt(d)
- *               scale does not change the ranking and is not applied to it).
+ *               over the group's query heads. The ranking key is the exact
+ *               real value of that dot product on the stored bf16/fp32 inputs
+ *               (no rounding enters the decision); the 1/sqrt(d) scale does not
+ *               change the ranking and is not applied to it.
  *   2. select   ZoomR 3.3, the equation I_top-k = argtop-k(alpha): the k_b
  *               segments with the largest keys; ties go to the lower segment
  *               index; k_b >= n_b selects every segment, k_b = 0 none.
@@ -33,8 +33,9 @@
  *   - zr_decode_attend is asynchronous on the caller's stream and allocates
  *     nothing. Indices that are found bad on the device (a physical block id
  *     outside [0, num_blocks)) set a sticky error word in the workspace; the
- *     offending row is skipped (no trap, no fault). zr_get_device_error reads
- *     and clears it.
+ *     offending row is skipped (no trap, no fault). A non-finite query or
+ *     summary-key value (unsupported) is ranked as zero and sets bit 3 (value 4)
+ *     of the same word. zr_get_device_error reads and clears it.
  *   - The plan is immutable after creation and may be reused for any number of
  *     layers and calls. Calls that may overlap on the GPU need separate
  *     workspaces.
@@ -196,9 +197,10 @@ ZR_API zr_status zr_decode_attend_static(zr_plan_t plan, const void* q, const vo
 
 /*
  * zr_get_device_error -- synchronize `stream`, then read and clear the sticky
- * device error word of `workspace` into *err_code (0 = none; bit 1 = a physical
- * block id outside the pool). Returns ZR_EDEVICE if the word was non-zero, ZR_OK
- * otherwise.
+ * device error word of `workspace` into *err_code (0 = none; bit 1 (value 1) = a
+ * physical block id outside the pool; bit 3 (value 4) = a non-finite query or
+ * summary-key value, ranked as zero). Returns ZR_EDEVICE if the word was non-zero,
+ * ZR_OK otherwise.
  */
 ZR_API zr_status zr_get_device_error(zr_plan_t plan, void* workspace, void* stream, int32_t* err_code);
 
@@ -313,9 +315,8 @@ ZR_API zr_status zr_consensus_dims(zr_plan_t plan, int32_t* c_max, int32_t* n_ma
  * zr_consensus_vote -- one layer's votes (ZoomR 3.3 "Per-Head Importance Scoring
  * and Voting"): for every query head h, alpha_i = q_h . kbar_i over the
  * sequence's n_b summaries, with kbar the mean summary key of S_i for the KV
- * head h / G; the top-k indices each get one vote. alpha is the fp32 dot with
- * each product and each partial sum rounded to nearest-even, components in
- * ascending order (no scale).
+ * head h / G; the top-k indices each get one vote. alpha is the exact dot
+ * product of the stored values (no scale), as in zr_decode_attend.
  *   q          [B, Hq, d] dtype (device)
  *   mean_keys  [seg_ptr[B], Hkv, d] dtype (device), pair rows in CSR order
  *              (zr_segment_summaries over the S_i spans computes them)

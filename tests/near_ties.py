@@ -17,7 +17,7 @@ to show that the two orders really disagree.
 from __future__ import annotations
 
 from fractions import Fraction
-from typing import List, Tuple
+from typing import List, Optional, Tuple
 
 import numpy as np
 import torch
@@ -53,12 +53,68 @@ def _rank_pair(keys: np.ndarray, k: int) -> Tuple[int, int]:
     return order[k - 1], order[k]
 
 
+def near_tie_row(q: np.ndarray, sk: np.ndarray, i: int, j: int, dtype: str) -> Optional[np.ndarray]:
+    """A nudged copy of summary key sk[i] to put in row j, or None if none is found.
+
+    q [G, d] holds the group's queries and sk [n, d] the unit's summary keys (exact stored values). With
+    the copy in row j, the exact keys of i and j differ, the exact order favours the higher index of the
+    two (where the tie rule would not), an ascending fp32 chain ranks them the other way, and no other
+    row's exact key lies between theirs.
+    """
+    n = sk.shape[0]
+    approx = (sk.astype(np.float64) @ q.astype(np.float64).T).max(axis=1)
+    hstar = int(np.argmax(sk[i].astype(np.float64) @ q.astype(np.float64).T))
+    ki = _exact(q, sk[i])
+    want_j_above = j > i
+    # one-ulp nudges of single components, and the change each makes to q_h* . s (exact in fp64)
+    nudges = []
+    for t in range(sk.shape[1]):
+        if sk[i, t] == 0:
+            continue
+        for up in (True, False):
+            x = _nudged(sk[i, t], up, dtype)
+            nudges.append((float(q[hstar, t]) * (float(x) - float(sk[i, t])), t, up))
+    # pairs of nudges on different components whose changes nearly cancel: smallest sum first
+    nudges.sort()
+    vals = np.array([v for v, _, _ in nudges])
+    pairs = []
+    for va, ta, ua in nudges:
+        m = int(np.searchsorted(vals, -va))
+        for c in (m - 1, m, m + 1):
+            if 0 <= c < len(nudges) and nudges[c][1] != ta and va + nudges[c][0] != 0:
+                pairs.append((abs(va + nudges[c][0]), (ta, ua), (nudges[c][1], nudges[c][2])))
+    pairs.sort()
+    for _, (t1, u1), (t2, u2) in pairs[:64]:
+        row = sk[i].copy()
+        row[t1] = _nudged(row[t1], u1, dtype)
+        row[t2] = _nudged(row[t2], u2, dtype)
+        kj = _exact(q, row)
+        if kj == ki or (kj > ki) != want_j_above:
+            continue
+        trial = sk.copy()
+        trial[j] = row
+        f32 = fp32_chain_keys(q, trial)
+        f32_j_above = f32[j] > f32[i] or (f32[j] == f32[i] and j < i)
+        if f32_j_above == want_j_above:
+            continue  # the fp32 chain kept the difference: not a disagreement
+        lo, hi = min(ki, kj), max(ki, kj)
+        others = [m for m in range(n) if m not in (i, j) and abs(approx[m] - float(ki)) < 1e-3]
+        if any(lo <= _exact(q, sk[m]) <= hi for m in others):
+            continue
+        return row
+    return None
+
+
+def boundary_pair(q: np.ndarray, sk: np.ndarray, k: int) -> Tuple[int, int]:
+    """The k-th and (k+1)-th rows in (key desc, index asc), keys estimated in fp64."""
+    return _rank_pair((sk.astype(np.float64) @ q.astype(np.float64).T).max(axis=1), k)
+
+
 def plant_near_ties(st: W.Structure, lt: W.LayerTensors, max_units: int = 64) -> List[Tuple[int, int, int, int]]:
     """Plant a near-tie into up to ``max_units`` units of ``lt`` (in place, on its device).
 
-    Returns (b, g, i, j) for every planted unit: segment j now holds a nudged copy
-    of segment i's summary key, the exact order of i and j differs from the fp32
-    chain's order, and no other segment's key lies between theirs.
+    Returns (b, g, i, j) for every planted unit: segment j now holds the row ``near_tie_row`` built
+    from segment i's summary key, i and j being the unit's k-th and (k+1)-th segments.
     """
     spec = st.spec
     G = spec.num_q_heads // spec.num_kv_heads
@@ -74,50 +130,11 @@ def plant_near_ties(st: W.Structure, lt: W.LayerTensors, max_units: int = 64) ->
             if len(planted) >= max_units:
                 break
             q = q_all[b, g * G:(g + 1) * G]
-            sk = sk_all[s0:s0 + n, g].copy()
-            approx = (sk.astype(np.float64) @ q.astype(np.float64).T).max(axis=1)
-            i, j = _rank_pair(approx, k)
-            hstar = int(np.argmax(sk[i].astype(np.float64) @ q.astype(np.float64).T))
-            ki = _exact(q, sk[i])
-            want_j_above = j > i  # the exact order must favour the higher index, where the tie rule would not
-            # one-ulp nudges of single components, and the change each makes to q_h* . s (exact in fp64)
-            nudges = []
-            for t in range(sk.shape[1]):
-                if sk[i, t] == 0:
-                    continue
-                for up in (True, False):
-                    x = _nudged(sk[i, t], up, spec.dtype)
-                    nudges.append((float(q[hstar, t]) * (float(x) - float(sk[i, t])), t, up))
-            # pairs of nudges on different components whose changes nearly cancel: smallest sum first
-            nudges.sort()
-            vals = np.array([v for v, _, _ in nudges])
-            pairs = []
-            for va, ta, ua in nudges:
-                m = int(np.searchsorted(vals, -va))
-                for c in (m - 1, m, m + 1):
-                    if 0 <= c < len(nudges) and nudges[c][1] != ta and va + nudges[c][0] != 0:
-                        pairs.append((abs(va + nudges[c][0]), (ta, ua), (nudges[c][1], nudges[c][2])))
-            pairs.sort()
-            for _, (t1, u1), (t2, u2) in pairs[:64]:
-                row = sk[i].copy()
-                row[t1] = _nudged(row[t1], u1, spec.dtype)
-                row[t2] = _nudged(row[t2], u2, spec.dtype)
-                kj = _exact(q, row)
-                if kj == ki or (kj > ki) != want_j_above:
-                    continue
-                trial = sk.copy()
-                trial[j] = row
-                f32 = fp32_chain_keys(q, trial)
-                f32_j_above = f32[j] > f32[i] or (f32[j] == f32[i] and j < i)
-                if f32_j_above == want_j_above:
-                    continue  # the fp32 chain kept the difference: not a disagreement
-                # no third key between the two (exact, against the float estimate's neighbours)
-                lo, hi = min(ki, kj), max(ki, kj)
-                others = [m for m in range(n) if m not in (i, j) and abs(approx[m] - float(ki)) < 1e-3]
-                if any(lo <= _exact(q, sk[m]) <= hi for m in others):
-                    continue
-                sk[j] = row
-                lt.sum_k[s0 + j, g] = torch.from_numpy(row).to(lt.sum_k.dtype).to(lt.sum_k.device)
-                planted.append((b, g, i, j))
-                break
+            sk = sk_all[s0:s0 + n, g]
+            i, j = boundary_pair(q, sk, k)
+            row = near_tie_row(q, sk, i, j, spec.dtype)
+            if row is None:
+                continue
+            lt.sum_k[s0 + j, g] = torch.from_numpy(row).to(lt.sum_k.dtype).to(lt.sum_k.device)
+            planted.append((b, g, i, j))
     return planted

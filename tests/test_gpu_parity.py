@@ -224,17 +224,17 @@ def test_out_of_pool_block_id_sets_the_error_word_and_nothing_faults():
     C.parity(st, lt, plan=plan)
 
 
-def test_key_chain_rounding_order_decides_the_selection():
-    """The ranking key is an fp32 sum in ascending element order, rounded after every add. Summary
-    keys built so that another order (or a fused multiply-add) gives a different key, and the
-    top-2 a different set: 2^24 + 1 - 2^24 is 0 in order (1 otherwise). Two KV heads, each with
-    one query head of its group carrying the signal, once in each half of a packed pair."""
+def test_exact_key_decides_where_an_fp32_chain_cancels():
+    """The ranking key is the exact dot product. Summary keys built so that an fp32 chain in
+    ascending order gives different keys and a different top-2: 2^24 + 1 - 2^24 is 1 exactly (0 in
+    that chain). Two KV heads, each with one query head of its group carrying the signal, once in
+    each half of a packed pair."""
     spec = W.small_spec(dtype="bf16", head_dim=128, batch=1, num_q_heads=8, num_kv_heads=2, seq_len=64,
                         seg_len_range=(16, 16), topk=2, window=0, seed=7)
     st, lt = _layer(spec)
     assert int(st.seg_ptr[1]) == 4
     big = float(2 ** 24)
-    rows = [[big, 1.0, -big], [0.5], [1.0, 1.0, -big, big], [-1.0]]  # keys 0, 0.5, 2, -1 in order
+    rows = [[big, 1.0, -big], [0.5], [1.0, 1.0, -big, big], [-1.0]]  # exact keys 1, 0.5, 2, 0 (max with 0)
     sk = torch.zeros_like(lt.sum_k)
     for i, r in enumerate(rows):
         sk[i, :, :len(r)] = torch.tensor(r, dtype=torch.float32).to(sk.dtype)
@@ -244,5 +244,5 @@ def test_key_chain_rounding_order_decides_the_selection():
     lt = dataclasses.replace(lt, sum_k=sk, q=q)
     r = C.parity(st, lt)
     for g in range(2):
-        assert list(r["sel"][0, g, :2]) == [1, 2]
-        assert list(r["oracle"].units[0][g].sel) == [1, 2]
+        assert list(r["sel"][0, g, :2]) == [0, 2]
+        assert list(r["oracle"].units[0][g].sel) == [0, 2]
