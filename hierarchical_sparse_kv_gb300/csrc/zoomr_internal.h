@@ -109,6 +109,11 @@ struct StepArgs {
 // Implemented in zoomr_plan.cpp: the launch arguments that point into `workspace` (plus the plan's sizes).
 StepArgs step_args(const Plan& p, void* workspace);
 
+// Implemented in zoomr_plan.cpp: the checks of a decode call's tensor arguments (null, alignment, plan
+// kind); ZR_OK or ZR_EINVAL, nothing launched.
+zr_status check_decode_args(zr_plan_t plan, const void* q, const void* k_pool, const void* v_pool,
+                            const int32_t* block_tables, const void* sum_k, const void* sum_v, const float* out);
+
 // Implemented in zoomr_plan.cpp: argument checks, then one decode step on `workspace`.
 zr_status decode_into(zr_plan_t plan, void* workspace, const void* q, const void* k_pool, const void* v_pool,
                       const int32_t* block_tables, const void* sum_k, const void* sum_v, float* out,

@@ -273,15 +273,23 @@ zr_status zr_plan_dims(zr_plan_t plan, int32_t* k_max, int32_t* n_max) {
 
 namespace zr {
 
+zr_status check_decode_args(zr_plan_t plan, const void* q, const void* k_pool, const void* v_pool,
+                             const int32_t* block_tables, const void* sum_k, const void* sum_v, const float* out) {
+  if (!plan || !q || !k_pool || !v_pool || !block_tables || !sum_k || !sum_v || !out) return ZR_EINVAL;
+  if (plan->p.mode != kDecodePlan) return ZR_EINVAL;
+  if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(sum_k, 16) ||
+      !aligned(sum_v, 16) || !aligned(out, 16) || !aligned(block_tables, 4))
+    return ZR_EINVAL;
+  return ZR_OK;
+}
+
 zr_status decode_into(zr_plan_t plan, void* workspace, const void* q, const void* k_pool, const void* v_pool,
                                const int32_t* block_tables, const void* sum_k, const void* sum_v, float* out,
                                int32_t* sel_out, int32_t* ranges_out, int32_t* nranges_out, void* stream,
                                void* ev_start, void* ev_stop) {
-  if (!plan || !workspace || !q || !k_pool || !v_pool || !block_tables || !sum_k || !sum_v || !out) return ZR_EINVAL;
-  if (plan->p.mode != kDecodePlan) return ZR_EINVAL;
-  if (!aligned(workspace, 256) || !aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) ||
-      !aligned(sum_k, 16) || !aligned(sum_v, 16) || !aligned(out, 16) || !aligned(block_tables, 4))
-    return ZR_EINVAL;
+  const zr_status st = check_decode_args(plan, q, k_pool, v_pool, block_tables, sum_k, sum_v, out);
+  if (st != ZR_OK) return st;
+  if (!workspace || !aligned(workspace, 256)) return ZR_EINVAL;
   zr::StepArgs a = step_args(plan->p, workspace);
   a.q = q;
   a.k_pool = k_pool;

@@ -13,7 +13,9 @@
 // which loads this library holds until the process exits. Host code never uses
 // the array's name as an address (in host code it is only a stand-in): the
 // device address is fetched with cudaGetSymbolAddress once per device, the
-// first time the entry point runs on that device, with that device current.
+// first time the entry point runs on that device, with that device current, and
+// kept for the life of the process. A device reset (cudaDeviceReset) reloads the
+// module at another address, so the entry point must not be used across one.
 
 #include <cuda_runtime.h>
 
@@ -59,11 +61,20 @@ extern "C" {
 zr_status zr_decode_attend_static(zr_plan_t plan, const void* q, const void* k_pool, const void* v_pool,
                                   const int32_t* block_tables, const void* sum_k, const void* sum_v, float* out,
                                   void* stream) {
-  if (!plan) return ZR_EINVAL;
-  if (plan->p.mode != zr::kDecodePlan) return ZR_EINVAL;
+  // Every check comes before the first enqueued operation: an error return leaves the stream untouched.
+  zr_status st = zr::check_decode_args(plan, q, k_pool, v_pool, block_tables, sum_k, sum_v, out);
+  if (st != ZR_OK) return st;
   if (plan->p.ws.total > kStaticScratchBytes) return ZR_EUNSUPPORTED;
+  // The plan's metadata, kernel attributes and grid size belong to its device: that device must be current
+  // (the scratch is looked up on the current device).
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return ZR_ECUDA;
+  }
+  if (dev != plan->p.device) return ZR_EINVAL;
   void* ws = nullptr;
-  zr_status st = scratch_on_current_device(&ws);
+  st = scratch_on_current_device(&ws);
   if (st != ZR_OK) return st;
   // The array keeps the previous call's contents; only the error word must start at zero.
   if (cudaMemsetAsync(static_cast<char*>(ws) + plan->p.ws.err, 0, sizeof(int32_t),

@@ -188,7 +188,11 @@ ZR_API zr_status zr_decode_attend_timed(zr_plan_t plan, void* workspace, const v
  *     them on one stream.
  *   - Out-of-pool block ids are masked as in zr_decode_attend, but not
  *     reported: the error word is cleared at the start of every call.
- * Errors: ZR_EINVAL (null plan or required pointer, misaligned pointer),
+ *   - The plan's device must be the current device (ZR_EINVAL otherwise).
+ *   - The device address of the array is kept for the life of the process:
+ *     do not use this entry point across a cudaDeviceReset.
+ * Errors (all returned before anything is enqueued on the stream): ZR_EINVAL
+ * (null plan or required pointer, misaligned pointer, another device current),
  * ZR_EUNSUPPORTED (workspace over 16 MiB), ZR_ECUDA.
  */
 ZR_API zr_status zr_decode_attend_static(zr_plan_t plan, const void* q, const void* k_pool, const void* v_pool,

@@ -1,7 +1,7 @@
 """Run one layer of a workload through the C ABI a few times (for profilers).
 
-  python -m hierarchical_sparse_kv_gb300.profile_case --workload 2 --layer 0 --reps 4
-  python -m hierarchical_sparse_kv_gb300.profile_case --path summaries --segments 8 --reps 3
+  python profile_case.py --workload 2 --layer 0 --reps 4
+  python profile_case.py --path summaries --segments 8 --reps 3
 
 Draws the workload's structure and one layer on cuda:0. The decode path plans
 the layer and runs the decode step ``--reps`` times; the summaries path runs

@@ -4,9 +4,12 @@ It serves callers that cannot allocate device memory: code handed only its
 input and output buffers by a host engine that owns all device allocations, or
 a loop that must not call cudaMalloc because it can synchronize the device. The
 test checks, through the C ABI, that two calls in a row give the same outputs as
-zr_decode_attend with a caller workspace, and that a plan too large for the
-16 MiB static scratch is refused before anything runs. This file is collected
-last on purpose.
+zr_decode_attend with a caller workspace; that an out-of-pool block id is masked
+the same way on both paths and that the next clean static call is unaffected
+(the error word starts at zero on every call); that a plan too large for the
+16 MiB static scratch is refused before anything runs; and, with two GPUs, that
+a call with another device current is refused. This file is collected last on
+purpose.
 """
 
 from __future__ import annotations
@@ -65,4 +68,44 @@ def test_plan_over_the_static_limit_is_refused():
     with pytest.raises(Z.ZoomrError) as e:
         Z.zr_decode_attend_static(plan.handle, small, small, small, bt, small, small, out)
     assert e.value.status == Z.ZR_EUNSUPPORTED
+    plan.close()
+
+
+def test_masked_bad_block_then_a_clean_call():
+    spec = W.small_spec(dtype="bf16", head_dim=128, batch=2, num_q_heads=8, num_kv_heads=2, seq_len=200,
+                        seg_len_range=(10, 30), topk=10_000, window=5, seed=3)
+    st = W.make_structure(spec)
+    lt = W.make_layer(st, 0, "cuda")
+    plan = Z.DecodePlan.from_structure(st)
+    good = torch.from_numpy(st.block_tables.astype(np.int32)).cuda()
+    bad_np = st.block_tables.copy()
+    bad_np[1, 3] = st.num_blocks + 1000  # outside the pool: masked on both paths
+    bad = torch.from_numpy(bad_np.astype(np.int32)).cuda()
+    outs = {}
+    for name, bt in (("bad", bad), ("good", good)):
+        ref = torch.full(lt.q.shape, float("nan"), dtype=torch.float32, device="cuda")
+        Z.zr_decode_attend(plan.handle, plan.ws, lt.q, lt.k_pool, lt.v_pool, bt, lt.sum_k, lt.sum_v, ref)
+        torch.cuda.synchronize()
+        assert plan.device_error() == (1 if name == "bad" else 0)
+        outs[name] = ref
+    for name in ("bad", "good"):  # the masked call, then a clean one on the same static scratch
+        out = torch.full(lt.q.shape, float("nan"), dtype=torch.float32, device="cuda")
+        Z.zr_decode_attend_static(plan.handle, lt.q, lt.k_pool, lt.v_pool, bad if name == "bad" else good,
+                                  lt.sum_k, lt.sum_v, out)
+        torch.cuda.synchronize()
+        assert torch.equal(out, outs[name]), name
+    plan.close()
+
+
+@pytest.mark.skipif(torch.cuda.device_count() < 2, reason="needs two GPUs")
+def test_another_device_current_is_refused():
+    st = W.make_structure(W.WORKLOADS[0])
+    lt = W.make_layer(st, 0, "cuda:0")
+    plan = Z.DecodePlan.from_structure(st, device="cuda:0")
+    bt = torch.from_numpy(st.block_tables.astype(np.int32)).cuda(0)
+    out = torch.zeros(lt.q.shape, dtype=torch.float32, device="cuda:0")
+    with torch.cuda.device(1):
+        with pytest.raises(Z.ZoomrError) as e:
+            Z.zr_decode_attend_static(plan.handle, lt.q, lt.k_pool, lt.v_pool, bt, lt.sum_k, lt.sum_v, out)
+    assert e.value.status == Z.ZR_EINVAL
     plan.close()
