@@ -207,6 +207,35 @@ def cpu_baseline(workload: int, budget_s: float) -> dict:
                       f"a step is {units_per_step} units"}
 
 
+def cpu_baseline_accounting(st, lts, G: int, eb: int):
+    """Part of the CPU-baseline leg: the oracle's selection steps (summary_keys, select_top_k,
+    gather_set) on host copies of the very queries and summary keys the GPU reads, for every unit of
+    every layer, outside any timed region. Returns (algorithmic attend bytes per layer, tokens gathered
+    per step, {(layer, b, g): token ranges}) for the byte accounting of the roofline."""
+    from oracle import zoomr_oracle as O
+
+    spec = st.spec
+    per_layer, tok_total, ranges = [], 0, {}
+    for l, lt in enumerate(lts):
+        q = W.to_numpy32(lt.q)
+        sk = W.to_numpy32(lt.sum_k)
+        tot = 0
+        for b in range(st.batch):
+            s0, n = int(st.seg_ptr[b]), st.num_segments(b)
+            bounds = np.asarray(st.bounds(b))
+            L_b = int(st.seq_lens[b])
+            for g in range(spec.num_kv_heads):
+                keys = O.summary_keys(q[b, g * G:(g + 1) * G], sk[s0:s0 + n, g])
+                sel = O.select_top_k(keys, int(st.topk[b]))
+                tokens, summaries = O.gather_set(bounds, sel, L_b, st.window)
+                tok_total += len(tokens)
+                ranges[(l, b, g)] = O.token_ranges(tokens)
+                tot += A.attend_bytes_per_unit(len(tokens), len(summaries), A.distinct_blocks(tokens), G,
+                                               spec.head_dim, eb)
+        per_layer.append(tot)
+    return per_layer, tok_total, ranges
+
+
 # ---------------------------------------------------------------------- distributed
 def dist_setup(n_gpus):
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -310,9 +339,11 @@ def run_zoomr(args):
     outs = [out_all[l] for l in range(len(lts))]
     G = spec.num_q_heads // spec.num_kv_heads
 
-    # Algorithmic bytes of each layer's attend launch (from that layer's selection).
+    # Algorithmic bytes of each layer's attend launch. The CPU-baseline leg runs the oracle's selection
+    # steps on the very inputs the GPU reads; the kernel's own ranges (debug outputs) must agree with it
+    # on every unit, and give the count only when that leg is skipped.
     dbg = plan.new_debug_outputs()
-    attend_bytes, select_bytes, tok_total = [], 0, 0
+    kern_bytes, select_bytes, kern_tok, kern_ranges = [], 0, 0, {}
     eb = 2 if spec.dtype == "bf16" else 4  # element bytes of q, K/V and summaries
     for l, lt in enumerate(lts):
         plan.run(lt.q, lt.k_pool, lt.v_pool, bt, lt.sum_k, lt.sum_v, outs[l], dbg)
@@ -323,71 +354,87 @@ def run_zoomr(args):
             k_b = min(int(st.topk[b]), n_b)
             for g in range(spec.num_kv_heads):
                 r = rng[b, g, :nr[b, g]]
+                kern_ranges[(l, b, g)] = r
                 ntok = A.ranges_token_count(r)
-                tok_total += ntok
+                kern_tok += ntok
                 tot += A.attend_bytes_per_unit(ntok, n_b - k_b, A.ranges_block_count(r), G, spec.head_dim, eb)
                 select_bytes += A.select_bytes_per_unit(n_b, G, spec.head_dim, eb)
-        attend_bytes.append(tot)
+        kern_bytes.append(tot)
     torch.cuda.synchronize()
     assert plan.device_error() == 0
+    if cpu_line is not None and not args.no_oracle_accounting:
+        t_acc = time.perf_counter()
+        attend_bytes, tok_total, oracle_ranges = cpu_baseline_accounting(st, lts, G, eb)
+        agree = all(np.array_equal(kern_ranges[key], oracle_ranges[key]) for key in oracle_ranges)
+        acct = {"source": "the oracle's selection steps (summary_keys, select_top_k, gather_set) on the GPU's "
+                          "inputs, in the CPU-baseline leg", "units": len(oracle_ranges),
+                "kernel_ranges_agree": agree, "seconds": round(time.perf_counter() - t_acc, 1)}
+    else:
+        attend_bytes, tok_total = kern_bytes, kern_tok
+        acct = {"source": "the kernel's own token ranges (the CPU-baseline leg was skipped)"}
     out_bytes = L * st.batch * spec.num_q_heads * spec.head_dim * 4
     step_bytes = sum(attend_bytes) + select_bytes + out_bytes
 
     stream = torch.cuda.Stream(device=dev)
-    # Every captured step times one layer's attend launch with a pair of events (the layer rotates
-    # over the captures, so all layers are timed within the timed region); the other launches keep
-    # their programmatic-dependent-launch overlap, which an event node between kernels would break.
-    n_graphs = max(1, min(args.steps, args.max_graphs))
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_graphs)]
-    # Captured step i times layer i mod L in one of three ways (mode i mod 3): 0 the attend launch
-    # alone (an event pair around it, which also breaks its overlap with the select kernel); 1 the
-    # select and attend launches together and 2 the select launch alone, both from an event of our
-    # own before the call, so 1 - 2 is what the attend kernel adds to the step with its launch
-    # overlap intact. Modes 1 and 2 need events that a capture records as graph nodes.
-    try:
-        pev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(n_graphs)]
-    except TypeError:
-        pev = None
-    modes = [i % 3 if pev is not None else 0 for i in range(n_graphs)]
 
-    def step(i, s):
+    def step(s, pair=None, sel_att=None, sel_only=None):
+        """One decode step over all layers. pair[l]: events around layer l's attend launch; sel_att[l]:
+        an event before layer l's call and one after its attend launch; sel_only[l]: an event before the
+        call and one after its select launch (the events of a capture become graph nodes)."""
         for l, lt in enumerate(lts):
-            if i is not None and l == i % L:
-                m = modes[i]
-                if m > 0:
-                    pev[i].record(s)
-                plan.run_timed(lt.q, lt.k_pool, lt.v_pool, bt, lt.sum_k, lt.sum_v, outs[l],
-                               evs[i][0] if m != 1 else None, evs[i][1] if m != 2 else None, stream=s)
+            if pair is not None:
+                plan.run_timed(lt.q, lt.k_pool, lt.v_pool, bt, lt.sum_k, lt.sum_v, outs[l], pair[l][0], pair[l][1],
+                               stream=s)
+            elif sel_att is not None:
+                sel_att[l][0].record(s)
+                plan.run_timed(lt.q, lt.k_pool, lt.v_pool, bt, lt.sum_k, lt.sum_v, outs[l], None, sel_att[l][1],
+                               stream=s)
+            elif sel_only is not None:
+                sel_only[l][0].record(s)
+                plan.run_timed(lt.q, lt.k_pool, lt.v_pool, bt, lt.sum_k, lt.sum_v, outs[l], sel_only[l][1], None,
+                               stream=s)
             else:
                 plan.run(lt.q, lt.k_pool, lt.v_pool, bt, lt.sum_k, lt.sum_v, outs[l], stream=s)
 
-    for a_, b_ in evs:  # torch creates CUDA events lazily: create them all before any capture
-        a_.record(stream)
-        b_.record(stream)
-    for e_ in pev or []:
-        e_.record(stream)
+    # Events for the measurement steps: plain pairs around each attend launch, and pairs whose first event
+    # precedes the call (recorded by us, so inside a capture it must be an "external" event node).
+    try:
+        ext = lambda: torch.cuda.Event(enable_timing=True, external=True)
+        ext()
+    except TypeError:
+        ext = None
+    mk = lambda: torch.cuda.Event(enable_timing=True)
+    pair = [(mk(), mk()) for _ in range(L)]
+    sel_att = [(ext(), mk()) for _ in range(L)] if ext else None
+    sel_only = [(ext(), mk()) for _ in range(L)] if ext else None
+    for e_ in [e for p_ in pair + (sel_att or []) + (sel_only or []) for e in p_]:
+        e_.record(stream)  # torch creates CUDA events lazily: create them all before any capture
     stream.wait_stream(torch.cuda.current_stream())
-    graphs = []
+    graphs = {}
     with torch.cuda.stream(stream):
-        step(0, stream)  # eager warm-up on the capture stream
+        step(stream)  # eager warm-up on the capture stream
         if not args.no_graph:
-            for i in range(n_graphs):
+            for name, kw in (("step", {}), ("pair", {"pair": pair}), ("sel_att", {"sel_att": sel_att}),
+                             ("sel_only", {"sel_only": sel_only})):
+                if name != "step" and not next(iter(kw.values())):
+                    continue
                 g = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(g, stream=stream):
-                    step(i, stream)
-                graphs.append(g)
+                    step(stream, **kw)
+                graphs[name] = g
     torch.cuda.current_stream().wait_stream(stream)
     torch.cuda.synchronize()
 
-    def replay(i):
+    def replay(name="step"):
         with torch.cuda.stream(stream):
             if graphs:
-                graphs[i % n_graphs].replay()
+                graphs[name].replay()
             else:
-                step(i % n_graphs, stream)
+                step(stream, **({"pair": pair} if name == "pair" else {"sel_att": sel_att} if name == "sel_att" else
+                                {"sel_only": sel_only} if name == "sel_only" else {}))
 
     for i in range(args.warmup):
-        replay(i)
+        replay()
     torch.cuda.synchronize()
     barrier(world)
     clocks = ClockSampler(dev.index) if rank == 0 else None
@@ -397,26 +444,43 @@ def run_zoomr(args):
     barrier(world)
     t_start.record(stream)
     for i in range(args.steps):
-        replay(i)
+        replay()
     t_stop.record(stream)
     torch.cuda.synchronize()
     barrier(world)
     clk = clocks.stop() if clocks else None
     ms = t_start.elapsed_time(t_stop) / args.steps
     ms = max_over_ranks(ms, world)
-    # attend kernel: the timed layer of each capture (its last replay in the timed region)
-    timed = [i for i in range(min(n_graphs, args.steps)) if modes[i] == 0]
-    # medians over the timed captures (the event pair: bytes over time per launch, median over launches)
-    attend_ms = statistics.median(evs[i][0].elapsed_time(evs[i][1]) for i in timed)
-    attend_bytes_avg = sum(attend_bytes[i % L] for i in timed) / len(timed)
+
+    # The attend kernel's duration, after the timed region: an event pair around every layer's attend
+    # launch, over `meas_reps` replays of a step (L launches each). Each pair breaks the launch's
+    # programmatic overlap with the select kernel and adds the event nodes' latency (an empty kernel
+    # between two event nodes measures about 4.4 us), so this direct figure is conservative. Beside it,
+    # the kernel's time with the overlap intact: median(select + attend) - median(select), each from an
+    # event before the call.
+    meas_reps = max(1, -(-args.attend_samples // L))
+    pair_ms, pair_bytes, sa, so = [], [], [], []
+    for _ in range(meas_reps):
+        replay("pair")
+        torch.cuda.synchronize()
+        pair_ms += [pair[l][0].elapsed_time(pair[l][1]) for l in range(L)]
+        pair_bytes += attend_bytes
+        if sel_att is not None:
+            replay("sel_att")
+            torch.cuda.synchronize()
+            sa += [sel_att[l][0].elapsed_time(sel_att[l][1]) for l in range(L)]
+            replay("sel_only")
+            torch.cuda.synchronize()
+            so += [sel_only[l][0].elapsed_time(sel_only[l][1]) for l in range(L)]
+    attend_ms = sum(pair_ms) / len(pair_ms)  # mean over the sampled launches
+    attend_bytes_avg = sum(pair_bytes) / len(pair_bytes)
     in_step = None
-    sa = [pev[i].elapsed_time(evs[i][1]) for i in range(min(n_graphs, args.steps)) if modes[i] == 1]
-    so = [pev[i].elapsed_time(evs[i][0]) for i in range(min(n_graphs, args.steps)) if modes[i] == 2]
     if sa and so:
         in_step_ms = statistics.median(sa) - statistics.median(so)
         mean_bytes = sum(attend_bytes) / L
         in_step = {"attend_us": in_step_ms * 1e3, "achieved": mean_bytes / (in_step_ms * 1e-3) / 1e9,
-                   "select_us": statistics.median(so) * 1e3, "select_attend_us": statistics.median(sa) * 1e3}
+                   "select_us": statistics.median(so) * 1e3, "select_attend_us": statistics.median(sa) * 1e3,
+                   "samples": len(sa)}
 
     # e2e through the public API with host buffers: one H2D of all layers' queries from pinned
     # memory, the step, one D2H of all layers' outputs into pinned memory.
@@ -428,7 +492,7 @@ def run_zoomr(args):
     with torch.cuda.stream(stream):
         for _ in range(2):
             q_all.copy_(host_q, non_blocking=True)
-            step(None, stream)
+            step(stream)
             host_out.copy_(out_all, non_blocking=True)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -436,7 +500,7 @@ def run_zoomr(args):
         e0.record(stream)
         for _ in range(e2e_steps):
             q_all.copy_(host_q, non_blocking=True)
-            step(None, stream)
+            step(stream)
             host_out.copy_(out_all, non_blocking=True)
         e1.record(stream)
     torch.cuda.synchronize()
@@ -460,34 +524,24 @@ def run_zoomr(args):
         "hbm_gbs": step_bytes / (ms * 1e-3) / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_kind": f"{peak_kind} copy bandwidth", "traffic": traffic,
-                     "kernel": kernel, "attend_us": attend_ms * 1e3,
-                     "alg_bytes_per_launch": attend_bytes_avg,
-                     "timing": "event pair around single attend launches (includes their launch latency)"},
+                     "kernel": kernel, "attend_us": attend_ms * 1e3, "samples": len(pair_ms),
+                     "alg_bytes_per_launch": attend_bytes_avg, "alg_bytes": acct,
+                     "timing": f"mean over {len(pair_ms)} attend launches ({meas_reps} replays of the step after "
+                               "the timed region, every layer), each between two CUDA events on the launching "
+                               "stream; the pair breaks the launch's overlap with the select kernel and includes "
+                               "the event nodes' latency"},
         "e2e": {"value": world * 1e3 / e2e_ms, "unit": "steps/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": 3 * L * args.steps,
         "attend_in_step": None if in_step is None else dict(
             in_step, frac=in_step["achieved"] / peak,
-            method="median(select+attend) - median(select), events before the call and after attend or select, "
-                   "launch overlap between the two kernels intact"),
-        "timing": "CUDA events on the launching stream around the graph replays; the attend kernel is timed with "
-                  "an event pair around one layer per captured step, rotating over the layers",
+            method="median(select+attend) - median(select) over the sampled layers, events before the call and "
+                   "after attend or select, launch overlap between the two kernels intact"),
+        "timing": "CUDA events on the launching stream around the replays of a captured step (no event nodes "
+                  "inside it)",
         "clocks": clk,
         "tokens_gathered_per_step": tok_total,
     }
-    if in_step is not None and not offload:
-        # The kernel's duration in the step: (select + attend) - select, both timed with events on the
-        # launching stream with the programmatic overlap intact. The event pair around a single launch
-        # breaks that overlap and adds the event nodes' own latency (about 4.4 us for an empty kernel);
-        # it stays beside it as the conservative figure. ncu's per-launch duration of the same step
-        # (launch list, serialised) agrees with the in-step figure.
-        raw = {k: line["roofline"][k] for k in ("achieved", "frac", "attend_us", "alg_bytes_per_launch", "timing")}
-        line["roofline"].update({"achieved": in_step["achieved"], "frac": in_step["achieved"] / peak,
-                                 "attend_us": in_step["attend_us"], "alg_bytes_per_launch": sum(attend_bytes) / L,
-                                 "timing": "attend kernel's time in the captured step: median(select + attend) - "
-                                           "median(select) over the timed replays, CUDA events on the launching stream, "
-                                           "launch overlap intact",
-                                 "event_pair": raw})
     if offload:
         line["path"] = "offload"
         line["roofline"].update({"bound": "link", "peak": link_gbs, "frac": achieved / link_gbs,
@@ -1107,6 +1161,10 @@ def main(argv=None):
     ap.add_argument("--no-graph", action="store_true", help="launch eagerly instead of replaying CUDA graphs")
     ap.add_argument("--max-graphs", type=int, default=64, help="distinct captured steps (each with its own events)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-oracle-accounting", action="store_true",
+                    help="count algorithmic bytes from the kernel's own ranges instead of the oracle's selection")
+    ap.add_argument("--attend-samples", type=int, default=128,
+                    help="attend launches timed with an event pair after the timed region")
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle work for cpu_baseline, once on one core and once on all cores")
     ap.add_argument("--ref-units", type=int, default=16, help="oracle units per reference-arm step")
