@@ -11,7 +11,7 @@ steps.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl zoomr|reference]
   python bench.py --path append      # the cache-update path: token appends and segment summaries
   python bench.py --path consensus   # ZoomR's consensus selection and attention over its final set
-  python bench.py --path offload     # the decode step with the K/V pools in pinned host memory
+  python bench.py --path offload     # the consensus decode with the cache in pinned host memory, staged per layer
   python bench.py --path generate    # the consensus path as a decode loop (appends, advance, periodic selection)
 
 Prints one JSON line (rank 0). Under torchrun each rank runs its own replica of
@@ -318,16 +318,6 @@ def run_zoomr(args):
     dev = torch.device("cuda", torch.cuda.current_device())
     spec, st, lts = make_inputs(dev, args.workload)
     L = len(lts)
-    offload = args.path == "offload"
-    link_gbs = None
-    if offload:
-        # the pages' offloaded cache: every layer's K/V pools in pinned host memory, read by the kernels
-        # across the CPU-GPU link; only queries, summaries, block tables and scratch stay in HBM
-        for lt in lts:
-            lt.k_pool = lt.k_pool.cpu().pin_memory()
-            lt.v_pool = lt.v_pool.cpu().pin_memory()
-        torch.cuda.empty_cache()
-        link_gbs = measure_link_gbs(dev)
     plan = Z.DecodePlan.from_structure(st, device=dev)
     bt = torch.from_numpy(st.block_tables.astype(np.int32)).to(dev)
     # every layer's queries and outputs are slices of one buffer each, so the end-to-end leg moves a
@@ -508,14 +498,14 @@ def run_zoomr(args):
 
     peak, peak_kind = read_peak()
     achieved = attend_bytes_avg / (attend_ms * 1e-3) / 1e9
-    traffic = read_traffic() if args.workload == WORKLOAD_ID and not offload else None
+    traffic = read_traffic() if args.workload == WORKLOAD_ID else None
     mma = spec.dtype == "bf16" and G <= 8
     kernel = f"zr_attend_mma_kernel<{spec.head_dim}>" if mma else \
         f"zr_attend_fma_kernel<{'bf16' if spec.dtype == 'bf16' else 'float'}, {spec.head_dim}>"
     l2 = (f"inputs exceed L2 (each step reads ~{step_bytes / 1e9:.2f} GB of K/V; no flush)" if step_bytes > 129e6 else
           f"inputs fit in L2 (each step reads ~{step_bytes / 1e6:.1f} MB; no flush: L2-resident timing)")
     line = {
-        "impl": "zoomr", "metric": OFFLOAD_METRIC if offload else METRIC, "value": world * 1e3 / ms, "unit": "steps/s",
+        "impl": "zoomr", "metric": METRIC, "value": world * 1e3 / ms, "unit": "steps/s",
         "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": spec.dtype,
@@ -542,12 +532,6 @@ def run_zoomr(args):
         "clocks": clk,
         "tokens_gathered_per_step": tok_total,
     }
-    if offload:
-        line["path"] = "offload"
-        line["roofline"].update({"bound": "link", "peak": link_gbs, "frac": achieved / link_gbs,
-                                 "peak_kind": "measured pinned-host-to-device copy bandwidth of this box (1 GiB "
-                                              "cudaMemcpyAsync, median of 5)"})
-        line["config"]["pools"] = "pinned host memory (every layer's K/V), read across the CPU-GPU link"
     if cpu_line is not None:
         line["cpu_baseline"] = cpu_line
     if rank == 0:
@@ -559,10 +543,6 @@ def run_zoomr(args):
         dist.destroy_process_group()
     return 0
 
-
-# ---------------------------------------------------------------------- offloaded pools
-OFFLOAD_METRIC = ("decode attention steps/s at 8B shape, 16K ctx, batch 8, 32 layers, K/V pools in pinned host memory "
-                  "read across the CPU-GPU link; link GB/s vs the measured copy bandwidth")
 
 
 def measure_link_gbs(dev) -> float:
@@ -999,6 +979,208 @@ def run_consensus(args):
     return 0
 
 
+# ---------------------------------------------------------------------- offloaded cache, staged per layer
+OFFLOAD_METRIC = ("ZoomR decode steps/s, 512-token prompt + 16K generated, batch 8, 32 layers, every layer's K/V in "
+                  "pinned host memory: per layer the final context's blocks are staged into HBM over the CPU-GPU link "
+                  "(the next layer's while the current one attends); link GB/s vs the measured copy bandwidth")
+
+
+def run_offload(args):
+    """The pages' offloaded decode (ZoomR 3.4, "Decoding Stage"): the cache in host memory; per step the
+    blocks of the consensus path's final context I_f are mapped to staging slots once, and every layer's
+    blocks are staged into one of two HBM staging pools on a copy stream while the previous layer
+    attends. Selection held fixed (a step between semantic boundaries)."""
+    spec = W.CONSENSUS_WORKLOADS[1]
+    world, rank, local = dist_setup(args.gpus)
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: the offload path needs a CUDA GPU")
+    from hierarchical_sparse_kv_gb300 import build as B
+    from hierarchical_sparse_kv_gb300 import zoomr as Z
+
+    if rank == 0 or world == 1:
+        B.build()
+    barrier(world)
+    Z.load()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    st = W.make_consensus_structure(spec)
+    L = spec.layers if args.layers is None else max(1, min(args.layers, spec.layers))
+    Bn, H, Hq, d = st.batch, spec.num_kv_heads, spec.num_q_heads, spec.head_dim
+    G = Hq // H
+    eb = 2 if spec.dtype == "bf16" else 4
+    dt = W.torch_dtype(spec.dtype)
+    bt = torch.from_numpy(st.block_tables.astype(np.int32)).to(dev)
+    cfg = Z.cache_config(batch=Bn, num_kv_heads=H, head_dim=d, num_blocks=st.num_blocks,
+                         max_blocks_per_seq=st.max_blocks_per_seq, dtype=spec.dtype)
+    segs = torch.tensor([(b, s, e, int(st.seg_ptr[b]) + i) for b in range(Bn)
+                         for i, (s, e) in enumerate(st.summary_spans(b))], dtype=torch.int32, device=dev)
+    lts, mks, host = [], [], []
+    for l in range(L):  # draw on the device, keep the mean keys and queries there, move the pools out
+        lt = W.make_consensus_layer(st, l, dev)
+        mk = torch.empty((st.total_segments, H, d), dtype=dt, device=dev)
+        Z.zr_segment_summaries(cfg, segs, bt, lt.k_pool, lt.v_pool, mk, torch.empty_like(mk))
+        mks.append(mk)
+        host.append((lt.k_pool.cpu().pin_memory(), lt.v_pool.cpu().pin_memory()))
+        lt.k_pool = lt.v_pool = None
+        lts.append(lt)
+        torch.cuda.empty_cache()
+    link_gbs = measure_link_gbs(dev)
+    plan = Z.ConsensusPlan.from_structure(st, device=dev)
+    q_all = torch.stack([lt.q for lt in lts])
+    for l, lt in enumerate(lts):
+        lt.q = q_all[l]
+    out_all = torch.empty((L, Bn, Hq, d), dtype=torch.float32, device=dev)
+    dbg = plan.new_debug_outputs()
+    for l in range(L):
+        plan.vote(lts[l].q, mks[l])
+    plan.select(dbg)
+    torch.cuda.synchronize()
+    _, _, rng, nr = (x.cpu().numpy() for x in dbg)
+    need = set()
+    for b in range(Bn):
+        for s_, e_ in rng[b, :nr[b]]:
+            need.update(int(st.block_tables[b, j]) for j in range(int(s_) // 16, (int(e_) - 1) // 16 + 1))
+    cap = len(need)
+    stage_ids = torch.zeros(cap, dtype=torch.int32, device=dev)
+    remap = torch.empty_like(bt)
+    n_staged = torch.zeros(1, dtype=torch.int32, device=dev)
+    bufs = [(torch.empty((cap, H, 16, d), dtype=dt, device=dev), torch.empty((cap, H, 16, d), dtype=dt, device=dev))
+            for _ in range(2)]
+    block_bytes = H * 16 * d * eb
+    staged_bytes = 2 * cap * block_bytes * L  # K and V of every staged block, every layer
+    tok = [A.ranges_token_count(rng[b, :nr[b]]) for b in range(Bn)]
+    attend_bytes = sum(A.attend_bytes_per_unit(tok[b], 0, A.ranges_block_count(rng[b, :nr[b]]), G, d, eb) * H
+                       for b in range(Bn)) + Bn * Hq * d * 4
+    # the attention on a higher-priority stream: its CTAs are placed before further staging-copy CTAs
+    lo_prio, hi_prio = torch.cuda.Stream.priority_range() if hasattr(torch.cuda.Stream, "priority_range") else (0, -1)
+    stream, copy = torch.cuda.Stream(device=dev, priority=hi_prio), torch.cuda.Stream(device=dev, priority=lo_prio)
+    ev_staged = [torch.cuda.Event() for _ in range(L)]
+    ev_freed = [torch.cuda.Event() for _ in range(L)]
+    ev_mapped = torch.cuda.Event()
+
+    def step(kind, s):
+        """kind: "full" (map, then per layer stage + attend, two streams), "stage" (map + the copies only),
+        "attend" (the attention over the staged pools only), "zero_copy" (the attention reading the host
+        pools in place, the previous design)."""
+        if kind == "zero_copy":
+            for l in range(L):
+                plan.attend(lts[l].q, host[l][0], host[l][1], bt, out_all[l], stream=s)
+            return
+        if kind == "attend":
+            for l in range(L):
+                plan.attend(lts[l].q, bufs[l % 2][0], bufs[l % 2][1], remap, out_all[l], stream=s)
+            return
+        Z.zr_offload_map(plan.handle, plan.ws, bt, cap, stage_ids, remap, n_staged, stream=s)
+        if kind == "stage":
+            for l in range(L):
+                Z.zr_offload_stage(plan.handle, host[l][0], host[l][1], stage_ids, n_staged, cap, bufs[l % 2][0],
+                                   bufs[l % 2][1], stream=s)
+            return
+        ev_mapped.record(s)
+        copy.wait_event(ev_mapped)
+        for l in range(L):
+            if l >= 2:
+                copy.wait_event(ev_freed[l - 2])  # staging pool l % 2 is free once layer l - 2 has attended
+            Z.zr_offload_stage(plan.handle, host[l][0], host[l][1], stage_ids, n_staged, cap, bufs[l % 2][0],
+                               bufs[l % 2][1], stream=copy)
+            ev_staged[l].record(copy)
+            s.wait_event(ev_staged[l])
+            plan.attend(lts[l].q, bufs[l % 2][0], bufs[l % 2][1], remap, out_all[l], stream=s)
+            ev_freed[l].record(s)
+
+    graphs = {}
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        step("full", stream)
+        for k in ("full", "stage", "attend", "zero_copy"):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                step(k, stream)
+            graphs[k] = g
+    torch.cuda.synchronize()
+    assert plan.device_error() == 0, "device error word set"
+
+    def timed(kind, steps):
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                graphs[kind].replay()
+        torch.cuda.synchronize()
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(steps):
+                graphs[kind].replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        return max_over_ranks(e0.elapsed_time(e1) / steps, world)
+
+    steps = max(3, min(args.steps, 20))  # a step moves ~3 GB over the link: keep the timed work short
+    clocks = ClockSampler(dev.index) if rank == 0 else None
+    time.sleep(0.25 if clocks and clocks.proc else 0)
+    ms = timed("full", steps)
+    clk = clocks.stop() if clocks else None
+    ms_stage = timed("stage", steps)
+    ms_attend = timed("attend", steps)
+    ms_zero = timed("zero_copy", max(3, steps // 4))
+    assert plan.device_error() == 0, "device error word set"
+
+    host_q = q_all.cpu().pin_memory()
+    host_out = torch.empty(out_all.shape, dtype=out_all.dtype).pin_memory()
+    with torch.cuda.stream(stream):
+        q_all.copy_(host_q, non_blocking=True)
+        graphs["full"].replay()
+        host_out.copy_(out_all, non_blocking=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps):
+            q_all.copy_(host_q, non_blocking=True)
+            graphs["full"].replay()
+            host_out.copy_(out_all, non_blocking=True)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / steps, world)
+
+    link_achieved = staged_bytes / (ms * 1e-3) / 1e9
+    overlap = (ms_stage + ms_attend - ms) / min(ms_stage, ms_attend) if min(ms_stage, ms_attend) > 0 else None
+    line = {
+        "impl": "zoomr", "path": "offload", "metric": OFFLOAD_METRIC, "value": world * 1e3 / ms, "unit": "steps/s",
+        "n_gpus": world, "steps": steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": spec.dtype,
+        "data": "synthetic (seeded N(0,1) K/V, queries near one summary segment's mean key)",
+        "config": {"workload": spec.name + "_offload" + ("" if L == spec.layers else f"_first{L}layers"),
+                   "batch": Bn, "prompt": spec.prompt_len, "generated": spec.gen_len, "layers": L, "q_heads": Hq,
+                   "kv_heads": H, "head_dim": d, "top_k": spec.topk, "consensus": spec.consensus,
+                   "window": spec.window, "graph": True, "staging_slots": cap, "staging_pools": 2,
+                   "pools": "pinned host memory (every layer's K/V); two HBM staging pools of the final context's blocks"},
+        "staged_bytes_per_step": staged_bytes, "final_set_tokens": tok,
+        "stage_only_ms": ms_stage, "attend_only_ms": ms_attend, "zero_copy_ms": ms_zero,
+        "overlap": overlap,
+        "roofline": {"bound": "link", "achieved": link_achieved, "peak": link_gbs, "unit": "GB/s",
+                     "frac": link_achieved / link_gbs, "traffic": None, "kernel": "zr_stage_copy_kernel",
+                     "peak_kind": "measured pinned-host-to-device copy bandwidth of this box (1 GiB cudaMemcpyAsync, "
+                                  "median of 5)",
+                     "alg_bytes_per_launch": 2 * cap * block_bytes,
+                     "timing": "the whole step (map, then every layer's staging copy on a copy stream and its "
+                               "attention on the compute stream), captured as one graph; link bytes / step time"},
+        "hbm_attend_alg_bytes_per_layer": attend_bytes,
+        "e2e": {"value": world * 1e3 / e2e_ms, "unit": "steps/s", "h2d_bytes_per_step": host_q.numel() * eb,
+                "d2h_bytes_per_step": host_out.numel() * 4},
+        "gpu_launches": (4 + L * 3) * steps,
+        "clocks": clk,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    plan.close()
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
 # ---------------------------------------------------------------------- generation loop
 GENERATE_METRIC = ("ZoomR generation steps/s at 8B shape, 512-token prompt + 16K generated, batch 8, 32 layers: every "
                    "step appends each layer's K/V and moves the window, every 35th step also votes and selects")
@@ -1171,10 +1353,11 @@ def main(argv=None):
     ap.add_argument("--path", choices=["decode", "append", "consensus", "offload", "generate"], default="decode",
                     help="decode: the headline decode step; append: the cache-update path (appends and summaries); "
                          "consensus: ZoomR's own consensus selection and attention over its final set; offload: the "
-                         "decode step with the K/V pools in pinned host memory; generate: the consensus path as a "
+                         "consensus decode step with every layer's K/V in pinned host memory, the final context "
+                         "staged into HBM per layer; generate: the consensus path as a "
                          "decode loop (appends, window advance, a selection every 35 steps)")
     ap.add_argument("--layers", type=int, default=None,
-                    help="append and consensus paths only: run the first N layers (a small case for profiling; "
+                    help="append, consensus and offload paths only: run the first N layers (a small case for profiling; "
                          "the metrics are defined on all 32)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
@@ -1185,6 +1368,8 @@ def main(argv=None):
         return run_append(args)
     if args.path == "generate":
         return run_generate(args)
+    if args.path == "offload":
+        return run_offload(args)
     return run_consensus(args) if args.path == "consensus" else run_zoomr(args)
 
 

@@ -18,7 +18,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libzoomr.so")
-SOURCES = ["zoomr_plan.cpp", "zoomr_kernels.cu", "zoomr_static.cu", "zoomr_append.cu", "zoomr_consensus.cu"]
+SOURCES = ["zoomr_plan.cpp", "zoomr_kernels.cu", "zoomr_static.cu", "zoomr_append.cu", "zoomr_consensus.cu",
+           "zoomr_offload.cu"]
 HEADERS = ["zoomr_internal.h", "zoomr_exact_key.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -27,7 +27,7 @@ constexpr int kUnitStartRows = ZR_UNIT_START_ROWS;
 constexpr uint32_t kSummaryFlag = 0x80000000u;  // row id refers to the summary tensors
 constexpr uint32_t kInvalidRow = 0xFFFFFFFFu;   // masked row (past the chunk end, or a bad block id)
 
-enum : int32_t { kErrBadBlock = 1, kErrBadIndex = 2, kErrNonFinite = 4 };
+enum : int32_t { kErrBadBlock = 1, kErrBadIndex = 2, kErrNonFinite = 4, kErrStage = 8 };
 
 // Small device metadata copied from the host at plan time (one allocation).
 struct DeviceMeta {
@@ -51,6 +51,7 @@ struct WsLayout {
   size_t part_o;      // float [U + attend_warps][G][d] unnormalised split outputs
   size_t part_ml;     // float [U + attend_warps][G][2] split (max, sum) in log2 units
   size_t bigkeys;     // uint32 [U][n_max][20] exact keys of units that take the general (640-bit) path
+  size_t stage_marks; // int32 [num_blocks] offload map: staging slot + 1 of every physical block (0: not staged)
   size_t votes;       // consensus only: int32 [B][n_max] vote counts, zero between selections
   size_t cruns;       // consensus only: int32 [B][n_max + 1][2] the last selection's runs before the window
   size_t cnruns;      // consensus only: int32 [B] their count

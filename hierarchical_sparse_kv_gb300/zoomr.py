@@ -93,6 +93,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.zr_decode_attend_reuse.restype = ctypes.c_int
     lib.zr_consensus_advance.argtypes = [_P] * 4
     lib.zr_consensus_advance.restype = ctypes.c_int
+    lib.zr_offload_map.argtypes = [_P, _P, _P, ctypes.c_int32, _P, _P, _P, _P]
+    lib.zr_offload_map.restype = ctypes.c_int
+    lib.zr_offload_stage.argtypes = [_P] * 5 + [ctypes.c_int32, _P, _P, _P]
+    lib.zr_offload_stage.restype = ctypes.c_int
     lib.zr_free.argtypes = [_P]
     lib.zr_free.restype = None
     lib.zr_status_string.argtypes = [ctypes.c_int]
@@ -298,6 +302,33 @@ def zr_segment_summaries(cfg: zr_config, segs: Optional[torch.Tensor], block_tab
                                      _dev(err), _stream(stream))
     if st != ZR_OK:
         raise ZoomrError(st, "zr_segment_summaries")
+
+
+def zr_offload_map(plan: int, workspace: torch.Tensor, block_tables: torch.Tensor, capacity: int,
+                   stage_ids: torch.Tensor, remap_tables: torch.Tensor, n_staged: torch.Tensor, stream=None) -> None:
+    """Staging slots for the blocks the workspace's current token ranges touch (ZoomR 3.4, the offloaded
+    cache): stage_ids [capacity], remap_tables [B, max_blocks] and n_staged [1], all int32 on the device."""
+    for name, t in (("stage_ids", stage_ids), ("remap_tables", remap_tables), ("n_staged", n_staged)):
+        if t.dtype != torch.int32 or not t.is_cuda:
+            raise ValueError(f"{name} must be an int32 CUDA tensor")
+    if stage_ids.numel() < capacity or n_staged.numel() < 1 or remap_tables.shape != block_tables.shape:
+        raise ValueError("zr_offload_map: stage_ids holds capacity entries, remap_tables matches block_tables")
+    st = load().zr_offload_map(plan, _dev(workspace), _dev(block_tables), int(capacity), _dev(stage_ids),
+                               _dev(remap_tables), _dev(n_staged), _stream(stream))
+    if st != ZR_OK:
+        raise ZoomrError(st, "zr_offload_map")
+
+
+def zr_offload_stage(plan: int, host_k_pool: torch.Tensor, host_v_pool: torch.Tensor, stage_ids: torch.Tensor,
+                     n_staged: torch.Tensor, capacity: int, stage_k: torch.Tensor, stage_v: torch.Tensor,
+                     stream=None) -> None:
+    """One layer's staging copy: the mapped blocks of the host pools into slots of the staging pools."""
+    if stage_k.shape[0] < capacity or stage_v.shape[0] < capacity:
+        raise ValueError("zr_offload_stage: the staging pools hold capacity blocks")
+    st = load().zr_offload_stage(plan, _pool(host_k_pool), _pool(host_v_pool), _dev(stage_ids), _dev(n_staged),
+                                 int(capacity), _dev(stage_k), _dev(stage_v), _stream(stream))
+    if st != ZR_OK:
+        raise ZoomrError(st, "zr_offload_stage")
 
 
 class DecodePlan:

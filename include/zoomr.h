@@ -203,8 +203,9 @@ ZR_API zr_status zr_decode_attend_static(zr_plan_t plan, const void* q, const vo
  * zr_get_device_error -- synchronize `stream`, then read and clear the sticky
  * device error word of `workspace` into *err_code (0 = none; bit 1 (value 1) = a
  * physical block id outside the pool; bit 3 (value 4) = a non-finite query or
- * summary-key value, ranked as zero). Returns ZR_EDEVICE if the word was non-zero,
- * ZR_OK otherwise.
+ * summary-key value, ranked as zero; bit 4 (value 8) = more blocks to stage than
+ * zr_offload_map's capacity). Returns ZR_EDEVICE if the word was non-zero, ZR_OK
+ * otherwise.
  */
 ZR_API zr_status zr_get_device_error(zr_plan_t plan, void* workspace, void* stream, int32_t* err_code);
 
@@ -390,6 +391,46 @@ ZR_API zr_status zr_decode_attend_reuse(zr_plan_t plan, void* workspace, const v
  * then attends over them.
  */
 ZR_API zr_status zr_consensus_advance(zr_plan_t plan, void* workspace, const int32_t* seq_lens, void* stream);
+
+/*
+ * The offloaded cache: ZoomR page, 3.4 "System Implementation and Inference",
+ * "Decoding Stage" (the full KV cache stays in host memory; for every layer only
+ * the final context I_f is brought to the GPU, the next layer's while the current
+ * one attends). The pools of every layer live in host memory the device can read
+ * (pinned or registered); the caller owns two staging pools in HBM of `capacity`
+ * blocks each, [capacity, Hkv, 16, d] dtype, and alternates them over the layers.
+ *
+ * zr_offload_map -- after a selection or an advance (zr_decode_attend,
+ * zr_consensus_select, zr_decode_advance, zr_consensus_advance on this
+ * workspace): give a staging slot to every physical block that the workspace's
+ * current token ranges touch (the union over every KV head of a sequence, each
+ * shared block once, slots in ascending physical order).
+ *   block_tables  [B, max_blocks_per_seq] int32 (device): the host pools' tables
+ *   capacity      slots per staging pool (>= 1)
+ *   stage_ids     [capacity] int32 (device, out): physical block of each used slot
+ *   remap_tables  [B, max_blocks_per_seq] int32 (device, out): the slot of every
+ *                 logical block a range touches, -1 elsewhere; pass it as the
+ *                 block tables of the attention over the staging pools
+ *   n_staged      [1] int32 (device, out): slots used, min(blocks touched, capacity)
+ * Asynchronous on `stream`. More blocks than `capacity` set bit 4 (value 8) of the
+ * workspace error word; the blocks past capacity map to -1 and their rows are
+ * masked. Errors: ZR_EINVAL (null pointer, capacity < 1), ZR_ECUDA.
+ */
+ZR_API zr_status zr_offload_map(zr_plan_t plan, void* workspace, const int32_t* block_tables, int32_t capacity,
+                                int32_t* stage_ids, int32_t* remap_tables, int32_t* n_staged, void* stream);
+
+/*
+ * zr_offload_stage -- one layer's staging copy: slot i of stage_k / stage_v
+ * receives block stage_ids[i] (all KV heads) of host_k_pool / host_v_pool, for
+ * i < *n_staged (both from zr_offload_map). Pools [num_blocks, Hkv, 16, d] in host
+ * memory the device can read; staging pools [capacity, Hkv, 16, d] in device
+ * memory; all 16-byte aligned. Asynchronous on `stream` (a copy stream, so the
+ * next layer's copy overlaps the current layer's attention). Errors: ZR_EINVAL
+ * (null or misaligned pointer, capacity < 1), ZR_ECUDA.
+ */
+ZR_API zr_status zr_offload_stage(zr_plan_t plan, const void* host_k_pool, const void* host_v_pool,
+                                  const int32_t* stage_ids, const int32_t* n_staged, int32_t capacity,
+                                  void* stage_k, void* stage_v, void* stream);
 
 /* zr_free -- release the plan and its small device metadata (NULL is a no-op). */
 ZR_API void zr_free(zr_plan_t plan);
