@@ -874,6 +874,9 @@ def run_consensus(args):
     attend_bytes = sum(A.attend_bytes_per_unit(tok[b], 0, A.ranges_block_count(rng[b, :nr[b]]), G, d, eb) * H
                        for b in range(Bn)) + Bn * Hq * d * 4
     stream = torch.cuda.Stream(device=dev)
+    pair = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(L)]
+    for e_ in [e for p_ in pair for e in p_]:
+        e_.record(stream)  # torch creates CUDA events lazily: create them all before any capture
 
     def step(kind, s):
         if kind in ("select", "full"):
@@ -883,12 +886,16 @@ def run_consensus(args):
         if kind in ("attend", "full"):
             for l in range(L):
                 plan.attend(lts[l].q, lts[l].k_pool, lts[l].v_pool, bt, out_all[l], stream=s)
+        if kind == "pair":  # an event pair around every layer's gather-attention kernel
+            for l in range(L):
+                plan.attend_timed(lts[l].q, lts[l].k_pool, lts[l].v_pool, bt, out_all[l], pair[l][0], pair[l][1],
+                                  stream=s)
 
     graphs = {}
     stream.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(stream):
         step("full", stream)
-        for k in ("full", "attend", "select"):
+        for k in ("full", "attend", "select", "pair"):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
                 step(k, stream)
@@ -917,6 +924,12 @@ def run_consensus(args):
     ms_full = timed("full", args.steps)
     clk = clocks.stop() if clocks else None
     ms_select = timed("select", args.steps)
+    pair_ms = []
+    for _ in range(max(1, -(-args.attend_samples // L))):
+        with torch.cuda.stream(stream):
+            graphs["pair"].replay()
+        torch.cuda.synchronize()
+        pair_ms += [pair[l][0].elapsed_time(pair[l][1]) for l in range(L)]
     assert plan.device_error() == 0, "device error word set"
     # one selection step every SELECTION_INTERVAL steps, attention-only steps in between
     ms_mixed = (ms_full + (SELECTION_INTERVAL - 1) * ms_attend) / SELECTION_INTERVAL
@@ -943,7 +956,8 @@ def run_consensus(args):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
 
     peak, peak_kind = read_peak()
-    attend_us = ms_attend * 1e3 / L
+    layer_us = ms_attend * 1e3 / L  # one layer of the attention-only step: gather-attention + merge + handoffs
+    attend_us = sum(pair_ms) / len(pair_ms) * 1e3
     achieved = attend_bytes / (attend_us * 1e-6) / 1e9
     line = {
         "impl": "zoomr", "path": "consensus", "metric": CONSENSUS_METRIC, "value": world * 1e3 / ms_mixed,
@@ -961,7 +975,14 @@ def run_consensus(args):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_kind": f"{peak_kind} copy bandwidth", "traffic": None,
                      "kernel": f"zr_attend_mma_kernel<{d}>", "alg_bytes_per_launch": attend_bytes,
-                     "timing": "attention-only graph of 32 layers (gather-attention + merge), time / 32"},
+                     "attend_us": attend_us, "samples": len(pair_ms),
+                     "timing": f"mean over {len(pair_ms)} gather-attention launches (every layer of replayed "
+                               "attention-only steps), each between two CUDA events on the launching stream (the "
+                               "pair includes the event nodes' latency)",
+                     "per_layer_of_step": {"us": layer_us, "achieved": attend_bytes / (layer_us * 1e-6) / 1e9,
+                                           "frac": attend_bytes / (layer_us * 1e-6) / 1e9 / peak,
+                                           "timing": "attention-only graph of 32 layers (gather-attention + merge "
+                                                     "+ handoffs), time / 32"}},
         "e2e": {"value": world * 1e3 / e2e_ms, "unit": "steps/s", "h2d_bytes_per_step": host_q.numel() * eb,
                 "d2h_bytes_per_step": host_out.numel() * 4},
         "gpu_launches": int(round(args.steps * (2 * L + (L + 1) / SELECTION_INTERVAL))),

@@ -126,8 +126,10 @@ zr_status decode_into(zr_plan_t plan, void* workspace, const void* q, const void
 // for at most `useful_warps` warps.
 zr_status configure_kernels(Plan& p, int64_t useful_warps);
 zr_status launch_step(const Plan& p, const StepArgs& a, void* stream, void* ev_start, void* ev_stop);
-// Gather-attention and merge only, over the unit metadata already in the workspace.
-zr_status launch_attend_only(const Plan& p, const StepArgs& a, void* stream);
+// Gather-attention and merge only, over the unit metadata already in the workspace; optional events
+// (null: none) recorded just before and just after the gather-attention kernel.
+zr_status launch_attend_only(const Plan& p, const StepArgs& a, void* stream, void* ev_start = nullptr,
+                             void* ev_stop = nullptr);
 
 // Implemented in zoomr_consensus.cu.
 size_t vote_smem_bytes(int G, int d, int n_max);

@@ -1319,15 +1319,17 @@ cudaError_t launch_for(const Plan& p, const StepArgs& a, cudaStream_t s, cudaEve
 }
 
 template <typename T, int D>
-cudaError_t launch_attend_for(const Plan& p, const StepArgs& a, cudaStream_t s) {
+cudaError_t launch_attend_for(const Plan& p, const StepArgs& a, cudaStream_t s, cudaEvent_t ev0, cudaEvent_t ev1) {
   const dim3 grid_attend(p.attend_ctas), block(kAttendWarps * 32);
   cudaError_t e = cudaSuccess;
+  if (ev0 && (e = record_event(ev0, s)) != cudaSuccess) return report("start event record", e), e;
   if (uses_mma<T, D>(p)) {
     if constexpr (sizeof(T) == 2) e = launch_pdl(zr_attend_mma_kernel<D>, grid_attend, block, p.attend_smem, s, a);
   } else {
     e = launch_pdl(zr_attend_fma_kernel<T, D>, grid_attend, block, 0, s, a);
   }
   if (e != cudaSuccess) return report("attend launch", e), e;
+  if (ev1 && (e = record_event(ev1, s)) != cudaSuccess) return report("stop event record", e), e;
   if (p.merge_parts) {
     e = launch_pdl(zr_merge_part_kernel<D>, dim3(p.B * p.Hq * (D / kMergeComp) / kMergeWarps),
                    dim3(kMergeWarps * 32), 0, s, a);
@@ -1348,13 +1350,15 @@ zr_status configure_kernels(Plan& p, int64_t useful_warps) {
   return p.d == 64 ? configure_for<float, 64>(p, useful_warps) : configure_for<float, 128>(p, useful_warps);
 }
 
-zr_status launch_attend_only(const Plan& p, const StepArgs& a, void* stream) {
+zr_status launch_attend_only(const Plan& p, const StepArgs& a, void* stream, void* ev_start, void* ev_stop) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaEvent_t e0 = static_cast<cudaEvent_t>(ev_start), e1 = static_cast<cudaEvent_t>(ev_stop);
   cudaError_t e;
   if (p.cfg.dtype == ZR_BF16)
-    e = p.d == 64 ? launch_attend_for<__nv_bfloat16, 64>(p, a, s) : launch_attend_for<__nv_bfloat16, 128>(p, a, s);
+    e = p.d == 64 ? launch_attend_for<__nv_bfloat16, 64>(p, a, s, e0, e1)
+                  : launch_attend_for<__nv_bfloat16, 128>(p, a, s, e0, e1);
   else
-    e = p.d == 64 ? launch_attend_for<float, 64>(p, a, s) : launch_attend_for<float, 128>(p, a, s);
+    e = p.d == 64 ? launch_attend_for<float, 64>(p, a, s, e0, e1) : launch_attend_for<float, 128>(p, a, s, e0, e1);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return ZR_ECUDA;

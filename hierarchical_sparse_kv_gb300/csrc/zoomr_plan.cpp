@@ -532,8 +532,10 @@ zr_status zr_consensus_select(zr_plan_t plan, void* workspace, int32_t* votes_ou
                               votes_out, consensus_out, stream);
 }
 
-zr_status zr_consensus_attend(zr_plan_t plan, void* workspace, const void* q, const void* k_pool,
-                              const void* v_pool, const int32_t* block_tables, float* out, void* stream) {
+namespace {
+zr_status consensus_attend_into(zr_plan_t plan, void* workspace, const void* q, const void* k_pool,
+                                const void* v_pool, const int32_t* block_tables, float* out, void* stream,
+                                void* ev_start, void* ev_stop) {
   if (!plan || !workspace || !q || !k_pool || !v_pool || !block_tables || !out) return ZR_EINVAL;
   if (plan->p.mode != zr::kConsensusPlan) return ZR_EINVAL;
   if (!aligned(workspace, 256) || !aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) ||
@@ -547,7 +549,20 @@ zr_status zr_consensus_attend(zr_plan_t plan, void* workspace, const void* q, co
   a.sum_k = k_pool;  // no summary rows are gathered: every unit's summary count is 0
   a.sum_v = v_pool;
   a.out = out;
-  return zr::launch_attend_only(plan->p, a, stream);
+  return zr::launch_attend_only(plan->p, a, stream, ev_start, ev_stop);
+}
+}  // namespace
+
+zr_status zr_consensus_attend(zr_plan_t plan, void* workspace, const void* q, const void* k_pool,
+                              const void* v_pool, const int32_t* block_tables, float* out, void* stream) {
+  return consensus_attend_into(plan, workspace, q, k_pool, v_pool, block_tables, out, stream, nullptr, nullptr);
+}
+
+zr_status zr_consensus_attend_timed(zr_plan_t plan, void* workspace, const void* q, const void* k_pool,
+                                    const void* v_pool, const int32_t* block_tables, float* out, void* ev_start,
+                                    void* ev_stop, void* stream) {
+  if (!ev_start && !ev_stop) return ZR_EINVAL;
+  return consensus_attend_into(plan, workspace, q, k_pool, v_pool, block_tables, out, stream, ev_start, ev_stop);
 }
 
 }  // extern "C"

@@ -87,6 +87,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.zr_consensus_select.restype = ctypes.c_int
     lib.zr_consensus_attend.argtypes = [_P] * 8
     lib.zr_consensus_attend.restype = ctypes.c_int
+    lib.zr_consensus_attend_timed.argtypes = [_P] * 10
+    lib.zr_consensus_attend_timed.restype = ctypes.c_int
     lib.zr_decode_advance.argtypes = [_P] * 4
     lib.zr_decode_advance.restype = ctypes.c_int
     lib.zr_decode_attend_reuse.argtypes = [_P] * 10
@@ -195,19 +197,24 @@ def zr_decode_attend(plan: int, workspace: torch.Tensor, q: torch.Tensor, k_pool
         raise ZoomrError(st, "zr_decode_attend")
 
 
+def _event(ev: Optional[torch.cuda.Event], stream=None) -> Optional[int]:
+    """The cudaEvent_t of a torch event (None stays None), created by a first record if needed."""
+    if ev is None:
+        return None
+    if ev.cuda_event == 0:  # torch creates the CUDA event lazily, at its first record
+        if torch.cuda.is_current_stream_capturing():
+            raise ValueError("zoomr: record timing events once before using them inside a stream capture")
+        ev.record(torch.cuda.current_stream() if stream is None or isinstance(stream, int) else stream)
+    return ev.cuda_event
+
+
 def zr_decode_attend_timed(plan: int, workspace: torch.Tensor, q: torch.Tensor, k_pool: torch.Tensor,
                            v_pool: torch.Tensor, block_tables: torch.Tensor, sum_k: torch.Tensor,
                            sum_v: torch.Tensor, out: torch.Tensor, ev_start: Optional[torch.cuda.Event],
                            ev_stop: Optional[torch.cuda.Event], stream=None) -> None:
-    for ev in (ev_start, ev_stop):
-        if ev is not None and ev.cuda_event == 0:  # torch creates the CUDA event lazily, at its first record
-            if torch.cuda.is_current_stream_capturing():
-                raise ValueError("zoomr: record timing events once before using them inside a stream capture")
-            ev.record(torch.cuda.current_stream() if stream is None or isinstance(stream, int) else stream)
     st = load().zr_decode_attend_timed(plan, _dev(workspace), _dev(q), _pool(k_pool), _pool(v_pool),
                                        _dev(block_tables), _dev(sum_k), _dev(sum_v), _dev(out),
-                                       ev_start.cuda_event if ev_start is not None else None,
-                                       ev_stop.cuda_event if ev_stop is not None else None, _stream(stream))
+                                       _event(ev_start, stream), _event(ev_stop, stream), _stream(stream))
     if st != ZR_OK:
         raise ZoomrError(st, "zr_decode_attend_timed")
 
@@ -489,6 +496,14 @@ class ConsensusPlan:
                                         _dev(block_tables), _dev(out), _stream(stream))
         if st != ZR_OK:
             raise ZoomrError(st, "zr_consensus_attend")
+
+    def attend_timed(self, q, k_pool, v_pool, block_tables, out, ev_start, ev_stop, stream=None) -> None:
+        """attend with CUDA events just before and just after the gather-attention kernel (either may be None)."""
+        st = load().zr_consensus_attend_timed(self.handle, _dev(self.ws), _dev(q), _pool(k_pool), _pool(v_pool),
+                                              _dev(block_tables), _dev(out), _event(ev_start, stream),
+                                              _event(ev_stop, stream), _stream(stream))
+        if st != ZR_OK:
+            raise ZoomrError(st, "zr_consensus_attend_timed")
 
     def advance(self, seq_lens: torch.Tensor, stream=None) -> None:
         """Move every sequence's window to the new lengths (device int32 [B]), I_c and I_s held fixed."""

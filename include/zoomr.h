@@ -353,6 +353,18 @@ ZR_API zr_status zr_consensus_attend(zr_plan_t plan, void* workspace, const void
                                      const void* v_pool, const int32_t* block_tables, float* out, void* stream);
 
 /*
+ * zr_consensus_attend_timed -- zr_consensus_attend with two CUDA events
+ * (cudaEvent_t, either may be NULL but not both) recorded on `stream` just
+ * before and just after the gather-attention kernel, so that the kernel alone can
+ * be timed; the merge follows the second event. In a stream capture the events
+ * become event-record nodes. Errors: as zr_consensus_attend; ZR_EINVAL if both
+ * events are NULL.
+ */
+ZR_API zr_status zr_consensus_attend_timed(zr_plan_t plan, void* workspace, const void* q, const void* k_pool,
+                                           const void* v_pool, const int32_t* block_tables, float* out,
+                                           void* ev_start, void* ev_stop, void* stream);
+
+/*
  * ------------------------------------------- steps between selections (amortisation)
  * ZoomR page, 3.4 "Decoding Stage" and appendix A.3 "Semantic Boundaries": the
  * selection is recomputed only at semantic boundaries (about every 35 tokens)

@@ -195,3 +195,28 @@ def test_full_size_votes_and_sampled_attention():
         for l in layers:
             want = OC.attend_final(_np32(lts[l].q)[b], kp[l], vp[l], st.block_tables[b], res[b].tokens, G)
             assert np.max(np.abs(o[l][b].astype(np.float64) - want)) <= TOL["bf16"], (b, l)
+
+
+def test_timed_attend_matches_and_times_the_kernel():
+    """zr_consensus_attend_timed: the same outputs as zr_consensus_attend, with events around the
+    gather-attention kernel (either one alone works too)."""
+    st, lts = _setup(dtype="bf16", head_dim=128, num_q_heads=8, num_kv_heads=2, layers=1)
+    plan = Z.ConsensusPlan.from_structure(st)
+    bt = torch.from_numpy(st.block_tables.astype(np.int32)).cuda()
+    sp = st.spec
+    mk = _device_mean_keys(st, lts[0], bt)
+    plan.vote(lts[0].q, mk)
+    plan.select()
+    ref = torch.empty((st.batch, sp.num_q_heads, sp.head_dim), device="cuda")
+    plan.attend(lts[0].q, lts[0].k_pool, lts[0].v_pool, bt, ref)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for a_, b_ in ((e0, e1), (e0, None), (None, e1)):
+        out = torch.full_like(ref, float("nan"))
+        plan.attend_timed(lts[0].q, lts[0].k_pool, lts[0].v_pool, bt, out, a_, b_)
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref)
+    plan.attend_timed(lts[0].q, lts[0].k_pool, lts[0].v_pool, bt, out, e0, e1)
+    torch.cuda.synchronize()
+    assert e0.elapsed_time(e1) > 0
+    assert plan.device_error() == 0
+    plan.close()
