@@ -38,6 +38,7 @@ namespace zr {
 namespace {
 
 constexpr unsigned kFull = 0xFFFFFFFFu;
+constexpr int kWarpRangesMax = 256;  // segments up to which one warp builds a unit's lists and ranges
 
 // ------------------------------------------------------------------ helpers
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
@@ -302,9 +303,11 @@ __global__ void __maxnreg__(80) zr_select_kernel(StepArgs a) {
   // 2. top-k: segment i is selected iff fewer than k segments beat it (a greater exact key, or an equal
   //    key and a lower index). The top-k of the estimates is the exact one when its certificate holds
   //    (the enclosures separate at the k boundary); otherwise the keys are computed exactly.
-  if (!xk::certify_top_k<kSelectThreads>(elo, ehi, n, k, kh, kl, flag, s_cert))
+  // (certify_top_k ends with a barrier after its flags are written; the exact path needs one more)
+  if (!xk::certify_top_k<kSelectThreads>(elo, ehi, n, k, kh, kl, flag, s_cert)) {
     exact_select<T, D>(a, u, qg, rows, stride, n, k, qh, ql, qtail, kh, kl, flag, &s_flags, s_red);
-  __syncthreads();
+    __syncthreads();
+  }
 
   // 3. the selected list (ascending), the summary list (the rest, ascending), the maximal runs of
   //    selected segments (consecutive segments touch), and the token ranges: the runs merged with
@@ -315,7 +318,74 @@ __global__ void __maxnreg__(80) zr_select_kernel(StepArgs a) {
   int* cum = a.cum + static_cast<size_t>(u) * (a.k_max + 2);
   int* rout = a.ranges_out ? a.ranges_out + static_cast<size_t>(u) * (a.k_max + 1) * 2 : nullptr;
   const int W0 = max(0, L - a.window);
-  if (n <= kSelectThreads) {
+  if (n <= kWarpRangesMax) {
+    // Warp 0 alone, 32 segments per pass: compaction and run numbering from ballots, with carries
+    // between passes; then the ranges. No CTA barrier: the other warps are done.
+    if (tid < 32) {
+      const int lane = tid;
+      const unsigned lt = (1u << lane) - 1u;
+      int c_sel = 0, c_run = 0, rstar = 0;
+      for (int base = 0; base < n; base += 32) {
+        const int i = base + lane;
+        const bool in = i < n;
+        const bool sel = in && flag[i];
+        const bool rstart = sel && !(i > 0 && flag[i - 1]);
+        const bool rend = sel && !(i + 1 < n && flag[i + 1]);
+        const int e_i = in ? bnd[i + 1] : 0;
+        const unsigned bs = __ballot_sync(kFull, sel), bst = __ballot_sync(kFull, rstart);
+        const unsigned bbe = __ballot_sync(kFull, rend && e_i < W0);
+        const int pos = c_sel + __popc(bs & lt);
+        if (in) {
+          if (sel) {
+            list[pos] = i;
+            sel_ws[pos] = i;
+          } else {
+            sum_ws[i - pos] = i;
+          }
+        }
+        if (rstart) runs_s[c_run + __popc(bst & lt)] = bnd[i];
+        if (rend) runs_e[c_run + __popc(bst & (lt | (1u << lane))) - 1] = e_i;
+        c_sel += __popc(bs);
+        c_run += __popc(bst);
+        rstar += __popc(bbe);
+      }
+      __syncwarp();  // runs_s / runs_e are complete
+      const int m = c_run;  // runs; rstar of them end before W0
+      const int nr = rstar < m ? rstar + 1 : m + (W0 < L ? 1 : 0);
+      int carry = 0;
+      for (int r0 = 0; r0 < nr; r0 += 32) {
+        const int r = r0 + lane;
+        int s_ = 0, e_ = 0;
+        if (r < nr) {
+          if (r < rstar) {
+            s_ = runs_s[r];
+            e_ = runs_e[r];
+          } else {
+            s_ = rstar < m ? min(W0, runs_s[rstar]) : W0;
+            e_ = L;
+          }
+        }
+        const int len = e_ - s_;
+        const int incl = warp_incl_scan(len, lane);
+        if (r < nr) {
+          rg[2 * r] = s_;
+          rg[2 * r + 1] = e_;
+          cum[r] = carry + incl - len;
+          if (rout) {
+            rout[2 * r] = s_;
+            rout[2 * r + 1] = e_;
+          }
+        }
+        carry += __shfl_sync(kFull, incl, 31);
+      }
+      if (lane == 0) {
+        cum[nr] = carry;
+        a.unit_info[u] = make_int4(nr, carry, n - k, 0);
+        a.unit_rows[u] = carry + n - k;
+        if (a.nranges_out) a.nranges_out[u] = nr;
+      }
+    }
+  } else if (n <= kSelectThreads) {
     // One thread per segment: compaction and run numbering from warp ballots.
     __shared__ int s_cnt[3][kSelectThreads / 32];
     const int lane = tid & 31, wi = tid >> 5, nwarps = blockDim.x >> 5;
@@ -476,6 +546,7 @@ __global__ void __maxnreg__(80) zr_select_kernel(StepArgs a) {
     if (tid < 32) add_sink_range(a, u, Ns, rg, cum, rout, tid);
   }
   if (a.sel_out) {
+    __syncthreads();  // list is complete (on the one-warp path warp 0 alone wrote it)
     int* so = a.sel_out + static_cast<size_t>(u) * a.k_max;
     for (int j = tid; j < a.k_max; j += blockDim.x) so[j] = j < k ? list[j] : -1;
   }
