@@ -1,11 +1,10 @@
 // Consensus selection of the ZoomR page, section 3.3, on the device.
 //
 //   vote       one CTA per (sequence b, KV head g) and layer: for every query head
-//              of the group, the fp32 score of every summary (3.3 "Per-Head
-//              Importance Scoring and Voting", alpha_i = q^T kbar_i; each product
-//              and partial sum rounded to nearest-even, components in ascending
-//              order), its top-k by rank counting (ties to the lower index), and
-//              one vote per selected summary added to the sequence's vote counts.
+//              of the group, the top-k of the summaries by the exact score
+//              alpha_i = q^T kbar_i of the stored values (3.3 "Per-Head Importance
+//              Scoring and Voting"; ties to the lower index), and one vote per
+//              selected summary added to the sequence's vote counts.
 //   consensus  one CTA per sequence, once per selection: I_all (summaries with a
 //              vote), I_c (the c with the most votes, ties to the lower index),
 //              I_s = I_all minus I_c (3.3 "Global Aggregation and Consensus"); the
@@ -33,12 +32,15 @@ constexpr unsigned kFullMask = 0xFFFFFFFFu;
 constexpr int kVoteThreads = 256;
 constexpr int kConsensusThreads = 256;
 
-// Shared memory: the exact-key scorer's query limb tables | key high words [n_max + 4] u64 | key low words
-// [n_max + 4] u64 | flag [n_max + 2] | fp32 enclosures lo, hi [n_max] each.
+// Shared memory: the exact-key scorer's query limb tables | the query table [G * D] | key high words
+// [n_max + 4] u64 | key low words [n_max + 4] u64 | flag [n_max + 2] | fp32 enclosures lo, hi [n_max] each.
 template <typename T, int D>
 struct VoteLayout {
   using SC = xk::Scorer<T, D, kVoteThreads>;
-  __host__ __device__ static constexpr size_t q_bytes(int G) { return (SC::smem_bytes(G) + 15) / 16 * 16; }
+  __host__ __device__ static constexpr size_t limb_bytes(int G) { return (SC::smem_bytes(G) + 15) / 16 * 16; }
+  __host__ __device__ static constexpr size_t q_bytes(int G) {
+    return limb_bytes(G) + sizeof(T) * static_cast<size_t>(G) * D;
+  }
   __host__ __device__ static constexpr size_t bytes(int G, int n_max) {
     return q_bytes(G) + 2 * sizeof(uint64_t) * (static_cast<size_t>(n_max) + 4) +
            sizeof(int) * (static_cast<size_t>(n_max) + 2) + 2 * sizeof(float) * static_cast<size_t>(n_max);
@@ -47,8 +49,8 @@ struct VoteLayout {
 
 // For every query head of the group, one at a time: the top-k of the summaries by the exact key
 // alpha_i = q_h . kbar_i on the stored values (ties to the lower index) and one vote per selected summary.
-// The fp32 estimates decide where their enclosures separate at the k boundary; otherwise the keys are
-// computed exactly (the integer limbs, or the general 640-bit path), the limb tables built once per unit.
+// The fp32 estimates decide where their enclosures separate at the k boundary; otherwise the uncertain
+// summaries' keys are computed exactly (the integer limbs, or the general 640-bit path).
 template <typename T, int D>
 __global__ void __maxnreg__(96) zr_vote_kernel(StepArgs a, const T* __restrict__ mean_keys,
                                                int32_t* __restrict__ votes) {
@@ -59,6 +61,7 @@ __global__ void __maxnreg__(96) zr_vote_kernel(StepArgs a, const T* __restrict__
   int* qh = reinterpret_cast<int*>(vsmem);
   int* ql = qh + G * SC::kQRow;
   int* qtail = ql + G * SC::kQRow;
+  uint4* qtab = reinterpret_cast<uint4*>(vsmem + LY::limb_bytes(G));
   uint64_t* kh = reinterpret_cast<uint64_t*>(vsmem + LY::q_bytes(G));
   uint64_t* kl = kh + nmax + 4;
   int* flag = reinterpret_cast<int*>(kl + nmax + 4);
@@ -76,12 +79,9 @@ __global__ void __maxnreg__(96) zr_vote_kernel(StepArgs a, const T* __restrict__
   const T* rows = mean_keys + (static_cast<size_t>(s0) * a.Hkv + g) * D;
   const size_t stride = static_cast<size_t>(a.Hkv) * D;
   int32_t* vb = votes + static_cast<size_t>(b) * nmax;
-  if (tid == 0) s_flags = 0;
-  bool exact_ready = false;  // CTA-uniform
-  xk::Frame fr{};
-  uint4 cache[SC::kVPS];
   for (int h = 0; h < G; ++h) {
-    xk::estimate_rows<T, D, kVoteThreads, false>(qg, h, 1, rows, stride, n,
+    // the first head builds the query table
+    xk::estimate_rows<T, D, kVoteThreads, false, 16>(h == 0 ? qg : nullptr, G, qtab, h, 1, rows, stride, n,
                                                   [&](int r, int, float mid, float lo, float hi) {
                                                     kh[r] = 0;
                                                     kl[r] = xk::order_bits(mid);
@@ -89,34 +89,15 @@ __global__ void __maxnreg__(96) zr_vote_kernel(StepArgs a, const T* __restrict__
                                                     ehi[r] = hi;
                                                   });
     __syncthreads();
-    if (!xk::certify_top_k<kVoteThreads>(elo, ehi, n, k, kh, kl, flag, s_cert)) {
-      int fl = 0;
-      if (!exact_ready) {
-        fr = xk::unit_frame<T, D, kVoteThreads>(qg, G, rows, stride, n, s_red, qtail, fl, cache);
-        if (!fr.general) xk::load_q_limbs<T, D, kVoteThreads>(qg, G, fr, qh, ql, qtail, fl);
-        exact_ready = true;
-      }
-      if (!fr.general)
-        xk::score_rows<T, D, kVoteThreads, false>(rows, stride, n, fr, qh, ql, qtail, h, 1, fl, cache,
-                                                   [&](int r, int, uint64_t uh, uint64_t ul) {
-                                                     kh[r] = uh;
-                                                     kl[r] = ul;
-                                                   });
-      if (fl) atomicOr(&s_flags, fl);
-      __syncthreads();
-      const int uflags = s_flags;
+    float cert_lo, cert_hi;
+    if (!xk::certify_top_k<kVoteThreads>(elo, ehi, n, k, kh, kl, flag, s_cert, cert_lo, cert_hi)) {
+      const int uflags = xk::resolve_top_k<T, D, kVoteThreads, false>(
+          qg, G, h, 1, rows, stride, n, k, elo, ehi, cert_lo, cert_hi, flag, reinterpret_cast<int*>(elo),
+          reinterpret_cast<int*>(ehi), kh, kl, qh, ql, qtail, s_red, &s_flags,
+          a.bigkeys + static_cast<size_t>(u) * nmax * xk::kBigDigits);
       if ((uflags & xk::kFlagNonFinite) && tid == 0) atomicOr(a.err, kErrNonFinite);
-      if (fr.general || (uflags & xk::kFlagDeep)) {
-        // a value far below its side's largest (or a non-finite one): the general 640-bit path, keys in
-        // the workspace
-        uint32_t* big = a.bigkeys + static_cast<size_t>(u) * nmax * xk::kBigDigits;
-        xk::big_keys<T, D, kVoteThreads>(qg, h, 1, rows, stride, n, big);
-        xk::big_rank_select<kVoteThreads>(big, n, k, flag);
-      } else {
-        xk::rank_select<kVoteThreads>(kh, kl, n, k, !fr.narrow, flag);
-      }
     }
-    __syncthreads();
+    // (certify_top_k and resolve_top_k end with a barrier after the flags are written)
     for (int i = tid; i < n; i += kVoteThreads)
       if (flag[i]) atomicAdd(vb + i, 1);
     __syncthreads();  // flag, the estimates and the keys are reused by the next head

@@ -185,13 +185,13 @@ __device__ __forceinline__ void add_vec(MagStats& s, const uint4& w) {
   for (int e = 0; e < 16 / static_cast<int>(sizeof(T)); ++e) add_mag<T>(s, elem_bits<T>(w, e));
 }
 
-// The unit's frame from the group's queries qg [G][D] and its n summary-key rows (row r at rows + r *
-// stride), reduced over the CTA; every thread returns it. cache receives this thread's slice of row
-// tid / kSPR (the scorer's first pass). red: shared [4 * NT/32]; qmask [kSPR] is cleared for
-// load_q_limbs (the barrier inside orders the two).
+// The frame from the group's queries qg [G][D] and n summary-key rows (row r at rows + idx[r] * stride,
+// or rows + r * stride without idx), reduced over the CTA; every thread returns it. cache receives this
+// thread's slice of row tid / kSPR (the scorer's first pass). red: shared [4 * NT/32]; qmask [kSPR] is
+// cleared for load_q_limbs (the barrier inside orders the two).
 template <typename T, int D, int NT>
 __device__ Frame unit_frame(const T* qg, int G, const T* rows, size_t stride, int n, uint32_t* red, int* qmask,
-                            int& flags, uint4 (&cache)[Scorer<T, D, NT>::kVPS]) {
+                            int& flags, uint4 (&cache)[Scorer<T, D, NT>::kVPS], const int* idx = nullptr) {
   using S = Scorer<T, D, NT>;
   using F = Fmt<T>;
   constexpr int NW = NT / 32;
@@ -201,7 +201,8 @@ __device__ Frame unit_frame(const T* qg, int G, const T* rows, size_t stride, in
   for (int v = tid; v < G * D / S::kEPV; v += NT) add_vec<T>(q, reinterpret_cast<const uint4*>(qg)[v]);
   const int j = tid % S::kSPR;
   for (int r = tid / S::kSPR; r < n; r += S::kRPP) {
-    const uint4* src = reinterpret_cast<const uint4*>(rows + r * stride + j * kSlice);
+    const uint4* src = reinterpret_cast<const uint4*>(rows + static_cast<size_t>(idx ? idx[r] : r) * stride +
+                                                      j * kSlice);
 #pragma unroll
     for (int c = 0; c < S::kVPS; ++c) {
       const uint4 w = src[c];
@@ -299,7 +300,8 @@ __device__ __forceinline__ void ordered(__int128 v, uint64_t& uh, uint64_t& ul) 
   ul = static_cast<uint64_t>(v);
 }
 
-// Exact keys of rows [0, n) against query heads [h0, h0 + nh), lane-parallel; not for general units. For
+// Exact keys of rows [0, n) (row r at rows + idx[r] * stride, or rows + r * stride without idx) against
+// query heads [h0, h0 + nh), lane-parallel; not for general units. For
 // every live row r, the row's first thread calls emit(r, h, uh, ul) for each head (kMax false), or once
 // with the maximum over the heads (kMax true, h = h0). (uh, ul) is the key as an order-preserving
 // unsigned 128-bit value: for a narrow unit (0, HH with its sign flipped), S = HH 2^56 exactly; otherwise
@@ -311,7 +313,8 @@ __device__ __forceinline__ void ordered(__int128 v, uint64_t& uh, uint64_t& ul) 
 template <typename T, int D, int NT, bool kMax, class Emit>
 __device__ void score_rows(const T* rows, size_t stride, int n, const Frame& f, const int* qh, const int* ql,
                            const int* qmask, int h0, int nh, int& flags,
-                           const uint4 (&cache)[Scorer<T, D, NT>::kVPS], Emit&& emit) {
+                           const uint4 (&cache)[Scorer<T, D, NT>::kVPS], Emit&& emit,
+                           const int* idx = nullptr) {
   using S = Scorer<T, D, NT>;
   constexpr uint64_t kSign = 0x8000000000000000ull;
   const int tid = threadIdx.x, j = tid % S::kSPR;
@@ -321,7 +324,7 @@ __device__ void score_rows(const T* rows, size_t stride, int n, const Frame& f, 
     if (r0 + (tid & ~31) / S::kSPR >= n) break;
     const int r = r0 + tid / S::kSPR;
     const bool live = r < n;
-    const T* src = rows + r * stride + j * kSlice;
+    const T* src = rows + static_cast<size_t>(live && idx ? idx[r] : (live ? r : 0)) * stride + j * kSlice;
     int sh[kSlice];
     uint32_t tm = 0;  // elements of this slice that may have a lower limb
     {
@@ -482,16 +485,18 @@ __device__ void big_dot(const T* q, const T* s, uint32_t (&out)[kBigDigits], int
 // Sign of a - b for two general-path keys.
 __device__ __forceinline__ int big_cmp(const uint32_t* a, const uint32_t* b);
 
-// General-path keys of rows [0, n), written to keys (row r at keys + r * kBigDigits): the maximum over the
-// query heads [h0, h0 + nh) of qg of the exact q_h . s_r. Ends with a barrier.
+// General-path keys of rows [0, n) (row r at rows + idx[r] * stride, or rows + r * stride without idx),
+// written to keys (row r at keys + r * kBigDigits): the maximum over the query heads [h0, h0 + nh) of qg
+// of the exact q_h . s_r. Ends with a barrier.
 template <typename T, int D, int NT>
 __device__ __noinline__ void big_keys(const T* qg, int h0, int nh, const T* rows, size_t stride, int n,
-                                      uint32_t* keys) {
+                                      uint32_t* keys, const int* idx = nullptr) {
   int fl = 0;
   for (int r = threadIdx.x; r < n; r += NT) {
     uint32_t best[kBigDigits], cur[kBigDigits];
+    const T* row = rows + static_cast<size_t>(idx ? idx[r] : r) * stride;
     for (int h = h0; h < h0 + nh; ++h) {
-      big_dot<T, D>(qg + static_cast<size_t>(h) * D, rows + r * stride, cur, fl);
+      big_dot<T, D>(qg + static_cast<size_t>(h) * D, row, cur, fl);
       if (h == h0 || big_cmp(cur, best) > 0)
         for (int i = 0; i < kBigDigits; ++i) best[i] = cur[i];
     }
@@ -680,6 +685,126 @@ __device__ __noinline__ void radix_top_k(const uint64_t* uh, const uint64_t* ul,
   __syncthreads();
 }
 
+// flag[i] = 1 for the k first of n 32-bit keys (the low words of ul) in the order (key desc, index asc);
+// any k. Most significant digit first, 8-bit digits from the highest bit where the keys differ, two
+// histograms in turn (the next one is cleared while the current one is counted): two barriers a digit.
+// Ends with a barrier.
+template <int NT>
+__device__ __noinline__ void radix_top_k32(const uint64_t* ul, int n, int k, int* flag) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  __shared__ int s_hist[2][256];
+  __shared__ uint32_t s_mm[2][NT / 32];
+  __shared__ int s_sel[3];
+  __shared__ int s_wsum[NT / 32];
+  if (k <= 0 || k >= n) {
+    for (int i = tid; i < n; i += NT) flag[i] = k > 0 ? 1 : 0;
+    __syncthreads();
+    return;
+  }
+  auto key = [&](int i) { return static_cast<uint32_t>(ul[i]); };
+  auto above_bits = [](uint32_t x, int s) { return s >= 32 ? 0u : x >> s; };
+  uint32_t mn = 0xFFFFFFFFu, mx = 0u;
+  for (int i = tid; i < n; i += NT) {
+    const uint32_t x = key(i);
+    mn = min(mn, x);
+    mx = max(mx, x);
+  }
+  mn = __reduce_min_sync(kAll, mn);
+  mx = __reduce_max_sync(kAll, mx);
+  if (lane == 0) {
+    s_mm[0][warp] = mn;
+    s_mm[1][warp] = mx;
+  }
+  for (int b = tid; b < 256; b += NT) s_hist[0][b] = 0;
+  __syncthreads();
+  mn = __reduce_min_sync(kAll, lane < NT / 32 ? s_mm[0][lane] : 0xFFFFFFFFu);
+  mx = __reduce_max_sync(kAll, lane < NT / 32 ? s_mm[1][lane] : 0u);
+  if (mn == mx) {  // every key equal: the k lowest indices
+    for (int i = tid; i < n; i += NT) flag[i] = i < k ? 1 : 0;
+    __syncthreads();
+    return;
+  }
+  int pos = 31 - __clz(static_cast<int>(mn ^ mx));
+  uint32_t prefix = above_bits(mx, pos + 1);  // the bits above pos, shared by every key
+  int need = k, buf = 0;
+  bool take_all = false;
+  while (true) {
+    const int width = pos + 1 < 8 ? pos + 1 : 8;
+    const int shift = pos + 1 - width;
+    const int nb = 1 << width;
+    for (int i = tid; i < n; i += NT) {
+      const uint32_t x = key(i);
+      if (above_bits(x, pos + 1) == prefix) atomicAdd(&s_hist[buf][(x >> shift) & (nb - 1)], 1);
+    }
+    for (int b = tid; b < 256; b += NT) s_hist[buf ^ 1][b] = 0;  // read last before the previous barrier
+    __syncthreads();
+    if (warp == 0) {
+      // lane l holds bins nb-1-8l .. nb-8-8l (descending digits)
+      int local = 0;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const int b = nb - 1 - 8 * lane - c;
+        local += b >= 0 ? s_hist[buf][b] : 0;
+      }
+      int incl = local;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(kAll, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const int above = incl - local;
+      if (above < need && need <= incl) {
+        int cum = above;
+        for (int c = 0; c < 8; ++c) {
+          const int b = nb - 1 - 8 * lane - c;
+          const int h = b >= 0 ? s_hist[buf][b] : 0;
+          if (b >= 0 && cum + h >= need) {
+            s_sel[0] = b;
+            s_sel[1] = cum;
+            s_sel[2] = h;
+            break;
+          }
+          cum += h;
+        }
+      }
+    }
+    __syncthreads();
+    const int Dg = s_sel[0], above = s_sel[1], cnt = s_sel[2];
+    need -= above;
+    prefix = (prefix << width) | static_cast<uint32_t>(Dg);
+    pos = shift - 1;
+    buf ^= 1;
+    if (cnt == need) {
+      take_all = true;
+      break;
+    }
+    if (pos < 0) break;
+  }
+  // prefix: the bits above pos of the k-th key. Keys above it are in, keys below it are out; keys equal
+  // to it are all in (take_all) or, at full depth, the `need` lowest indices among them.
+  if (take_all) {
+    for (int i = tid; i < n; i += NT) flag[i] = above_bits(key(i), pos + 1) >= prefix ? 1 : 0;
+    __syncthreads();
+    return;
+  }
+  const int per = (n + NT - 1) / NT;
+  const int i0 = min(n, tid * per), i1 = min(n, i0 + per);
+  int eq = 0;
+  for (int i = i0; i < i1; ++i) eq += key(i) == prefix;
+  int total;
+  int rank = block_excl_scan<NT>(eq, &total, s_wsum);
+  for (int i = i0; i < i1; ++i) {
+    const uint32_t x = key(i);
+    if (x == prefix) {
+      flag[i] = rank < need ? 1 : 0;
+      ++rank;
+    } else {
+      flag[i] = x > prefix ? 1 : 0;
+    }
+  }
+  __syncthreads();
+}
+
 // flag[i] = 1 for the k first keys in the order (key desc, index asc), keys given as order-preserving
 // unsigned 128-bit values (uh, ul) in shared memory; wide = false when every uh is 0. 0 <= k, n >= 1.
 template <int NT>
@@ -727,15 +852,18 @@ __device__ void rank_select(const uint64_t* uh, const uint64_t* ul, int n, int k
 // estimated in fp32 with an enclosure that provably contains the exact value; when every selected key's
 // lower bound exceeds every other key's upper bound, the fp32 selection is the exact selection.
 //
-// Error bound. A thread sums its 16 products with fused multiply-adds (each product enters exactly;
-// one rounding per add) and the row's slices are added in a 3-level (D = 128) or 2-level (D = 64)
-// shuffle tree: every term passes through at most 20 roundings. With u = 2^-24 and the underflow model
-// fl(x) = x (1 + d) + e, |d| <= u, |e| <= 2^-150, the computed sum a and the computed absolute sum B
-// (the same tree over |q_t| |s_t|) satisfy |a - q.s| <= g (sum |q_t s_t|) + 2^-142 and
-// sum |q_t s_t| <= (B + 2^-142) / (1 - g), g = 20 u / (1 - 20 u) (at most 128 adds contribute e). So
-// eps = 21 u B + 2^-141 bounds the error, and [a - eps, a + eps] (rounded outward) encloses q . s. The
-// maximum over the group's heads is enclosed by the maxima of the bounds. A non-finite estimate (an
-// overflow, or a non-finite input) gets (-inf, +inf), which no certificate accepts.
+// Error bound (a running bound). A lane sums its 16 or 32 products with fused multiply-adds, and the
+// row's slices are added in a shuffle tree of at most 3 levels: at most 135 operations, each
+// rounding its exact result once to nearest. Such a rounding changes a result r by at most u |r| + 2^-126
+// (u = 2^-24; the second term covers a subnormal result, rounded or flushed to zero), and the errors of
+// the operations add up without amplification (every operation takes the previous results as they are),
+// so the computed sum a satisfies |a - q.s| <= u R + 2^-118, R = the sum of |r| over every operation that
+// led to a. Each lane accumulates R with upward rounding next to its sums (the tree adds the partner's R
+// and the new |r|), so the computed R is at least the true one, and eps = u R + 2^-118 rounded up bounds
+// the error:
+// [a - eps, a + eps] (rounded outward) encloses q . s. The maximum over the group's heads is enclosed
+// by the maxima of the bounds. A non-finite estimate or R (an overflow, or a non-finite input) gets
+// (-inf, +inf), which no certificate accepts.
 
 __device__ __forceinline__ uint32_t order_bits(float x) {  // order-preserving for finite values and infinities
   const uint32_t b = __float_as_uint(x);
@@ -745,93 +873,178 @@ __device__ __forceinline__ float from_order_bits(uint32_t o) {
   return __uint_as_float((o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o);
 }
 
-// fp32 estimates of every row's key with enclosures, lane-parallel like score_rows: for every live row r,
-// the row's first thread calls emit(r, h, mid, lo, hi) for each head of [h0, h0 + nh) (kMax false), or
-// once with the maxima over the heads (kMax true, h = h0). lo <= exact q.s <= hi; a non-finite estimate
-// gives (-inf, +inf). Every thread calls it. Heads go in chunks whose query loads are issued together.
-template <typename T, int D, int NT, bool kMax, class Emit>
-__device__ void estimate_rows(const T* qg, int h0, int nh, const T* rows, size_t stride, int n, Emit&& emit) {
-  using S = Scorer<T, D, NT>;
-  constexpr int HC = 8 / S::kVPS;                 // heads per chunk: 4 (bf16) or 2 (f32), 8 query vectors
-  constexpr float kEpsRel = 21.0f / 16777216.0f;  // 21 u, exact in fp32
-  const float kEpsAbs = __uint_as_float(0x09000000u);  // 2^-141
+// Shapes of the estimate for a CTA of NT threads when a lane takes ES consecutive elements of a row.
+template <typename T, int D, int NT, int ES>
+struct EstShape {
+  static constexpr int kEPV = 16 / static_cast<int>(sizeof(T));  // elements per 16-byte word
+  static constexpr int kSPR = D / ES;                            // lanes per row
+  static constexpr int kRPP = NT / kSPR;                         // rows per pass
+  static constexpr int kVPS = ES / kEPV;                         // words per lane and row
+  static_assert(D % ES == 0 && 32 % kSPR == 0 && kSPR >= 4 && ES % kEPV == 0, "estimate layout");
+};
+
+// The group's queries qg [G][D] in shared memory for estimate_rows, in their own type: qs holds G * D
+// values, head h's lane-j slice as kVPS 16-byte words at ((h * kVPS + v) * kSPR + j), so that the lanes
+// of a row read consecutive words. Ends with a barrier.
+template <typename T, int D, int NT, int ES>
+__device__ void load_q_table(const T* qg, int G, uint4* qs) {
+  using S = EstShape<T, D, NT, ES>;
+  for (int vi = threadIdx.x; vi < G * D / S::kEPV; vi += NT) {
+    const int h = vi / (D / S::kEPV), c = vi % (D / S::kEPV);  // word c of head h's row
+    qs[(h * S::kVPS + c % S::kVPS) * S::kSPR + c / S::kVPS] = reinterpret_cast<const uint4*>(qg)[vi];
+  }
+  __syncthreads();
+}
+
+// fp32 estimates of every row's key with enclosures, lane-parallel (ES elements of a row per lane, the
+// lanes of a row consecutive in one warp): for every live row r, the row's first lane calls
+// emit(r, h, mid, lo, hi) for each head of [h0, h0 + nh) (kMax false), or once with the maxima over the
+// heads (kMax true, h = h0). lo <= exact q.s <= hi; a non-finite estimate gives (-inf, +inf). The
+// queries come from load_q_table's table qs, which is built first when qg is not null (the first pass's
+// row loads are issued before it, so both latencies overlap). A pass takes kRPP rows; with ES = 16 the
+// next pass's row slices are loaded while the current pass computes. Every thread calls it.
+//
+// With kMax the slices of a row are summed in a transposed tree: at each of the first two levels a lane
+// keeps half of its heads and sends the other half to its partner, which keeps those, so that the lanes
+// finish with one head each (two lanes per head when kSPR = 8); the maximum over the heads then takes
+// two more levels.
+template <typename T, int D, int NT, bool kMax, int ES, class Emit>
+__device__ void estimate_rows(const T* qg, int G, uint4* qs, int h0, int nh, const T* rows, size_t stride, int n,
+                              Emit&& emit) {
+  using S = EstShape<T, D, NT, ES>;
+  constexpr int HC = 4;                                // heads per chunk
+  constexpr bool kDB = ES == 16;                       // double-buffered row slices
+  constexpr float kU = 1.0f / 16777216.0f;             // u = 2^-24
+  const float kEpsAbs = __uint_as_float(0x04800000u);  // 2^-118 >= 256 operations x 2^-126
   const int tid = threadIdx.x, j = tid % S::kSPR;
+  auto load_slice = [&](int r, uint4 (&w)[S::kVPS]) {
+    const uint4* src = reinterpret_cast<const uint4*>(rows + static_cast<size_t>(r < n ? r : 0) * stride + j * ES);
+#pragma unroll
+    for (int c = 0; c < S::kVPS; ++c) w[c] = r < n ? src[c] : make_uint4(0, 0, 0, 0);
+  };
+  uint4 sw[S::kVPS];
+  load_slice(tid / S::kSPR, sw);
+  if (qg) load_q_table<T, D, NT, ES>(qg, G, qs);
   for (int r0 = 0; r0 < n; r0 += S::kRPP) {
     if (r0 + (tid & ~31) / S::kSPR >= n) break;  // warp-uniform: no row of this warp is left
     const int r = r0 + tid / S::kSPR;
     const bool live = r < n;
-    uint4 sw[S::kVPS];
-    {
-      const uint4* src = reinterpret_cast<const uint4*>(rows + (live ? r : 0) * stride + j * kSlice);
+    if (!kDB && r0 > 0) load_slice(r, sw);
+    uint4 nx[kDB ? S::kVPS : 1];  // the next pass's slice, in flight during this one
+    if constexpr (kDB) load_slice(r + S::kRPP, nx);
+    float xs[ES];
 #pragma unroll
-      for (int c = 0; c < S::kVPS; ++c) sw[c] = live ? src[c] : make_uint4(0, 0, 0, 0);
-    }
-    float best_mid = 0.f, best_lo = 0.f, best_hi = 0.f;
+    for (int c = 0; c < S::kVPS; ++c)
+#pragma unroll
+      for (int e = 0; e < S::kEPV; ++e) xs[c * S::kEPV + e] = as_f32<T>(elem_bits<T>(sw[c], e));
+    float best_mid = -INFINITY, best_lo = -INFINITY, best_hi = -INFINITY;
     bool bad = false;
     for (int hb = 0; hb < nh; hb += HC) {
-      uint4 qw[HC][S::kVPS];
-#pragma unroll
-      for (int c = 0; c < HC; ++c)
-#pragma unroll
-        for (int v = 0; v < S::kVPS; ++v)
-          qw[c][v] = hb + c < nh ? reinterpret_cast<const uint4*>(qg + static_cast<size_t>(h0 + hb + c) * D +
-                                                                  j * kSlice)[v]
-                                 : make_uint4(0, 0, 0, 0);
-      float acc[HC], ab[HC];
+      float acc[HC], rb[HC];  // the sum, and the running bound R (rounded up)
 #pragma unroll
       for (int c = 0; c < HC; ++c) {
         acc[c] = 0.f;
-        ab[c] = 0.f;
+        rb[c] = 0.f;
+        if (hb + c < nh) {
 #pragma unroll
-        for (int v = 0; v < S::kVPS; ++v)
+          for (int v = 0; v < S::kVPS; ++v) {
+            const uint4 qw = qs[((h0 + hb + c) * S::kVPS + v) * S::kSPR + j];
 #pragma unroll
-          for (int e = 0; e < S::kEPV; ++e) {
-            const float qv = as_f32<T>(elem_bits<T>(qw[c][v], e)), x = as_f32<T>(elem_bits<T>(sw[v], e));
-            acc[c] = __fmaf_rn(qv, x, acc[c]);
-            ab[c] = __fmaf_rn(fabsf(qv), fabsf(x), ab[c]);
+            for (int e = 0; e < S::kEPV; ++e) {
+              acc[c] = __fmaf_rn(as_f32<T>(elem_bits<T>(qw, e)), xs[v * S::kEPV + e], acc[c]);
+              rb[c] = __fadd_ru(rb[c], fabsf(acc[c]));
+            }
           }
+        }
       }
+      if constexpr (kMax) {
+        // transposed tree: after the first two levels lane j holds head c1 = 2 * b2 + b1 (b2 = bit
+        // kSPR/2 of j, b1 = the next lower bit), summed over the lanes that differ in those bits
+        constexpr int o2 = S::kSPR / 2, o1 = S::kSPR / 4;
+        const bool up2 = (j & o2) != 0, up1 = (j & o1) != 0;
+        float a2[2], r2[2];
 #pragma unroll
-      for (int o = S::kSPR / 2; o > 0; o >>= 1)
+        for (int i = 0; i < 2; ++i) {  // keep heads 2 up2 + i, send heads 2 (1 - up2) + i
+          const float sa = up2 ? acc[i] : acc[2 + i], sr = up2 ? rb[i] : rb[2 + i];
+          const float ka = up2 ? acc[2 + i] : acc[i], kr = up2 ? rb[2 + i] : rb[i];
+          a2[i] = __fadd_rn(ka, __shfl_xor_sync(kAll, sa, o2));
+          r2[i] = __fadd_ru(__fadd_ru(kr, __shfl_xor_sync(kAll, sr, o2)), fabsf(a2[i]));
+        }
+        float a1, r1;
+        {
+          const float sa = up1 ? a2[0] : a2[1], sr = up1 ? r2[0] : r2[1];
+          const float ka = up1 ? a2[1] : a2[0], kr = up1 ? r2[1] : r2[0];
+          a1 = __fadd_rn(ka, __shfl_xor_sync(kAll, sa, o1));
+          r1 = __fadd_ru(__fadd_ru(kr, __shfl_xor_sync(kAll, sr, o1)), fabsf(a1));
+        }
+#pragma unroll
+        for (int o = S::kSPR / 8; o > 0; o >>= 1) {  // the lanes that still hold the same head (kSPR = 8)
+          a1 = __fadd_rn(a1, __shfl_xor_sync(kAll, a1, o));
+          r1 = __fadd_ru(__fadd_ru(r1, __shfl_xor_sync(kAll, r1, o)), fabsf(a1));
+        }
+        const int c1 = (up2 ? 2 : 0) + (up1 ? 1 : 0);
+        float mid = a1, lo, hi;
+        {
+          const float eps = __fmaf_ru(kU, r1, kEpsAbs);
+          lo = __fsub_rd(a1, eps);
+          hi = __fadd_ru(a1, eps);
+          if (!isfinite(a1) || !isfinite(eps)) {
+            lo = -INFINITY;
+            hi = INFINITY;
+            bad = true;
+          }
+          if (hb + c1 >= nh) mid = lo = hi = -INFINITY;  // a head past the group: not in the maximum
+        }
+#pragma unroll
+        for (int o = o1; o <= o2; o <<= 1) {
+          mid = fmaxf(mid, __shfl_xor_sync(kAll, mid, o));
+          lo = fmaxf(lo, __shfl_xor_sync(kAll, lo, o));
+          hi = fmaxf(hi, __shfl_xor_sync(kAll, hi, o));
+        }
+        best_mid = fmaxf(best_mid, mid);
+        best_lo = fmaxf(best_lo, lo);
+        best_hi = fmaxf(best_hi, hi);
+      } else {
+#pragma unroll
+        for (int o = S::kSPR / 2; o > 0; o >>= 1)
+#pragma unroll
+          for (int c = 0; c < HC; ++c) {
+            if (hb + c >= nh) continue;
+            acc[c] = __fadd_rn(acc[c], __shfl_xor_sync(kAll, acc[c], o));
+            rb[c] = __fadd_ru(__fadd_ru(rb[c], __shfl_xor_sync(kAll, rb[c], o)), fabsf(acc[c]));
+          }
 #pragma unroll
         for (int c = 0; c < HC; ++c) {
-          acc[c] = __fadd_rn(acc[c], __shfl_xor_sync(kAll, acc[c], o));
-          ab[c] = __fadd_rn(ab[c], __shfl_xor_sync(kAll, ab[c], o));
-        }
-#pragma unroll
-      for (int c = 0; c < HC; ++c) {
-        if (hb + c >= nh) continue;
-        const float eps = __fmaf_ru(kEpsRel, ab[c], kEpsAbs);
-        float lo = __fsub_rd(acc[c], eps), hi = __fadd_ru(acc[c], eps);
-        if (!isfinite(acc[c]) || !isfinite(eps)) {
-          lo = -INFINITY;
-          hi = INFINITY;
-          bad = true;
-        }
-        if constexpr (kMax) {
-          const bool first = hb + c == 0;
-          best_mid = first ? acc[c] : fmaxf(best_mid, acc[c]);
-          best_lo = first ? lo : fmaxf(best_lo, lo);
-          best_hi = first ? hi : fmaxf(best_hi, hi);
-        } else {
+          if (hb + c >= nh) continue;
+          const float eps = __fmaf_ru(kU, rb[c], kEpsAbs);
+          float lo = __fsub_rd(acc[c], eps), hi = __fadd_ru(acc[c], eps);
+          if (!isfinite(acc[c]) || !isfinite(eps)) {
+            lo = -INFINITY;
+            hi = INFINITY;
+          }
           if (j == 0 && live) emit(r, h0 + hb + c, acc[c], lo, hi);
         }
       }
     }
     if constexpr (kMax) {
+      bad = __any_sync(kAll, bad);  // any head of the row (lanes of other rows only widen it: no harm)
       if (j == 0 && live) emit(r, h0, best_mid, bad ? -INFINITY : best_lo, bad ? INFINITY : best_hi);
+    }
+    if constexpr (kDB) {
+#pragma unroll
+      for (int c = 0; c < S::kVPS; ++c) sw[c] = nx[c];
     }
   }
 }
 
 // The top-k of the estimates (ties to the lower index) and its certificate: true when every enclosure is
-// finite and min lo over the selected > max hi over the others; flag then holds the exact selection.
-// ul [n] holds order_bits(mid) (uh [n] zero, used for n above the counting limit), written before a
-// barrier. Block-wide; every thread gets the answer. red: shared [3 * NT/32], not used by the caller
-// until its next barrier.
+// finite and Lb = min lo over the selected > Hb = max hi over the others; flag then holds the exact
+// selection. ul [n] holds order_bits(mid) (uh [n] zero), written before a barrier. Block-wide; every
+// thread gets the answer and (Lb, Hb) (NaN for an empty side). red: shared [3 * NT/32], not used by the
+// caller until its next barrier.
 template <int NT>
 __device__ bool certify_top_k(const float* lo, const float* hi, int n, int k, const uint64_t* uh,
-                              const uint64_t* ul, int* flag, uint32_t* red) {
+                              const uint64_t* ul, int* flag, uint32_t* red, float& Lb, float& Hb) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   uint32_t L = 0xFFFFFFFFu, H = 0u, bad = 0u;  // min lo over the selected, max hi over the rest (order bits)
   if (n <= kRadixMinN) {
@@ -861,7 +1074,7 @@ __device__ bool certify_top_k(const float* lo, const float* hi, int n, int k, co
       }
     }
   } else {
-    rank_select<NT>(uh, ul, n, k, false, flag);
+    radix_top_k32<NT>(ul, n, k, flag);
     for (int i = tid; i < n; i += NT) {
       const float l = lo[i], h = hi[i];
       bad |= !(isfinite(l) && isfinite(h));
@@ -885,9 +1098,83 @@ __device__ bool certify_top_k(const float* lo, const float* hi, int n, int k, co
   bad = __reduce_or_sync(kAll, lane < NT / 32 ? red[2 * (NT / 32) + lane] : 0u);
   // k = 0 or k >= n: every flag is already exact; a non-finite input still goes to the exact path
   // (which reports it)
+  Lb = L == 0xFFFFFFFFu ? __uint_as_float(0x7FC00000u) : from_order_bits(L);
+  Hb = H == 0u ? __uint_as_float(0x7FC00000u) : from_order_bits(H);
   if (bad) return false;
   if (k <= 0 || k >= n) return true;
-  return from_order_bits(L) > from_order_bits(H);  // a float comparison: -0 and +0 do not separate
+  return Lb > Hb;  // a float comparison: -0 and +0 do not separate
+}
+
+
+// After a failed certificate: the exact top-k from the exact keys of the uncertain segments only. Lb and
+// Hb are certify_top_k's bounds (min lo over the provisional top-k, max hi over the rest).
+// - A provisional member with lo > Hb has a key above every non-member's, so fewer than k segments can
+//   beat it: it stays in.
+// - A non-member with hi < Lb is beaten by all k members: it stays out.
+// - The rest U (ascending; every non-finite enclosure is in it) is ranked by exact key within U, ties to
+//   the lower index, and its first r = k - (members that stay in) are in. A member of U outranked within
+//   U by r others is out: those r have keys above Hb, so they are provisional members, of which U holds
+//   exactly r with itself among them, a contradiction unless all k - r stayers outrank it too.
+// Returns the unit flags the exact keys raised (kFlagNonFinite, kFlagDeep). Scratch: ulist, uflag [n]
+// ints (they may alias lo and hi: those are last read before the first barrier); the keys kh, kl [n];
+// the q limb tables qh, ql, qmask; red [4 * NT/32]; s_flags; big (n * kBigDigits words, global).
+// kMax: the key of a row is the maximum over heads [h0, h0 + nh) (else nh = 1). Block-wide; ends with a
+// barrier after flag is final.
+template <typename T, int D, int NT, bool kMax>
+__device__ __noinline__ int resolve_top_k(const T* qg, int G, int h0, int nh, const T* rows, size_t stride,
+                                          int n, int k, const float* lo, const float* hi, float Lb, float Hb,
+                                          int* flag, int* ulist, int* uflag, uint64_t* kh, uint64_t* kl, int* qh,
+                                          int* ql, int* qmask, uint32_t* red, int* s_flags, uint32_t* big) {
+  using S = Scorer<T, D, NT>;
+  __shared__ int s_wsum[NT / 32];
+  const int tid = threadIdx.x;
+  if (tid == 0) *s_flags = 0;
+  // 1. the uncertain segments, and the members that stay in; a contiguous slice per thread (<= 32)
+  const int per = (n + NT - 1) / NT;
+  const int i0 = min(n, tid * per), i1 = min(n, i0 + per);
+  uint32_t um = 0u;
+  int stay = 0;
+  for (int i = i0; i < i1; ++i) {
+    const float l = lo[i], h = hi[i];
+    const bool in = flag[i] != 0;
+    const bool unc = !(isfinite(l) && isfinite(h)) || (in ? l <= Hb : h >= Lb);
+    um |= (unc ? 1u : 0u) << (i - i0);
+    stay += in && !unc;
+  }
+  int total;
+  int pos = block_excl_scan<NT>(__popc(um) | (stay << 16), &total, s_wsum) & 0xFFFF;  // n < 2^16
+  const int m = total & 0xFFFF, r = k - (total >> 16);
+  for (int i = i0; i < i1; ++i)
+    if ((um >> (i - i0)) & 1u) ulist[pos++] = i;
+  __syncthreads();
+  // 2. exact keys of U's rows in a frame of their own (keys of U compare exactly with one another)
+  int fl = 0;
+  uint4 cache[S::kVPS];
+  const Frame fr = unit_frame<T, D, NT>(qg, G, rows, stride, m, red, qmask, fl, cache, ulist);
+  if (!fr.general) {
+    load_q_limbs<T, D, NT>(qg, G, fr, qh, ql, qmask, fl);
+    score_rows<T, D, NT, kMax>(
+        rows, stride, m, fr, qh, ql, qmask, h0, nh, fl, cache,
+        [&](int j, int, uint64_t uh, uint64_t ulw) {
+          kh[j] = uh;
+          kl[j] = ulw;
+        },
+        ulist);
+  }
+  if (fl) atomicOr(s_flags, fl);
+  __syncthreads();
+  const int uflags = *s_flags;
+  // 3. the first r of U
+  if (fr.general || (uflags & kFlagDeep)) {
+    big_keys<T, D, NT>(qg, h0, nh, rows, stride, m, big, ulist);
+    big_rank_select<NT>(big, m, r, uflag);
+    __syncthreads();
+  } else {
+    rank_select<NT>(kh, kl, m, r, !fr.narrow, uflag);
+  }
+  for (int j = tid; j < m; j += NT) flag[ulist[j]] = uflag[j];
+  __syncthreads();
+  return uflags;
 }
 
 }  // namespace xk

@@ -190,52 +190,21 @@ __device__ void add_sink_range(const StepArgs& a, int u, int Ns, int32_t* rg, in
   }
 }
 
-// Shared memory: the exact-key scorer's query limb tables | key high words [n_max + 4] u64 | key low
-//   words [n_max + 4] u64 | flag [n_max + 2] | bounds [n_max + 1] | list [n_max] | runs_s [n_max] | runs_e [n_max]
-//   | fp32 enclosures lo, hi [n_max] each
+// Shared memory: the exact-key scorer's query limb tables | the query table [G * D] | key high words
+//   [n_max + 4] u64 | key low words [n_max + 4] u64 | flag [n_max + 2] | bounds [n_max + 1] | list [n_max] |
+//   runs_s [n_max] | runs_e [n_max] | fp32 enclosures lo, hi [n_max] each
 template <typename T, int D>
 struct SelectLayout {
   using SC = xk::Scorer<T, D, kSelectThreads>;
-  __host__ __device__ static constexpr size_t q_bytes(int G) { return (SC::smem_bytes(G) + 15) / 16 * 16; }
+  __host__ __device__ static constexpr size_t limb_bytes(int G) { return (SC::smem_bytes(G) + 15) / 16 * 16; }
+  __host__ __device__ static constexpr size_t q_bytes(int G) {
+    return limb_bytes(G) + sizeof(T) * static_cast<size_t>(G) * D;
+  }
   __host__ __device__ static constexpr size_t bytes(int G, int n_max) {
     return q_bytes(G) + 2 * sizeof(uint64_t) * (static_cast<size_t>(n_max) + 4) +
            sizeof(int) * (5 * static_cast<size_t>(n_max) + 3) + 2 * sizeof(float) * static_cast<size_t>(n_max);
   }
 };
-
-// The exact top-k of one unit (every thread of the select CTA calls it), for units whose fp32 enclosures
-// do not separate at the k boundary: exact integer keys (the general 640-bit path where a value lies far
-// below its side's largest or is not finite), then the exact ranking into flag. Shared-memory scratch:
-// the query limb tables qh, ql, qtail, the keys kh, kl, the unit flags word and red.
-template <typename T, int D>
-__device__ __noinline__ void exact_select(const StepArgs& a, int u, const T* qg, const T* rows, size_t stride,
-                                          int n, int k, int* qh, int* ql, int* qtail, uint64_t* kh, uint64_t* kl,
-                                          int* flag, int* s_flags, uint32_t* s_red) {
-  using SC = xk::Scorer<T, D, kSelectThreads>;
-  const int G = a.G;
-  int fl = 0;
-  uint4 cache[SC::kVPS];
-  const xk::Frame fr = xk::unit_frame<T, D, kSelectThreads>(qg, G, rows, stride, n, s_red, qtail, fl, cache);
-  if (!fr.general) {
-    xk::load_q_limbs<T, D, kSelectThreads>(qg, G, fr, qh, ql, qtail, fl);
-    xk::score_rows<T, D, kSelectThreads, true>(rows, stride, n, fr, qh, ql, qtail, 0, G, fl, cache,
-                                                 [&](int r, int, uint64_t uh, uint64_t ul) {
-                                                   kh[r] = uh;
-                                                   kl[r] = ul;
-                                                 });
-  }
-  if (fl) atomicOr(s_flags, fl);
-  __syncthreads();
-  const int uflags = *s_flags;
-  if ((uflags & xk::kFlagNonFinite) && threadIdx.x == 0) atomicOr(a.err, kErrNonFinite);
-  if (fr.general || (uflags & xk::kFlagDeep)) {
-    uint32_t* big = a.bigkeys + static_cast<size_t>(u) * a.n_max * xk::kBigDigits;
-    xk::big_keys<T, D, kSelectThreads>(qg, 0, G, rows, stride, n, big);
-    xk::big_rank_select<kSelectThreads>(big, n, k, flag);
-  } else {
-    xk::rank_select<kSelectThreads>(kh, kl, n, k, !fr.narrow, flag);
-  }
-}
 
 // 80 registers per thread (no spills): a select CTA then leaves room on its SM for an attend CTA of
 // the same layer, which launches early and waits (programmatic dependent launch).
@@ -250,6 +219,7 @@ __global__ void __maxnreg__(80) zr_select_kernel(StepArgs a) {
   int* qh = reinterpret_cast<int*>(smem_raw);
   int* ql = qh + G * SC::kQRow;
   int* qtail = ql + G * SC::kQRow;
+  uint4* qtab = reinterpret_cast<uint4*>(smem_raw + LY::limb_bytes(G));
   uint64_t* kh = reinterpret_cast<uint64_t*>(smem_raw + LY::q_bytes(G));
   uint64_t* kl = kh + nmax + 4;
   int* flag = reinterpret_cast<int*>(kl + nmax + 4);
@@ -272,7 +242,6 @@ __global__ void __maxnreg__(80) zr_select_kernel(StepArgs a) {
   const int k = a.meta.topk[b];
   const int Ns = a.meta.prompt_lens[b];
   for (int i = tid; i <= n; i += blockDim.x) bnd[i] = a.meta.seg_bounds[s0 + b + i];
-  if (tid == 0) s_flags = 0;
   const T* qg = static_cast<const T*>(a.q) + (static_cast<size_t>(b) * a.Hq + static_cast<size_t>(g) * G) * D;
   const T* rows = static_cast<const T*>(a.sum_k) + (static_cast<size_t>(s0) * a.Hkv + g) * D;
   const size_t stride = static_cast<size_t>(a.Hkv) * D;
@@ -291,22 +260,32 @@ __global__ void __maxnreg__(80) zr_select_kernel(StepArgs a) {
 
   // 1. ranking key: max over the group of the exact dot q_h . s_i. First an fp32 estimate of every key
   //    with an enclosure of the exact value (lane-parallel fused multiply-adds).
-  xk::estimate_rows<T, D, kSelectThreads, true>(qg, 0, G, rows, stride, n,
-                                                [&](int r, int, float mid, float lo, float hi) {
-                                                  kh[r] = 0;
-                                                  kl[r] = xk::order_bits(mid);
-                                                  elo[r] = lo;
-                                                  ehi[r] = hi;
-                                                });
+  {
+    auto emit = [&](int r, int, float mid, float lo, float hi) {
+      kh[r] = 0;
+      kl[r] = xk::order_bits(mid);
+      elo[r] = lo;
+      ehi[r] = hi;
+    };
+    // 16 elements a lane (64 rows a pass), or 32 (128 rows a pass) when that saves a pass
+    if (D == 128 && n > xk::EstShape<T, D, kSelectThreads, 16>::kRPP)
+      xk::estimate_rows<T, D, kSelectThreads, true, D == 128 ? 32 : 16>(qg, G, qtab, 0, G, rows, stride, n, emit);
+    else
+      xk::estimate_rows<T, D, kSelectThreads, true, 16>(qg, G, qtab, 0, G, rows, stride, n, emit);
+  }
   __syncthreads();
 
   // 2. top-k: segment i is selected iff fewer than k segments beat it (a greater exact key, or an equal
   //    key and a lower index). The top-k of the estimates is the exact one when its certificate holds
-  //    (the enclosures separate at the k boundary); otherwise the keys are computed exactly.
-  // (certify_top_k ends with a barrier after its flags are written; the exact path needs one more)
-  if (!xk::certify_top_k<kSelectThreads>(elo, ehi, n, k, kh, kl, flag, s_cert)) {
-    exact_select<T, D>(a, u, qg, rows, stride, n, k, qh, ql, qtail, kh, kl, flag, &s_flags, s_red);
-    __syncthreads();
+  //    (the enclosures separate at the k boundary); otherwise the uncertain segments' keys are computed
+  //    exactly. (certify_top_k and resolve_top_k end with a barrier after the flags are written.)
+  float cert_lo, cert_hi;
+  if (!xk::certify_top_k<kSelectThreads>(elo, ehi, n, k, kh, kl, flag, s_cert, cert_lo, cert_hi)) {
+    const int uflags = xk::resolve_top_k<T, D, kSelectThreads, true>(
+        qg, G, 0, G, rows, stride, n, k, elo, ehi, cert_lo, cert_hi, flag, reinterpret_cast<int*>(elo),
+        reinterpret_cast<int*>(ehi), kh, kl, qh, ql, qtail, s_red, &s_flags,
+        a.bigkeys + static_cast<size_t>(u) * nmax * xk::kBigDigits);
+    if ((uflags & xk::kFlagNonFinite) && tid == 0) atomicOr(a.err, kErrNonFinite);
   }
 
   // 3. the selected list (ascending), the summary list (the rest, ascending), the maximal runs of
