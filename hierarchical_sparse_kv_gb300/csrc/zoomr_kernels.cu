@@ -772,6 +772,20 @@ constexpr size_t attend_ring_bytes() {
 __device__ __forceinline__ void cp_async16(uint32_t smem_dst, const void* gsrc, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_dst), "l"(gsrc), "r"(src_bytes) : "memory");
 }
+// The same copy with an L2 eviction policy (createpolicy): the streamed K/V rows are read once per
+// layer, so they are marked to leave L2 first, and the kernels' code, the metadata and the partials
+// of the step stay resident.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ void cp_async16_stream(uint32_t smem_dst, const void* gsrc, uint32_t src_bytes,
+                                                  uint64_t pol) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;" ::"r"(smem_dst), "l"(gsrc),
+               "r"(src_bytes), "l"(pol)
+               : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
@@ -796,6 +810,7 @@ struct LoadBases {
   const char* vp;
   const char* sk;
   const char* sv;
+  uint64_t pol;  // L2 policy of the pool rows (evict first)
 };
 
 // Stage the 16 K rows and 16 V rows of tile t0. Every cp.async instruction moves whole rows
@@ -817,8 +832,8 @@ __device__ __forceinline__ void mma_issue_tile(uint32_t stage, const uint32_t* t
     const size_t off = static_cast<size_t>(ok ? (id & ~kSummaryFlag) : 0u) * (D * 2);
     const uint32_t bytes = ok ? 16u : 0u;
     const uint32_t dst = stage + row * RB + ch * 16;
-    cp_async16(dst, (is_sum ? lb.sk : lb.kp) + off, bytes);
-    cp_async16(dst + 16 * RB, (is_sum ? lb.sv : lb.vp) + off, bytes);
+    cp_async16_stream(dst, (is_sum ? lb.sk : lb.kp) + off, bytes, lb.pol);
+    cp_async16_stream(dst + 16 * RB, (is_sum ? lb.sv : lb.vp) + off, bytes, lb.pol);
   }
 }
 
@@ -967,7 +982,8 @@ __global__ void __launch_bounds__(kAttendWarps * 32, 3) zr_attend_mma_kernel(Ste
   wk.ring = static_cast<uint32_t>(__cvta_generic_to_shared(attend_smem)) + warp * kStages * MmaWorker<D>::kStageBytes;
   const int chunk_off = (lane % (D / 8)) * 16;
   wk.lb = LoadBases{static_cast<const char*>(a.k_pool) + chunk_off, static_cast<const char*>(a.v_pool) + chunk_off,
-                    static_cast<const char*>(a.sum_k) + chunk_off, static_cast<const char*>(a.sum_v) + chunk_off};
+                    static_cast<const char*>(a.sum_k) + chunk_off, static_cast<const char*>(a.sum_v) + chunk_off,
+                    l2_evict_first_policy()};
   attend_balanced(a, stage_unit_rows(a, s_rows), wk, rowtab[warp], warp, lane);
 }
 
