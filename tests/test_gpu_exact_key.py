@@ -5,7 +5,8 @@ Importance Scoring and Voting"). These cases are built so that only exact arithm
 oracle's selection:
 
 * near-ties planted at the top-k boundary where an ascending fp32 chain ranks the pair the
-  other way (bf16 on the 8 x 4K workload; fp32 on a small shape);
+  other way (bf16 on the 8 x 4K workload; fp32 on a small shape; bf16 and fp32 with 64 to 128
+  segments per sequence, where the estimate takes 32 elements a lane);
 * ties decided by one tiny value: a lower limb (about 2^-30 below the largest), a value below
   the 56-bit frame (the general 640-bit path), a subnormal, and the same on the query side;
 * segment counts where the top-k is a radix select (300, 2048 and 4096 segments), with random
@@ -54,10 +55,17 @@ def _fp32_chain_sel(st, lt, b, g):
 
 @pytest.mark.parametrize("spec", [W.WORKLOADS[1],
                                   W.small_spec(dtype="f32", head_dim=64, batch=3, num_q_heads=8, num_kv_heads=2,
-                                               seq_len=1500, seg_len_range=(20, 60), topk=5, window=32, seed=21)],
-                         ids=["bf16_8x4K", "f32_small"])
+                                               seq_len=1500, seg_len_range=(20, 60), topk=5, window=32, seed=21),
+                                  # 64 < n <= 128 segments: the estimate takes 32 elements a lane (one pass)
+                                  W.small_spec(dtype="bf16", head_dim=128, batch=4, num_q_heads=16, num_kv_heads=4,
+                                               seq_len=3000, seg_len_range=(20, 40), topk=9, window=40, seed=23),
+                                  W.small_spec(dtype="f32", head_dim=128, batch=3, num_q_heads=8, num_kv_heads=2,
+                                               seq_len=3000, seg_len_range=(20, 40), topk=9, window=40, seed=24)],
+                         ids=["bf16_8x4K", "f32_small", "bf16_n100", "f32_d128_n100"])
 def test_planted_near_ties_follow_the_exact_order(spec):
     st, lt = _layer(spec)
+    if spec.seg_len_range == (20, 40):
+        assert all(64 < st.num_segments(b) <= 128 for b in range(st.batch))
     flips = NT.plant_near_ties(st, lt)
     assert len(flips) >= 4, flips
     r = C.parity(st, lt)
