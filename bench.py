@@ -1026,15 +1026,15 @@ def run_consensus(args):
 
 # ---------------------------------------------------------------------- offloaded cache, staged per layer
 OFFLOAD_METRIC = ("ZoomR decode steps/s, 512-token prompt + 16K generated, batch 8, 32 layers, every layer's K/V in "
-                  "pinned host memory: per layer the final context's blocks are staged into HBM over the CPU-GPU link "
+                  "pinned host memory: per layer the final context's rows are staged into HBM over the CPU-GPU link "
                   "(the next layer's while the current one attends); link GB/s vs the measured copy bandwidth")
 
 
 def run_offload(args):
     """The pages' offloaded decode (ZoomR 3.4, "Decoding Stage"): the cache in host memory; per step the
-    blocks of the consensus path's final context I_f are mapped to staging slots once, and every layer's
-    blocks are staged into one of two HBM staging pools on a copy stream while the previous layer
-    attends. Selection held fixed (a step between semantic boundaries)."""
+    blocks of the consensus path's final context I_f are mapped to staging slots once (with the rows each
+    KV head needs), and every layer's rows of I_f are staged into one of two HBM staging pools on a copy
+    stream while the previous layer attends. Selection held fixed (a step between semantic boundaries)."""
     spec = W.CONSENSUS_WORKLOADS[1]
     world, rank, local = dist_setup(args.gpus)
     if not torch.cuda.is_available():
@@ -1080,18 +1080,19 @@ def run_offload(args):
     plan.select(dbg)
     torch.cuda.synchronize()
     _, _, rng, nr = (x.cpu().numpy() for x in dbg)
-    need = set()
+    need, need_rows = set(), set()
     for b in range(Bn):
         for s_, e_ in rng[b, :nr[b]]:
             need.update(int(st.block_tables[b, j]) for j in range(int(s_) // 16, (int(e_) - 1) // 16 + 1))
+            need_rows.update((int(st.block_tables[b, t // 16]), t % 16) for t in range(int(s_), int(e_)))
     cap = len(need)
     stage_ids = torch.zeros(cap, dtype=torch.int32, device=dev)
     remap = torch.empty_like(bt)
     n_staged = torch.zeros(1, dtype=torch.int32, device=dev)
     bufs = [(torch.empty((cap, H, 16, d), dtype=dt, device=dev), torch.empty((cap, H, 16, d), dtype=dt, device=dev))
             for _ in range(2)]
-    block_bytes = H * 16 * d * eb
-    staged_bytes = 2 * cap * block_bytes * L  # K and V of every staged block, every layer
+    # K and V of every staged row (the rows of I_f, every KV head: the map's row masks), every layer
+    staged_bytes = 2 * len(need_rows) * H * d * eb * L
     tok = [A.ranges_token_count(rng[b, :nr[b]]) for b in range(Bn)]
     attend_bytes = sum(A.attend_bytes_per_unit(tok[b], 0, A.ranges_block_count(rng[b, :nr[b]]), G, d, eb) * H
                        for b in range(Bn)) + Bn * Hq * d * 4
@@ -1117,7 +1118,7 @@ def run_offload(args):
         Z.zr_offload_map(plan.handle, plan.ws, bt, cap, stage_ids, remap, n_staged, stream=s)
         if kind == "stage":
             for l in range(L):
-                Z.zr_offload_stage(plan.handle, host[l][0], host[l][1], stage_ids, n_staged, cap, bufs[l % 2][0],
+                Z.zr_offload_stage(plan.handle, plan.ws, host[l][0], host[l][1], stage_ids, n_staged, cap, bufs[l % 2][0],
                                    bufs[l % 2][1], stream=s)
             return
         ev_mapped.record(s)
@@ -1125,7 +1126,7 @@ def run_offload(args):
         for l in range(L):
             if l >= 2:
                 copy.wait_event(ev_freed[l - 2])  # staging pool l % 2 is free once layer l - 2 has attended
-            Z.zr_offload_stage(plan.handle, host[l][0], host[l][1], stage_ids, n_staged, cap, bufs[l % 2][0],
+            Z.zr_offload_stage(plan.handle, plan.ws, host[l][0], host[l][1], stage_ids, n_staged, cap, bufs[l % 2][0],
                                bufs[l % 2][1], stream=copy)
             ev_staged[l].record(copy)
             s.wait_event(ev_staged[l])
@@ -1199,7 +1200,7 @@ def run_offload(args):
                    "batch": Bn, "prompt": spec.prompt_len, "generated": spec.gen_len, "layers": L, "q_heads": Hq,
                    "kv_heads": H, "head_dim": d, "top_k": spec.topk, "consensus": spec.consensus,
                    "window": spec.window, "graph": True, "staging_slots": cap, "staging_pools": 2,
-                   "pools": "pinned host memory (every layer's K/V); two HBM staging pools of the final context's blocks"},
+                   "pools": "pinned host memory (every layer's K/V); two HBM staging pools holding the final context's rows"},
         "staged_bytes_per_step": staged_bytes, "final_set_tokens": tok,
         "stage_only_ms": ms_stage, "attend_only_ms": ms_attend, "zero_copy_ms": ms_zero,
         "overlap": overlap,
@@ -1207,7 +1208,7 @@ def run_offload(args):
                      "frac": link_achieved / link_gbs, "traffic": None, "kernel": "zr_stage_copy_kernel",
                      "peak_kind": "measured pinned-host-to-device copy bandwidth of this box (1 GiB cudaMemcpyAsync, "
                                   "median of 5)",
-                     "alg_bytes_per_launch": 2 * cap * block_bytes,
+                     "alg_bytes_per_launch": staged_bytes // L,
                      "timing": "the whole step (map, then every layer's staging copy on a copy stream and its "
                                "attention on the compute stream), captured as one graph; link bytes / step time"},
         "hbm_attend_alg_bytes_per_layer": attend_bytes,

@@ -52,6 +52,7 @@ struct WsLayout {
   size_t part_ml;     // float [U + attend_warps][G][2] split (max, sum) in log2 units
   size_t bigkeys;     // uint32 [U][n_max][20] exact keys of units that take the general (640-bit) path
   size_t stage_marks; // int32 [num_blocks] offload map: staging slot + 1 of every physical block (0: not staged)
+  size_t stage_rows;  // uint32 [num_blocks][Hkv] offload map: rows of the block that a range of the head covers
   size_t votes;       // consensus only: int32 [B][n_max] vote counts, zero between selections
   size_t cruns;       // consensus only: int32 [B][n_max + 1][2] the last selection's runs before the window
   size_t cnruns;      // consensus only: int32 [B] their count

@@ -123,6 +123,7 @@ void layout_workspace(zr::Plan& p) {
   p.ws.part_ml = take(slots * p.G * 2 * sizeof(float));
   p.ws.bigkeys = take(U * p.n_max * 20 * sizeof(uint32_t));
   p.ws.stage_marks = take(static_cast<size_t>(p.num_blocks) * sizeof(int32_t));
+  p.ws.stage_rows = take(static_cast<size_t>(p.num_blocks) * p.Hkv * sizeof(uint32_t));
   const bool cons = p.mode == zr::kConsensusPlan;
   p.ws.votes = cons ? take(static_cast<size_t>(p.B) * p.n_max * sizeof(int32_t)) : 0;
   p.ws.cruns = cons ? take(static_cast<size_t>(p.B) * (p.n_max + 1) * 2 * sizeof(int32_t)) : 0;

@@ -97,7 +97,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.zr_consensus_advance.restype = ctypes.c_int
     lib.zr_offload_map.argtypes = [_P, _P, _P, ctypes.c_int32, _P, _P, _P, _P]
     lib.zr_offload_map.restype = ctypes.c_int
-    lib.zr_offload_stage.argtypes = [_P] * 5 + [ctypes.c_int32, _P, _P, _P]
+    lib.zr_offload_stage.argtypes = [_P] * 6 + [ctypes.c_int32, _P, _P, _P]
     lib.zr_offload_stage.restype = ctypes.c_int
     lib.zr_free.argtypes = [_P]
     lib.zr_free.restype = None
@@ -326,14 +326,15 @@ def zr_offload_map(plan: int, workspace: torch.Tensor, block_tables: torch.Tenso
         raise ZoomrError(st, "zr_offload_map")
 
 
-def zr_offload_stage(plan: int, host_k_pool: torch.Tensor, host_v_pool: torch.Tensor, stage_ids: torch.Tensor,
-                     n_staged: torch.Tensor, capacity: int, stage_k: torch.Tensor, stage_v: torch.Tensor,
-                     stream=None) -> None:
-    """One layer's staging copy: the mapped blocks of the host pools into slots of the staging pools."""
+def zr_offload_stage(plan: int, workspace: torch.Tensor, host_k_pool: torch.Tensor, host_v_pool: torch.Tensor,
+                     stage_ids: torch.Tensor, n_staged: torch.Tensor, capacity: int, stage_k: torch.Tensor,
+                     stage_v: torch.Tensor, stream=None) -> None:
+    """One layer's staging copy: the rows of the mapped blocks that the workspace's ranges cover (the row
+    masks zr_offload_map left in the workspace), from the host pools into slots of the staging pools."""
     if stage_k.shape[0] < capacity or stage_v.shape[0] < capacity:
         raise ValueError("zr_offload_stage: the staging pools hold capacity blocks")
-    st = load().zr_offload_stage(plan, _pool(host_k_pool), _pool(host_v_pool), _dev(stage_ids), _dev(n_staged),
-                                 int(capacity), _dev(stage_k), _dev(stage_v), _stream(stream))
+    st = load().zr_offload_stage(plan, _dev(workspace), _pool(host_k_pool), _pool(host_v_pool), _dev(stage_ids),
+                                 _dev(n_staged), int(capacity), _dev(stage_k), _dev(stage_v), _stream(stream))
     if st != ZR_OK:
         raise ZoomrError(st, "zr_offload_stage")
 

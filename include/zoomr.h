@@ -416,7 +416,8 @@ ZR_API zr_status zr_consensus_advance(zr_plan_t plan, void* workspace, const int
  * zr_consensus_select, zr_decode_advance, zr_consensus_advance on this
  * workspace): give a staging slot to every physical block that the workspace's
  * current token ranges touch (the union over every KV head of a sequence, each
- * shared block once, slots in ascending physical order).
+ * shared block once, slots in ascending physical order), and keep in the
+ * workspace, per (block, KV head), the mask of the rows those ranges cover.
  *   block_tables  [B, max_blocks_per_seq] int32 (device): the host pools' tables
  *   capacity      slots per staging pool (>= 1)
  *   stage_ids     [capacity] int32 (device, out): physical block of each used slot
@@ -433,16 +434,20 @@ ZR_API zr_status zr_offload_map(zr_plan_t plan, void* workspace, const int32_t* 
 
 /*
  * zr_offload_stage -- one layer's staging copy: slot i of stage_k / stage_v
- * receives block stage_ids[i] (all KV heads) of host_k_pool / host_v_pool, for
- * i < *n_staged (both from zr_offload_map). Pools [num_blocks, Hkv, 16, d] in host
- * memory the device can read; staging pools [capacity, Hkv, 16, d] in device
- * memory; all 16-byte aligned. Asynchronous on `stream` (a copy stream, so the
- * next layer's copy overlaps the current layer's attention). Errors: ZR_EINVAL
- * (null or misaligned pointer, capacity < 1), ZR_ECUDA.
+ * receives the rows of block stage_ids[i] of host_k_pool / host_v_pool that the
+ * workspace's ranges cover (row r of KV head h when some range of head h holds
+ * that token: exactly the rows of I_f), for i < *n_staged (all from
+ * zr_offload_map on this workspace, whose row masks it reads). The other rows of
+ * a slot keep whatever they held; the attention never reads them. Pools
+ * [num_blocks, Hkv, 16, d] in host memory the device can read; staging pools
+ * [capacity, Hkv, 16, d] in device memory; all 16-byte aligned. Asynchronous on
+ * `stream` (a copy stream, so the next layer's copy overlaps the current layer's
+ * attention). Errors: ZR_EINVAL (null or misaligned pointer, capacity < 1),
+ * ZR_EUNSUPPORTED (more than 256 KV heads), ZR_ECUDA.
  */
-ZR_API zr_status zr_offload_stage(zr_plan_t plan, const void* host_k_pool, const void* host_v_pool,
-                                  const int32_t* stage_ids, const int32_t* n_staged, int32_t capacity,
-                                  void* stage_k, void* stage_v, void* stream);
+ZR_API zr_status zr_offload_stage(zr_plan_t plan, const void* workspace, const void* host_k_pool,
+                                  const void* host_v_pool, const int32_t* stage_ids, const int32_t* n_staged,
+                                  int32_t capacity, void* stage_k, void* stage_v, void* stream);
 
 /* zr_free -- release the plan and its small device metadata (NULL is a no-op). */
 ZR_API void zr_free(zr_plan_t plan);

@@ -120,9 +120,11 @@ def _touched_blocks(st, tokens_by_seq):
 
 @pytest.mark.parametrize("dtype,d", [("bf16", 128), ("f32", 64)])
 def test_staged_consensus_layers_match_the_oracle(dtype, d):
-    """Every layer's pools in pinned host memory; per layer the blocks of I_f are staged into one of two
+    """Every layer's pools in pinned host memory; per layer the rows of I_f are staged into one of two
     HBM staging pools on a copy stream (the next layer's while the current one attends), and the
-    attention runs over the staging pools through the remapped tables. Outputs against the oracle."""
+    attention runs over the staging pools through the remapped tables. Outputs against the oracle; the
+    staging pools start as NaN, so a row that was not staged and were read would show; the rows staged
+    are exactly the rows of I_f (every KV head)."""
     from oracle import zoomr_append as OA
     from oracle import zoomr_consensus as OC
 
@@ -158,8 +160,8 @@ def test_staged_consensus_layers_match_the_oracle(dtype, d):
     remap = torch.empty_like(bt)
     n_staged = torch.zeros(1, dtype=torch.int32, device="cuda")
     Z.zr_offload_map(plan.handle, plan.ws, bt, cap, stage_ids, remap, n_staged)
-    bufs = [(torch.empty((cap, sp.num_kv_heads, 16, d), dtype=tdt, device="cuda"),
-             torch.empty((cap, sp.num_kv_heads, 16, d), dtype=tdt, device="cuda")) for _ in range(2)]
+    bufs = [(torch.full((cap, sp.num_kv_heads, 16, d), float("nan"), dtype=tdt, device="cuda"),
+             torch.full((cap, sp.num_kv_heads, 16, d), float("nan"), dtype=tdt, device="cuda")) for _ in range(2)]
     outs = [torch.full((st.batch, sp.num_q_heads, d), float("nan"), device="cuda") for _ in lts]
     main, copy = torch.cuda.current_stream(), torch.cuda.Stream()
     staged = [torch.cuda.Event() for _ in lts]
@@ -168,7 +170,7 @@ def test_staged_consensus_layers_match_the_oracle(dtype, d):
     for l, lt in enumerate(lts):  # issued in this order, so every event is recorded before it is waited on
         if l >= 2:
             copy.wait_event(freed[l - 2])  # buffer l % 2 is free once layer l - 2 has attended
-        Z.zr_offload_stage(plan.handle, host[l][0], host[l][1], stage_ids, n_staged, cap, bufs[l % 2][0],
+        Z.zr_offload_stage(plan.handle, plan.ws, host[l][0], host[l][1], stage_ids, n_staged, cap, bufs[l % 2][0],
                            bufs[l % 2][1], stream=copy)
         staged[l].record(copy)
         main.wait_event(staged[l])
@@ -186,6 +188,16 @@ def test_staged_consensus_layers_match_the_oracle(dtype, d):
         for l in range(len(lts)):
             e = float(np.max(np.abs(outs[l][b].cpu().numpy().astype(np.float64) - r.out[l])))
             assert np.isfinite(e) and e <= C.TOL[dtype], (b, l, e)
+    # the staged rows of the last layer's pool: exactly I_f's rows, all KV heads
+    slot_of = {blk: i for i, blk in enumerate(want_blocks)}
+    want_rows = np.zeros((n, sp.num_kv_heads, 16), bool)
+    for b, r in enumerate(res):
+        for t in r.tokens:
+            want_rows[slot_of[int(st.block_tables[b, int(t) // 16])], :, int(t) % 16] = True
+    last = len(lts) - 1
+    for pool in bufs[last % 2]:
+        got_rows = ~torch.isnan(pool[:n].float()).any(dim=-1).cpu().numpy()
+        assert np.array_equal(got_rows, want_rows)
     plan.close()
 
 
@@ -207,9 +219,9 @@ def test_staged_decode_equals_the_hbm_step_and_overflow_is_reported():
         remap = torch.empty_like(bt)
         n_staged = torch.zeros(1, dtype=torch.int32, device="cuda")
         Z.zr_offload_map(plan.handle, plan.ws, bt, cap, stage_ids, remap, n_staged)
-        sk = torch.empty((cap, 2, 16, 128), dtype=torch.bfloat16, device="cuda")
-        sv = torch.empty_like(sk)
-        Z.zr_offload_stage(plan.handle, hk, hv, stage_ids, n_staged, cap, sk, sv)
+        sk = torch.full((cap, 2, 16, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+        sv = torch.full_like(sk, float("nan"))
+        Z.zr_offload_stage(plan.handle, plan.ws, hk, hv, stage_ids, n_staged, cap, sk, sv)
         out = torch.empty_like(ref)
         plan.run_reuse(lt.q, sk, sv, remap, lt.sum_k, lt.sum_v, out)
         torch.cuda.synchronize()
