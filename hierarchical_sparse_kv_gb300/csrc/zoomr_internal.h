@@ -69,6 +69,7 @@ struct Plan {
   int c_max;                          // consensus: max clipped c (at least 1)
   int attend_ctas;   // persistent attend grid (one resident wave)
   int attend_warps;  // attend_ctas * kAttendWarps
+  int fixed_rows;    // max over sequences of the tokens gathered whatever the selection: sink / prompt + window
   int device;
   void* d_meta_base;
   DeviceMeta meta;
@@ -105,6 +106,7 @@ struct StepArgs {
   int32_t* cnruns;  // consensus only
   int B, Hq, Hkv, G, window, num_blocks, max_blocks, k_max, n_max, attend_warps;
   int unit_cost;  // virtual rows in front of every unit in the attend kernels' even split (see kernels)
+  int fixed_rows;  // rows per sequence prefetched before the attend kernel's wait (0: none; decode step only)
   float scale_log2;  // log2(e) / sqrt(d)
 };
 

@@ -699,6 +699,40 @@ __device__ __forceinline__ void prefetch_attend_inputs(const StepArgs& a, size_t
   prefetch_span(a.q, static_cast<size_t>(a.B) * a.Hq * q_row_bytes, t, nt);
 }
 
+// Before its wait an attend CTA also prefetches into L2 its slice of the K and V rows that every unit
+// gathers whatever the selection decides: the sink or prompt [0, Ns) and the window [L - w, L) of each
+// sequence, every KV head (one bulk prefetch per row). The memory system is otherwise idle while the
+// select kernel runs, and these rows then come from L2 in the streaming phase. A prefetch moves no data
+// the kernel uses: a block table still being written by an earlier kernel can only misdirect it (block
+// ids are range-checked, so every address lies inside the pools).
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+__device__ void prefetch_fixed_rows(const StepArgs& a, uint32_t row_bytes) {
+  const int F = a.fixed_rows, H = a.Hkv;
+  const long long total = static_cast<long long>(a.B) * F * H;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int b = static_cast<int>(i / (static_cast<long long>(F) * H));
+    const int r = static_cast<int>(i % (static_cast<long long>(F) * H));
+    const int j = r / H, g = r - (r / H) * H;  // the j-th fixed token of b, KV head g
+    const int L = a.meta.seq_lens[b], Ns = a.meta.prompt_lens[b];
+    const int Wb = min(a.window, L);
+    int t;
+    if (j < Ns) {
+      t = j;
+    } else {
+      t = L - Wb + (j - Ns);
+      if (t >= L || t < Ns) continue;  // past the window, or a window token inside the prompt
+    }
+    const int phys = a.block_tables[static_cast<size_t>(b) * a.max_blocks + (t >> 4)];
+    if (static_cast<unsigned>(phys) >= static_cast<unsigned>(a.num_blocks)) continue;
+    const size_t off = ((static_cast<size_t>(phys) * H + g) * kBlockTokens + (t & 15)) * row_bytes;
+    prefetch_l2_bulk(static_cast<const char*>(a.k_pool) + off, row_bytes);
+    prefetch_l2_bulk(static_cast<const char*>(a.v_pool) + off, row_bytes);
+  }
+}
+
 // One warp's walk over its rows: for every unit its range touches, begin_unit, run over row
 // tables of up to kChunkRows rows, and end_unit into slot u + w.
 template <class Worker>
@@ -976,6 +1010,7 @@ __global__ void __launch_bounds__(kAttendWarps * 32, 3) zr_attend_mma_kernel(Ste
   __shared__ int32_t s_rows[kStagedUnits];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   prefetch_attend_inputs(a, sizeof(__nv_bfloat16) * D);
+  prefetch_fixed_rows(a, sizeof(__nv_bfloat16) * D);
   pdl_wait();
   pdl_trigger();  // after the wait: the merge kernel may read the select kernel's unit sizes at once
   MmaWorker<D> wk;
@@ -1066,6 +1101,7 @@ __global__ void __launch_bounds__(kAttendWarps * 32) zr_attend_fma_kernel(StepAr
   __shared__ int32_t s_rows[kStagedUnits];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   prefetch_attend_inputs(a, sizeof(T) * D);
+  prefetch_fixed_rows(a, sizeof(T) * D);
   pdl_wait();
   pdl_trigger();  // after the wait: the merge kernel may read the select kernel's unit sizes at once
   FmaWorker<T, D> wk;

@@ -200,6 +200,8 @@ zr_status make_decode_plan(const zr_config* cfg, const int32_t* seq_lens, const 
     for (int i = 0; i < kclip[b]; ++i) top += lens[i];
     const int32_t sink = sink_lens ? sink_lens[b] : 0;
     const int64_t tok_bound = std::min<int64_t>(L, sink + std::min<int64_t>(p.window, L) + top);
+    p.fixed_rows =
+        static_cast<int>(std::max<int64_t>(p.fixed_rows, std::min<int64_t>(L, sink + std::min(p.window, L))));
     rows_bound += (tok_bound + (n - kclip[b])) * p.Hkv;
     any_sink = any_sink || sink > 0;
   }
@@ -303,6 +305,10 @@ zr_status decode_into(zr_plan_t plan, void* workspace, const void* q, const void
   a.sel_out = sel_out;
   a.ranges_out = ranges_out;
   a.nranges_out = nranges_out;
+  // The pools of a decode step are the plan's full pools, so the attend kernel may prefetch the rows every
+  // unit gathers (sink and window) through the block tables before its wait. The attend-only entry points
+  // can be given staging pools with fewer blocks (the offloaded cache) and do not prefetch.
+  a.fixed_rows = plan->p.fixed_rows;
   return zr::launch_step(plan->p, a, stream, ev_start, ev_stop);
 }
 
@@ -336,6 +342,7 @@ StepArgs step_args(const Plan& p, void* workspace) {
   // different tokens (each KV head selects its own segments); consensus units share one token set,
   // whose block-table entries the next unit finds cached, and a start there costs little.
   a.unit_cost = p.mode == kConsensusPlan ? 0 : kUnitStartRows;
+  a.fixed_rows = 0;  // set by the decode step only (see decode_into)
   a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(p.d)));
   return a;
 }
@@ -449,6 +456,8 @@ zr_status zr_consensus_plan(const zr_config* cfg, const int32_t* seq_lens, const
     for (int i = 0; i < cclip[b]; ++i) top += reg[i];
     const int64_t tok = std::min<int64_t>(L, prompt_lens[b] + std::min<int64_t>(p.window, L) + top + sum_s);
     rows_bound += tok * p.Hkv;
+    p.fixed_rows = static_cast<int>(
+        std::max<int64_t>(p.fixed_rows, std::min<int64_t>(L, prompt_lens[b] + std::min(p.window, L))));
   }
   p.k_max = p.n_max + 1;  // range capacity per unit: prompt, one piece per pair, window
   if (cudaGetDevice(&p.device) != cudaSuccess) {
