@@ -9,6 +9,7 @@
 namespace zr {
 
 constexpr int kBlockTokens = 16;      // tokens per paged KV block
+constexpr int kSelPrefetchBlocks = 128;  // blocks before each unit's window the select kernel lists for prefetch
 constexpr int kMaxSegments = 4096;    // n_b limit of the select kernel's shared memory
 constexpr int kMaxGroup = 16;         // query heads per KV head
 constexpr int kMmaMaxGroup = 8;       // the tensor-core attend kernel packs the group into 8 MMA columns
@@ -53,6 +54,7 @@ struct WsLayout {
   size_t bigkeys;     // uint32 [U][n_max][20] exact keys of units that take the general (640-bit) path
   size_t stage_marks; // int32 [num_blocks] offload map: staging slot + 1 of every physical block (0: not staged)
   size_t stage_rows;  // uint32 [num_blocks][Hkv] offload map: rows of the block that a range of the head covers
+  size_t pf_list;     // int32 [U][kSelPrefetchBlocks] selected blocks before each unit's window (-1: none)
   size_t votes;       // consensus only: int32 [B][n_max] vote counts, zero between selections
   size_t cruns;       // consensus only: int32 [B][n_max + 1][2] the last selection's runs before the window
   size_t cnruns;      // consensus only: int32 [B] their count
@@ -102,11 +104,13 @@ struct StepArgs {
   float* part_o;
   float2* part_ml;
   uint32_t* bigkeys;
+  int32_t* pf_list;  // decode step: blocks the attend kernel prefetches after its wait
   int32_t* cruns;   // consensus only
   int32_t* cnruns;  // consensus only
   int B, Hq, Hkv, G, window, num_blocks, max_blocks, k_max, n_max, attend_warps;
   int unit_cost;  // virtual rows in front of every unit in the attend kernels' even split (see kernels)
   int fixed_rows;  // rows per sequence prefetched before the attend kernel's wait (0: none; decode step only)
+  int prefetch_selected;  // 1: the select kernel lists selected blocks, the attend kernel prefetches them (decode step)
   float scale_log2;  // log2(e) / sqrt(d)
 };
 

@@ -47,6 +47,10 @@ __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.lau
 // An L2 prefetch: a hint only (a later load still reads the current value), so kernels issue it for
 // their inputs before waiting on the previous kernel, which cannot make it read anything stale.
 __device__ __forceinline__ void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
+// Bulk prefetch of `bytes` (a multiple of 16, 16-byte aligned address) into L2.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
 
 // Prefetch `bytes` at `base` into L2, one 128-byte line per thread of the grid slice [t0, t0 + nt).
 __device__ __forceinline__ void prefetch_span(const void* base, size_t bytes, size_t t, size_t nt) {
@@ -190,6 +194,38 @@ __device__ void add_sink_range(const StepArgs& a, int u, int Ns, int32_t* rg, in
   }
 }
 
+// Once a unit's selection is final, the select CTA's idle warps list for the attend kernel the selected
+// segments' blocks among the kSelPrefetchBlocks blocks just before the window (entry q of the unit's list:
+// the physical block, or -1). The attend kernel prefetches their K and V tiles into L2 right after its
+// wait, while its first row tables are built: it gathers these blocks last, so they have the longest
+// time to arrive. (Prefetched by the select kernel itself, they would hold up its completion.)
+__device__ void list_selected_tail(const StepArgs& a, int u, int b, int n, int W0, const int* flag, const int* bnd,
+                                   int t, int nt) {
+  int32_t* list = a.pf_list + static_cast<size_t>(u) * kSelPrefetchBlocks;
+  for (int q = t; q < kSelPrefetchBlocks; q += nt) {
+    const int j = W0 / kBlockTokens - 1 - q;  // a block wholly before the window, walking back
+    int out = -1;
+    if (j < 0) {
+      list[q] = out;
+      continue;
+    }
+    const int t0 = j * kBlockTokens, t1 = t0 + kBlockTokens;
+    // the segments overlapping [t0, t1): from the last bound <= t0 (bnd ascending, bnd[0] = 0)
+    int lo = 0, hi = n;  // invariant: bnd[lo] <= t0 < bnd[hi] (or hi = n)
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (bnd[mid] <= t0) lo = mid; else hi = mid;
+    }
+    bool any = false;
+    for (int i = lo; i < n && bnd[i] < t1; ++i) any |= flag[i] != 0;
+    if (any) {
+      const int phys = a.block_tables[static_cast<size_t>(b) * a.max_blocks + j];
+      if (static_cast<unsigned>(phys) < static_cast<unsigned>(a.num_blocks)) out = phys;
+    }
+    list[q] = out;
+  }
+}
+
 // Shared memory: the exact-key scorer's query limb tables | the query table [G * D] | key high words
 //   [n_max + 4] u64 | key low words [n_max + 4] u64 | flag [n_max + 2] | bounds [n_max + 1] | list [n_max] |
 //   runs_s [n_max] | runs_e [n_max] | fp32 enclosures lo, hi [n_max] each
@@ -299,7 +335,8 @@ __global__ void __maxnreg__(80) zr_select_kernel(StepArgs a) {
   const int W0 = max(0, L - a.window);
   if (n <= kWarpRangesMax) {
     // Warp 0 alone, 32 segments per pass: compaction and run numbering from ballots, with carries
-    // between passes; then the ranges. No CTA barrier: the other warps are done.
+    // between passes; then the ranges. No CTA barrier: the other warps prefetch and are done.
+    if (tid >= 32 && a.prefetch_selected) list_selected_tail(a, u, b, n, W0, flag, bnd, tid - 32, blockDim.x - 32);
     if (tid < 32) {
       const int lane = tid;
       const unsigned lt = (1u << lane) - 1u;
@@ -437,7 +474,11 @@ __global__ void __maxnreg__(80) zr_select_kernel(StepArgs a) {
       }
     }
   } else {
-    // Any n: block-wide scans over contiguous per-thread slices.
+    // Any n: block-wide scans over contiguous per-thread slices. (No prefetch list here: the flags are
+    // reused as scratch below.)
+    if (a.prefetch_selected)
+      for (int q = tid; q < kSelPrefetchBlocks; q += blockDim.x)
+        a.pf_list[static_cast<size_t>(u) * kSelPrefetchBlocks + q] = -1;
     {
       const int per = (n + blockDim.x - 1) / blockDim.x;
       const int i0 = min(n, tid * per), i1 = min(n, i0 + per);
@@ -705,9 +746,6 @@ __device__ __forceinline__ void prefetch_attend_inputs(const StepArgs& a, size_t
 // select kernel runs, and these rows then come from L2 in the streaming phase. A prefetch moves no data
 // the kernel uses: a block table still being written by an earlier kernel can only misdirect it (block
 // ids are range-checked, so every address lies inside the pools).
-__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
 __device__ void prefetch_fixed_rows(const StepArgs& a, uint32_t row_bytes) {
   const int F = a.fixed_rows, H = a.Hkv;
   const long long total = static_cast<long long>(a.B) * F * H;
@@ -730,6 +768,21 @@ __device__ void prefetch_fixed_rows(const StepArgs& a, uint32_t row_bytes) {
     const size_t off = ((static_cast<size_t>(phys) * H + g) * kBlockTokens + (t & 15)) * row_bytes;
     prefetch_l2_bulk(static_cast<const char*>(a.k_pool) + off, row_bytes);
     prefetch_l2_bulk(static_cast<const char*>(a.v_pool) + off, row_bytes);
+  }
+}
+
+// Right after its wait an attend CTA prefetches into L2 its slice of the select kernel's lists (the
+// selected blocks just before each unit's window; see list_selected_tail): one bulk prefetch per K and V
+// tile of a listed block, overlapping the round trips of the first row tables.
+__device__ void prefetch_selected_lists(const StepArgs& a, uint32_t tile_bytes) {
+  const int total = a.B * a.Hkv * kSelPrefetchBlocks;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
+    const int phys = a.pf_list[i];
+    if (static_cast<unsigned>(phys) >= static_cast<unsigned>(a.num_blocks)) continue;
+    const int g = (i / kSelPrefetchBlocks) % a.Hkv;  // unit u = b * Hkv + g
+    const size_t off = (static_cast<size_t>(phys) * a.Hkv + g) * tile_bytes;
+    prefetch_l2_bulk(static_cast<const char*>(a.k_pool) + off, tile_bytes);
+    prefetch_l2_bulk(static_cast<const char*>(a.v_pool) + off, tile_bytes);
   }
 }
 
@@ -1013,6 +1066,7 @@ __global__ void __launch_bounds__(kAttendWarps * 32, 3) zr_attend_mma_kernel(Ste
   prefetch_fixed_rows(a, sizeof(__nv_bfloat16) * D);
   pdl_wait();
   pdl_trigger();  // after the wait: the merge kernel may read the select kernel's unit sizes at once
+  if (a.prefetch_selected) prefetch_selected_lists(a, kBlockTokens * D * sizeof(__nv_bfloat16));
   MmaWorker<D> wk;
   wk.ring = static_cast<uint32_t>(__cvta_generic_to_shared(attend_smem)) + warp * kStages * MmaWorker<D>::kStageBytes;
   const int chunk_off = (lane % (D / 8)) * 16;
@@ -1104,6 +1158,7 @@ __global__ void __launch_bounds__(kAttendWarps * 32) zr_attend_fma_kernel(StepAr
   prefetch_fixed_rows(a, sizeof(T) * D);
   pdl_wait();
   pdl_trigger();  // after the wait: the merge kernel may read the select kernel's unit sizes at once
+  if (a.prefetch_selected) prefetch_selected_lists(a, kBlockTokens * D * sizeof(T));
   FmaWorker<T, D> wk;
   attend_balanced(a, stage_unit_rows(a, s_rows), wk, rowtab[warp], warp, lane);
 }

@@ -124,6 +124,7 @@ void layout_workspace(zr::Plan& p) {
   p.ws.bigkeys = take(U * p.n_max * 20 * sizeof(uint32_t));
   p.ws.stage_marks = take(static_cast<size_t>(p.num_blocks) * sizeof(int32_t));
   p.ws.stage_rows = take(static_cast<size_t>(p.num_blocks) * p.Hkv * sizeof(uint32_t));
+  p.ws.pf_list = take(U * zr::kSelPrefetchBlocks * sizeof(int32_t));
   const bool cons = p.mode == zr::kConsensusPlan;
   p.ws.votes = cons ? take(static_cast<size_t>(p.B) * p.n_max * sizeof(int32_t)) : 0;
   p.ws.cruns = cons ? take(static_cast<size_t>(p.B) * (p.n_max + 1) * 2 * sizeof(int32_t)) : 0;
@@ -309,6 +310,7 @@ zr_status decode_into(zr_plan_t plan, void* workspace, const void* q, const void
   // unit gathers (sink and window) through the block tables before its wait. The attend-only entry points
   // can be given staging pools with fewer blocks (the offloaded cache) and do not prefetch.
   a.fixed_rows = plan->p.fixed_rows;
+  a.prefetch_selected = 1;
   return zr::launch_step(plan->p, a, stream, ev_start, ev_stop);
 }
 
@@ -326,6 +328,7 @@ StepArgs step_args(const Plan& p, void* workspace) {
   a.part_o = reinterpret_cast<float*>(ws + p.ws.part_o);
   a.part_ml = reinterpret_cast<float2*>(ws + p.ws.part_ml);
   a.bigkeys = reinterpret_cast<uint32_t*>(ws + p.ws.bigkeys);
+  a.pf_list = reinterpret_cast<int32_t*>(ws + p.ws.pf_list);
   a.cruns = p.mode == kConsensusPlan ? reinterpret_cast<int32_t*>(ws + p.ws.cruns) : nullptr;
   a.cnruns = p.mode == kConsensusPlan ? reinterpret_cast<int32_t*>(ws + p.ws.cnruns) : nullptr;
   a.B = p.B;
@@ -343,6 +346,7 @@ StepArgs step_args(const Plan& p, void* workspace) {
   // whose block-table entries the next unit finds cached, and a start there costs little.
   a.unit_cost = p.mode == kConsensusPlan ? 0 : kUnitStartRows;
   a.fixed_rows = 0;  // set by the decode step only (see decode_into)
+  a.prefetch_selected = 0;
   a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(p.d)));
   return a;
 }
