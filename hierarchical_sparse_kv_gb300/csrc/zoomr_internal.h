@@ -72,6 +72,7 @@ struct Plan {
   int attend_ctas;   // persistent attend grid (one resident wave)
   int attend_warps;  // attend_ctas * kAttendWarps
   int fixed_rows;    // max over sequences of the tokens gathered whatever the selection: sink / prompt + window
+  int pf_blocks;     // decode step: blocks before each unit's window scanned for the selected-tile prefetch
   int device;
   void* d_meta_base;
   DeviceMeta meta;
@@ -111,6 +112,7 @@ struct StepArgs {
   int unit_cost;  // virtual rows in front of every unit in the attend kernels' even split (see kernels)
   int fixed_rows;  // rows per sequence prefetched before the attend kernel's wait (0: none; decode step only)
   int prefetch_selected;  // 1: the select kernel lists selected blocks, the attend kernel prefetches them (decode step)
+  int pf_blocks;  // of those blocks, how many are scanned (the rest listed as -1)
   float scale_log2;  // log2(e) / sqrt(d)
 };
 

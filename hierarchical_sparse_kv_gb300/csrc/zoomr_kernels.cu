@@ -195,8 +195,8 @@ __device__ void add_sink_range(const StepArgs& a, int u, int Ns, int32_t* rg, in
 }
 
 // Once a unit's selection is final, the select CTA's idle warps list for the attend kernel the selected
-// segments' blocks among the kSelPrefetchBlocks blocks just before the window (entry q of the unit's list:
-// the physical block, or -1). The attend kernel prefetches their K and V tiles into L2 right after its
+// segments' blocks among the a.pf_blocks (at most kSelPrefetchBlocks) blocks just before the window
+// (entry q of the unit's list: the physical block, or -1). The attend kernel prefetches their K and V tiles into L2 right after its
 // wait, while its first row tables are built: it gathers these blocks last, so they have the longest
 // time to arrive. (Prefetched by the select kernel itself, they would hold up its completion.)
 __device__ void list_selected_tail(const StepArgs& a, int u, int b, int n, int W0, const int* flag, const int* bnd,
@@ -205,7 +205,7 @@ __device__ void list_selected_tail(const StepArgs& a, int u, int b, int n, int W
   for (int q = t; q < kSelPrefetchBlocks; q += nt) {
     const int j = W0 / kBlockTokens - 1 - q;  // a block wholly before the window, walking back
     int out = -1;
-    if (j < 0) {
+    if (j < 0 || q >= a.pf_blocks) {
       list[q] = out;
       continue;
     }

@@ -207,6 +207,11 @@ zr_status make_decode_plan(const zr_config* cfg, const int32_t* seq_lens, const 
     any_sink = any_sink || sink > 0;
   }
   if (any_sink) ++p.k_max;  // one more range slot per unit for the sink's range
+  // The selected-tile prefetch scans up to kSelPrefetchBlocks blocks per unit and about 8192 over all
+  // units (about a quarter of them selected: some 16 MB of K and V, what the attend start-up leaves
+  // idle); more units scan fewer blocks each (8 x 16K: 128; 32 ragged sequences: 32).
+  p.pf_blocks = static_cast<int>(std::min<int64_t>(zr::kSelPrefetchBlocks,
+                                                   std::max<int64_t>(8, 8192 / (static_cast<int64_t>(p.B) * p.Hkv))));
   if (cudaGetDevice(&p.device) != cudaSuccess) {
     cudaGetLastError();
     delete P;
@@ -311,6 +316,7 @@ zr_status decode_into(zr_plan_t plan, void* workspace, const void* q, const void
   // can be given staging pools with fewer blocks (the offloaded cache) and do not prefetch.
   a.fixed_rows = plan->p.fixed_rows;
   a.prefetch_selected = 1;
+  a.pf_blocks = plan->p.pf_blocks;
   return zr::launch_step(plan->p, a, stream, ev_start, ev_stop);
 }
 
