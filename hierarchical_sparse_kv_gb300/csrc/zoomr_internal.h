@@ -73,6 +73,7 @@ struct Plan {
   int attend_warps;  // attend_ctas * kAttendWarps
   int fixed_rows;    // max over sequences of the tokens gathered whatever the selection: sink / prompt + window
   int pf_blocks;     // decode step: blocks before each unit's window scanned for the selected-tile prefetch
+  int prompt_rows;   // max over sequences of the sink / prompt length
   int device;
   void* d_meta_base;
   DeviceMeta meta;
@@ -110,7 +111,8 @@ struct StepArgs {
   int32_t* cnruns;  // consensus only
   int B, Hq, Hkv, G, window, num_blocks, max_blocks, k_max, n_max, attend_warps;
   int unit_cost;  // virtual rows in front of every unit in the attend kernels' even split (see kernels)
-  int fixed_rows;  // rows per sequence prefetched before the attend kernel's wait (0: none; decode step only)
+  int fixed_rows;  // rows per sequence prefetched before the attend kernel's wait (0: none)
+  int fixed_window;  // 1: the window rows too (the decode step, whose lengths are the plan's); 0: the prompt only
   int prefetch_selected;  // 1: the select kernel lists selected blocks, the attend kernel prefetches them (decode step)
   int pf_blocks;  // of those blocks, how many are scanned (the rest listed as -1)
   float scale_log2;  // log2(e) / sqrt(d)

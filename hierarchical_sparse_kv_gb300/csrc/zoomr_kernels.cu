@@ -760,6 +760,7 @@ __device__ void prefetch_fixed_rows(const StepArgs& a, uint32_t row_bytes) {
     if (j < Ns) {
       t = j;
     } else {
+      if (!a.fixed_window) continue;
       t = L - Wb + (j - Ns);
       if (t >= L || t < Ns) continue;  // past the window, or a window token inside the prompt
     }

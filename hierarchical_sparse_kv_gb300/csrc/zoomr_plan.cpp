@@ -203,6 +203,7 @@ zr_status make_decode_plan(const zr_config* cfg, const int32_t* seq_lens, const 
     const int64_t tok_bound = std::min<int64_t>(L, sink + std::min<int64_t>(p.window, L) + top);
     p.fixed_rows =
         static_cast<int>(std::max<int64_t>(p.fixed_rows, std::min<int64_t>(L, sink + std::min(p.window, L))));
+    p.prompt_rows = std::max(p.prompt_rows, static_cast<int>(sink));
     rows_bound += (tok_bound + (n - kclip[b])) * p.Hkv;
     any_sink = any_sink || sink > 0;
   }
@@ -315,6 +316,7 @@ zr_status decode_into(zr_plan_t plan, void* workspace, const void* q, const void
   // unit gathers (sink and window) through the block tables before its wait. The attend-only entry points
   // can be given staging pools with fewer blocks (the offloaded cache) and do not prefetch.
   a.fixed_rows = plan->p.fixed_rows;
+  a.fixed_window = 1;
   a.prefetch_selected = 1;
   a.pf_blocks = plan->p.pf_blocks;
   return zr::launch_step(plan->p, a, stream, ev_start, ev_stop);
@@ -351,7 +353,8 @@ StepArgs step_args(const Plan& p, void* workspace) {
   // different tokens (each KV head selects its own segments); consensus units share one token set,
   // whose block-table entries the next unit finds cached, and a start there costs little.
   a.unit_cost = p.mode == kConsensusPlan ? 0 : kUnitStartRows;
-  a.fixed_rows = 0;  // set by the decode step only (see decode_into)
+  a.fixed_rows = 0;  // set by the decode step and the attend-only calls (see decode_into)
+  a.fixed_window = 0;
   a.prefetch_selected = 0;
   a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(p.d)));
   return a;
@@ -468,6 +471,7 @@ zr_status zr_consensus_plan(const zr_config* cfg, const int32_t* seq_lens, const
     rows_bound += tok * p.Hkv;
     p.fixed_rows = static_cast<int>(
         std::max<int64_t>(p.fixed_rows, std::min<int64_t>(L, prompt_lens[b] + std::min(p.window, L))));
+    p.prompt_rows = std::max(p.prompt_rows, static_cast<int>(prompt_lens[b]));
   }
   p.k_max = p.n_max + 1;  // range capacity per unit: prompt, one piece per pair, window
   if (cudaGetDevice(&p.device) != cudaSuccess) {
@@ -553,6 +557,39 @@ zr_status zr_consensus_select(zr_plan_t plan, void* workspace, int32_t* votes_ou
 }
 
 namespace {
+// True when the device allocation holding p extends at least `bytes` past it (the driver's address-range
+// query; false for host memory or when the query is unavailable).
+bool spans_bytes(const void* p, size_t bytes) {
+  using Fn = int (*)(unsigned long long*, size_t*, unsigned long long);
+  static const Fn fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuMemGetAddressRange", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess) {
+      cudaGetLastError();
+      return static_cast<Fn>(nullptr);
+    }
+    return reinterpret_cast<Fn>(f);
+  }();
+  if (!fn) return false;
+  unsigned long long base = 0;
+  size_t size = 0;
+  const unsigned long long at = reinterpret_cast<unsigned long long>(p);
+  if (fn(&base, &size, at) != 0) return false;
+  return at >= base && at + bytes <= base + size;
+}
+
+// The attend-only calls prefetch the sink or prompt rows before their wait (as the decode step does) only
+// when both pools lie in allocations that hold the plan's num_blocks blocks: then even a block table still
+// being written by an earlier kernel can only send a prefetch elsewhere inside them. Staging pools of the
+// offloaded cache, or pools in host memory, get no prefetch. The window is left out: between selections
+// the sequences grow past the plan's lengths (the advance calls), and the prompt does not move.
+int prompt_rows_if_full_pools(const zr::Plan& p, const void* k_pool, const void* v_pool) {
+  const size_t eb = p.cfg.dtype == ZR_BF16 ? 2 : 4;
+  const size_t bytes = static_cast<size_t>(p.num_blocks) * p.Hkv * zr::kBlockTokens * p.d * eb;
+  return spans_bytes(k_pool, bytes) && spans_bytes(v_pool, bytes) ? p.prompt_rows : 0;
+}
+
 zr_status consensus_attend_into(zr_plan_t plan, void* workspace, const void* q, const void* k_pool,
                                 const void* v_pool, const int32_t* block_tables, float* out, void* stream,
                                 void* ev_start, void* ev_stop) {
@@ -569,6 +606,8 @@ zr_status consensus_attend_into(zr_plan_t plan, void* workspace, const void* q, 
   a.sum_k = k_pool;  // no summary rows are gathered: every unit's summary count is 0
   a.sum_v = v_pool;
   a.out = out;
+  a.fixed_rows = prompt_rows_if_full_pools(plan->p, k_pool, v_pool);
+  a.fixed_window = 0;
   return zr::launch_attend_only(plan->p, a, stream, ev_start, ev_stop);
 }
 }  // namespace
@@ -611,6 +650,8 @@ zr_status zr_decode_attend_reuse(zr_plan_t plan, void* workspace, const void* q,
   a.sum_k = sum_k;
   a.sum_v = sum_v;
   a.out = out;
+  a.fixed_rows = prompt_rows_if_full_pools(plan->p, k_pool, v_pool);
+  a.fixed_window = 0;
   return zr::launch_attend_only(plan->p, a, stream);
 }
 
