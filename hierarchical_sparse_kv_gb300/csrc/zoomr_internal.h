@@ -113,8 +113,8 @@ struct StepArgs {
   int unit_cost;  // virtual rows in front of every unit in the attend kernels' even split (see kernels)
   int fixed_rows;  // rows per sequence prefetched before the attend kernel's wait (0: none)
   int fixed_window;  // 1: the window rows too (the decode step, whose lengths are the plan's); 0: the prompt only
-  int prefetch_selected;  // 1: the select kernel lists selected blocks, the attend kernel prefetches them (decode step)
-  int pf_blocks;  // of those blocks, how many are scanned (the rest listed as -1)
+  int pf_blocks;  // decode step: blocks before each window the select kernel scans and lists for the attend
+                  // kernel's prefetch (entries up to kSelPrefetchBlocks, the rest -1); 0: no list, no prefetch
   float scale_log2;  // log2(e) / sqrt(d)
 };
 

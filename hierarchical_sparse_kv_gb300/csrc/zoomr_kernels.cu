@@ -336,7 +336,7 @@ __global__ void __maxnreg__(80) zr_select_kernel(StepArgs a) {
   if (n <= kWarpRangesMax) {
     // Warp 0 alone, 32 segments per pass: compaction and run numbering from ballots, with carries
     // between passes; then the ranges. No CTA barrier: the other warps prefetch and are done.
-    if (tid >= 32 && a.prefetch_selected) list_selected_tail(a, u, b, n, W0, flag, bnd, tid - 32, blockDim.x - 32);
+    if (tid >= 32 && a.pf_blocks > 0) list_selected_tail(a, u, b, n, W0, flag, bnd, tid - 32, blockDim.x - 32);
     if (tid < 32) {
       const int lane = tid;
       const unsigned lt = (1u << lane) - 1u;
@@ -476,7 +476,7 @@ __global__ void __maxnreg__(80) zr_select_kernel(StepArgs a) {
   } else {
     // Any n: block-wide scans over contiguous per-thread slices. (No prefetch list here: the flags are
     // reused as scratch below.)
-    if (a.prefetch_selected)
+    if (a.pf_blocks > 0)
       for (int q = tid; q < kSelPrefetchBlocks; q += blockDim.x)
         a.pf_list[static_cast<size_t>(u) * kSelPrefetchBlocks + q] = -1;
     {
@@ -1067,7 +1067,7 @@ __global__ void __launch_bounds__(kAttendWarps * 32, 3) zr_attend_mma_kernel(Ste
   prefetch_fixed_rows(a, sizeof(__nv_bfloat16) * D);
   pdl_wait();
   pdl_trigger();  // after the wait: the merge kernel may read the select kernel's unit sizes at once
-  if (a.prefetch_selected) prefetch_selected_lists(a, kBlockTokens * D * sizeof(__nv_bfloat16));
+  if (a.pf_blocks > 0) prefetch_selected_lists(a, kBlockTokens * D * sizeof(__nv_bfloat16));
   MmaWorker<D> wk;
   wk.ring = static_cast<uint32_t>(__cvta_generic_to_shared(attend_smem)) + warp * kStages * MmaWorker<D>::kStageBytes;
   const int chunk_off = (lane % (D / 8)) * 16;
@@ -1159,7 +1159,7 @@ __global__ void __launch_bounds__(kAttendWarps * 32) zr_attend_fma_kernel(StepAr
   prefetch_fixed_rows(a, sizeof(T) * D);
   pdl_wait();
   pdl_trigger();  // after the wait: the merge kernel may read the select kernel's unit sizes at once
-  if (a.prefetch_selected) prefetch_selected_lists(a, kBlockTokens * D * sizeof(T));
+  if (a.pf_blocks > 0) prefetch_selected_lists(a, kBlockTokens * D * sizeof(T));
   FmaWorker<T, D> wk;
   attend_balanced(a, stage_unit_rows(a, s_rows), wk, rowtab[warp], warp, lane);
 }

@@ -317,7 +317,6 @@ zr_status decode_into(zr_plan_t plan, void* workspace, const void* q, const void
   // can be given staging pools with fewer blocks (the offloaded cache) and do not prefetch.
   a.fixed_rows = plan->p.fixed_rows;
   a.fixed_window = 1;
-  a.prefetch_selected = 1;
   a.pf_blocks = plan->p.pf_blocks;
   return zr::launch_step(plan->p, a, stream, ev_start, ev_stop);
 }
@@ -355,7 +354,7 @@ StepArgs step_args(const Plan& p, void* workspace) {
   a.unit_cost = p.mode == kConsensusPlan ? 0 : kUnitStartRows;
   a.fixed_rows = 0;  // set by the decode step and the attend-only calls (see decode_into)
   a.fixed_window = 0;
-  a.prefetch_selected = 0;
+  a.pf_blocks = 0;
   a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(p.d)));
   return a;
 }
