@@ -342,7 +342,7 @@ def run_zoomr(args):
     dev = torch.device("cuda", torch.cuda.current_device())
     spec, st, lts = make_inputs(dev, args.workload)
     L = len(lts)
-    plan = Z.DecodePlan.from_structure(st, device=dev)
+    plan = Z.DecodePlan.from_structure(st, device=dev).set_deterministic(args.deterministic)
     bt = torch.from_numpy(st.block_tables.astype(np.int32)).to(dev)
     # every layer's queries and outputs are slices of one buffer each, so the end-to-end leg moves a
     # step's inputs and results with one copy per direction
@@ -534,7 +534,8 @@ def run_zoomr(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": spec.dtype,
         "data": "synthetic (seeded N(0,1) K/V, segment-mean summaries + N(0,0.1), queries near segment means)",
-        "config": config_dict(spec, {"graph": not args.no_graph, "replicas_per_gpu": 1, "l2": l2}),
+        "config": config_dict(spec, {"graph": not args.no_graph, "replicas_per_gpu": 1, "l2": l2,
+                                     "split": "static" if args.deterministic else "dynamic"}),
         "hbm_gbs": step_bytes / (ms * 1e-3) / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_kind": f"{peak_kind} copy bandwidth", "traffic": traffic,
@@ -883,7 +884,7 @@ def run_consensus(args):
         mk = torch.empty((st.total_segments, H, d), dtype=dt, device=dev)
         Z.zr_segment_summaries(cfg, segs, bt, lt.k_pool, lt.v_pool, mk, torch.empty_like(mk))
         mks.append(mk)
-    plan = Z.ConsensusPlan.from_structure(st, device=dev)
+    plan = Z.ConsensusPlan.from_structure(st, device=dev).set_deterministic(args.deterministic)
     q_all = torch.stack([lt.q for lt in lts])
     for l, lt in enumerate(lts):
         lt.q = q_all[l]
@@ -988,7 +989,7 @@ def run_consensus(args):
         "unit": "steps/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_mixed,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": spec.dtype,
         "data": "synthetic (seeded N(0,1) K/V, queries near one summary segment's mean key)",
-        "config": {"workload": spec.name + ("" if L == spec.layers else f"_first{L}layers"), "batch": Bn,
+        "config": {"split": "static" if args.deterministic else "dynamic", "workload": spec.name + ("" if L == spec.layers else f"_first{L}layers"), "batch": Bn,
                    "prompt": spec.prompt_len, "generated": spec.gen_len, "layers": L, "q_heads": Hq, "kv_heads": H,
                    "head_dim": d, "top_k": spec.topk, "consensus": spec.consensus, "window": spec.window,
                    "regular_len": list(spec.reg_len_range), "summary_len": list(spec.sum_len_range),
@@ -1069,7 +1070,7 @@ def run_offload(args):
         lts.append(lt)
         torch.cuda.empty_cache()
     link_gbs = measure_link_gbs(dev)
-    plan = Z.ConsensusPlan.from_structure(st, device=dev)
+    plan = Z.ConsensusPlan.from_structure(st, device=dev).set_deterministic(args.deterministic)
     q_all = torch.stack([lt.q for lt in lts])
     for l, lt in enumerate(lts):
         lt.q = q_all[l]
@@ -1196,7 +1197,7 @@ def run_offload(args):
         "n_gpus": world, "steps": steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": spec.dtype,
         "data": "synthetic (seeded N(0,1) K/V, queries near one summary segment's mean key)",
-        "config": {"workload": spec.name + "_offload" + ("" if L == spec.layers else f"_first{L}layers"),
+        "config": {"split": "static" if args.deterministic else "dynamic", "workload": spec.name + "_offload" + ("" if L == spec.layers else f"_first{L}layers"),
                    "batch": Bn, "prompt": spec.prompt_len, "generated": spec.gen_len, "layers": L, "q_heads": Hq,
                    "kv_heads": H, "head_dim": d, "top_k": spec.topk, "consensus": spec.consensus,
                    "window": spec.window, "graph": True, "staging_slots": cap, "staging_pools": 2,
@@ -1280,7 +1281,7 @@ def run_generate(args):
         mk = torch.empty((st.total_segments, H, d), dtype=dt, device=dev)
         Z.zr_segment_summaries(cfg, segs, bt, lt.k_pool, lt.v_pool, mk, torch.empty_like(mk))
         mks.append(mk)
-    plan = Z.ConsensusPlan.from_structure(st, device=dev)
+    plan = Z.ConsensusPlan.from_structure(st, device=dev).set_deterministic(args.deterministic)
     gen = torch.Generator(device=dev)
     gen.manual_seed(spec.seed + 1)
     kn = torch.randn((L, Bn, H, d), generator=gen, device=dev).to(dt)
@@ -1357,7 +1358,7 @@ def run_generate(args):
         "n_gpus": world, "steps": args.steps * T, "warmup": args.warmup * T, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": spec.dtype,
         "data": "synthetic (seeded N(0,1) K/V and new rows, queries near one summary segment's mean key)",
-        "config": {"workload": spec.name + ("" if L == spec.layers else f"_first{L}layers") + "_generate",
+        "config": {"split": "static" if args.deterministic else "dynamic", "workload": spec.name + ("" if L == spec.layers else f"_first{L}layers") + "_generate",
                    "batch": Bn, "prompt": spec.prompt_len, "generated_at_start": spec.gen_len, "layers": L,
                    "q_heads": Hq, "kv_heads": H, "head_dim": d, "top_k": spec.topk, "consensus": spec.consensus,
                    "window": spec.window, "selection_interval": T, "graph": True,
@@ -1387,6 +1388,8 @@ def main(argv=None):
     ap.add_argument("--workload", type=int, default=WORKLOAD_ID, choices=sorted(W.WORKLOADS),
                     help="seeded workload (default: the 8 x 16K, 32-layer headline step)")
     ap.add_argument("--no-graph", action="store_true", help="launch eagerly instead of replaying CUDA graphs")
+    ap.add_argument("--deterministic", action="store_true",
+                    help="the attend kernel's static split (bit-identical outputs) instead of the dynamic one")
     ap.add_argument("--max-graphs", type=int, default=64, help="distinct captured steps (each with its own events)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-oracle-accounting", action="store_true",

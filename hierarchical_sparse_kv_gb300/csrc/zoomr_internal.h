@@ -14,6 +14,10 @@ constexpr int kMaxSegments = 4096;    // n_b limit of the select kernel's shared
 constexpr int kMaxGroup = 16;         // query heads per KV head
 constexpr int kMmaMaxGroup = 8;       // the tensor-core attend kernel packs the group into 8 MMA columns
 constexpr int kChunkRows = 256;       // rows of one attend warp's row table (a range is walked in such pieces)
+constexpr int kBatchRows = 32;        // dynamic split: rows a warp claims at a time
+constexpr int kRangeCache = 95;       // dynamic split: ranges per unit a warp keeps in its row table's space
+constexpr int kCtrStride = 32;        // dynamic split: one counter per 128-byte line (claims of different units
+                                      // meet in different L2 slices)
 #ifndef ZR_ATTEND_WARPS
 #define ZR_ATTEND_WARPS 4
 #endif
@@ -55,6 +59,7 @@ struct WsLayout {
   size_t stage_marks; // int32 [num_blocks] offload map: staging slot + 1 of every physical block (0: not staged)
   size_t stage_rows;  // uint32 [num_blocks][Hkv] offload map: rows of the block that a range of the head covers
   size_t pf_list;     // int32 [U][kSelPrefetchBlocks] selected blocks before each unit's window (-1: none)
+  size_t tile_ctr;    // int32 [U][kCtrStride] dynamic split: the next 32-row batch of unit u at [u][0] (0 between launches)
   size_t votes;       // consensus only: int32 [B][n_max] vote counts, zero between selections
   size_t cruns;       // consensus only: int32 [B][n_max + 1][2] the last selection's runs before the window
   size_t cnruns;      // consensus only: int32 [B] their count
@@ -79,6 +84,7 @@ struct Plan {
   DeviceMeta meta;
   WsLayout ws;
   int merge_parts;     // merge layout: 1 lanes over partials, 0 lanes over components
+  int deterministic;   // 1: the attend kernels' static split (outputs bit-identical across calls)
   size_t select_smem;  // dynamic shared memory of the select kernel
   size_t attend_smem;  // dynamic shared memory of the attend kernel
 };
@@ -107,10 +113,12 @@ struct StepArgs {
   float2* part_ml;
   uint32_t* bigkeys;
   int32_t* pf_list;  // decode step: blocks the attend kernel prefetches after its wait
+  int32_t* tile_ctr;  // dynamic split: per-unit batch counters
   int32_t* cruns;   // consensus only
   int32_t* cnruns;  // consensus only
   int B, Hq, Hkv, G, window, num_blocks, max_blocks, k_max, n_max, attend_warps;
   int unit_cost;  // virtual rows in front of every unit in the attend kernels' even split (see kernels)
+  int dynamic;    // 1: the tensor-core attend kernel hands out each unit's rows in 32-row batches (see kernels)
   int fixed_rows;  // rows per sequence prefetched before the attend kernel's wait (0: none)
   int fixed_window;  // 1: the window rows too (the decode step, whose lengths are the plan's); 0: the prompt only
   int pf_blocks;  // decode step: blocks before each window the select kernel scans and lists for the attend

@@ -925,6 +925,30 @@ __device__ __forceinline__ void mma_issue_tile(uint32_t stage, const uint32_t* t
   }
 }
 
+// The same copies with the pool and summary bases read from the kernel parameters at every issue
+// (constant-bank operands) instead of registers: the dynamic split keeps more state live.
+template <int D>
+__device__ __forceinline__ void mma_issue_tile_p(uint32_t stage, const uint32_t* tab, int t0, int lane,
+                                                 const StepArgs& a) {
+  constexpr int RB = ring_row_bytes<D>();
+  constexpr int CPR = D / 8;
+  constexpr int RPI = 32 / CPR;
+  const int sub = lane / CPR, ch = lane % CPR;
+  const uint64_t pol = l2_evict_first_policy();
+#pragma unroll
+  for (int j = 0; j < 16 / RPI; ++j) {
+    const int row = RPI * j + sub;
+    const uint32_t id = tab[t0 + row];
+    const bool ok = id != kInvalidRow;
+    const bool is_sum = (id & kSummaryFlag) != 0;
+    const size_t off = static_cast<size_t>(ok ? (id & ~kSummaryFlag) : 0u) * (D * 2) + ch * 16;
+    const uint32_t bytes = ok ? 16u : 0u;
+    const uint32_t dst = stage + row * RB + ch * 16;
+    cp_async16_stream(dst, static_cast<const char*>(is_sum ? a.sum_k : a.k_pool) + off, bytes, pol);
+    cp_async16_stream(dst + 16 * RB, static_cast<const char*>(is_sum ? a.sum_v : a.v_pool) + off, bytes, pol);
+  }
+}
+
 template <int D>
 struct MmaState {
   uint32_t qa0[D / 16], qa2[D / 16];  // Q A-fragments (rows r < G); rows r+8 are zero
@@ -1057,6 +1081,203 @@ struct MmaWorker {
   }
 };
 
+// ------------------------------------------------------------------ attend: dynamic split
+//
+// With a fixed even split every warp streams the same number of rows, and the grid ends with its
+// slowest warp: SMs that stream more slowly, CTAs that start late behind the previous kernel and rows
+// that miss L2 all lengthen one warp's share, and the last warps finish several microseconds after
+// the median one. The dynamic split keeps which warps serve which unit (the home warps of a unit are
+// the warps whose share of the cost coordinate meets its rows, so partial slot u + p and the merge are
+// unchanged) but hands the unit's rows out in batches of 32 from a counter per unit, so all home
+// warps of a unit keep streaming until its rows run out. Warp positions along the cost coordinate are
+// taken warp-major over the grid (p = warp * ctas + cta), which spreads a unit's home warps over
+// many SMs. The attend-only calls use it: there the previous layer's merge and attend kernels still
+// hold SMs when the CTAs launch, and measured CTA entry times spread over up to 15 us. (The decode
+// step, whose CTAs are all resident while the select kernel runs, keeps the even split.)
+//
+// Batches are handed out in row order: the attend-only calls prefetch the prompt, the first rows of
+// every unit, into L2 before their wait, and the first claims find those rows there.
+//
+// Per warp the batches flow through three stages, each one batch ahead of the next: the claim of a
+// batch (an atomic add), the loads that resolve its 32 row ids (one row per lane: a block-table entry
+// or a summary index), and the cp.async copies of its tiles into the 2-stage ring. A batch has two
+// 16-row tiles (one for a unit's final batch of at most 16 rows). On the last tile of batch n the warp
+// writes batch n+1's table from the ids loaded a batch earlier and issues its first tile, then
+// resolves the claim of batch n+2 (issued a batch earlier), starts loading its ids and claims again:
+// the round trips of the claims and the id loads overlap a whole batch of copies, and the ring never
+// drains between batches.
+//
+// Every home warp claims until its first failing claim (a value >= the unit's batch count T), so a
+// unit's counter ends at T + H (H home warps); the warp whose failing claim returns T + H - 1 makes
+// the last increment of the call and stores 0, which leaves the counter ready for the next call.
+static_assert(kRangeCache == (kChunkRows - 2 * kBatchRows - 1) / 2, "two batch tables and the range cache share a row table");
+
+// One lane's part in resolving a batch: its row's kind (-1 masked, 0..15 the token's slot in its block,
+// 16 a summary row) and the value it loads (the token's block-table entry or the summary's segment).
+struct RowPrep {
+  int kind;
+  int val;
+};
+
+struct UnitView {
+  const int32_t* cache;  // shared memory: the range prefix sums [nr + 1], then the range starts [nr]
+  int u, b, g, nr, n_tok, R, seg0;
+};
+
+__device__ __forceinline__ RowPrep prep_row(const StepArgs& a, const UnitView& v, int r) {
+  RowPrep o{-1, 0};
+  if (r >= v.R) return o;
+  if (r >= v.n_tok) {
+    o.kind = 16;
+    o.val = a.sumlist[static_cast<size_t>(v.u) * a.n_max + (r - v.n_tok)];
+    return o;
+  }
+  const int32_t* cum = v.cache;
+  int lo = 0, hi = v.nr - 1;  // the last range whose first row is <= r
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (cum[mid] <= r) lo = mid; else hi = mid - 1;
+  }
+  const int t = cum[v.nr + 1 + lo] + (r - cum[lo]);
+  o.kind = t & 15;
+  o.val = a.block_tables[static_cast<size_t>(v.b) * a.max_blocks + (t >> 4)];
+  return o;
+}
+
+__device__ __forceinline__ uint32_t finish_row(const StepArgs& a, const UnitView& v, RowPrep rp) {
+  if (rp.kind < 0) return kInvalidRow;
+  if (rp.kind == 16) return (static_cast<uint32_t>(v.seg0 + rp.val) * a.Hkv + v.g) | kSummaryFlag;
+  if (static_cast<unsigned>(rp.val) < static_cast<unsigned>(a.num_blocks))
+    return ((static_cast<uint32_t>(rp.val) * a.Hkv + v.g) << 4) | static_cast<uint32_t>(rp.kind);
+  atomicOr(a.err, kErrBadBlock);
+  return kInvalidRow;
+}
+
+// All rows of unit u that this warp claims, then its partial into `slot`. H: the unit's home warps.
+template <int D>
+__device__ void visit_unit_dynamic(const StepArgs& a, MmaWorker<D>& wk, uint32_t* tab, int u, int p, int H,
+                                   int lane) {
+  constexpr uint32_t SB = MmaWorker<D>::kStageBytes;
+  const int b = u / a.Hkv, g = u - b * a.Hkv;
+  const int32_t* rg = a.ranges + static_cast<size_t>(u) * (a.k_max + 1) * 2;
+  const int32_t* cum = a.cum + static_cast<size_t>(u) * (a.k_max + 2);
+  // One round trip: the first claim, the unit's sizes, the first 32 range bounds and the queries.
+  int claim = 0;
+  if (lane == 0) claim = atomicAdd(a.tile_ctr + static_cast<size_t>(u) * kCtrStride, 1);
+  const int c_l = lane <= a.k_max + 1 ? cum[lane] : 0;
+  const int s_l = lane <= a.k_max ? rg[2 * lane] : 0;
+  const int4 info = a.unit_info[u];
+  UnitView v;
+  v.seg0 = a.meta.seg_ptr[b];
+  wk.begin_unit(a, b, g, lane);
+  v.u = u;
+  v.b = b;
+  v.g = g;
+  v.nr = info.x;
+  v.n_tok = info.y;
+  v.R = info.y + info.z;
+  const int T = (v.R + kBatchRows - 1) / kBatchRows;
+  int32_t* cache = reinterpret_cast<int32_t*>(tab) + 2 * kBatchRows;
+  __syncwarp();  // the previous unit's readers of the table and the cache are done
+  // The plan enables the dynamic split only when k_max + 1 <= kRangeCache, so every unit's ranges fit.
+  if (lane <= v.nr) cache[lane] = c_l;
+  if (lane < v.nr) cache[v.nr + 1 + lane] = s_l;
+  for (int i = 32 + lane; i <= v.nr; i += 32) cache[i] = cum[i];
+  for (int i = 32 + lane; i < v.nr; i += 32) cache[v.nr + 1 + i] = rg[2 * i];
+  v.cache = cache;
+  __syncwarp();
+  auto failed = [&](int c) {  // c: this warp's failing claim (>= T), the same in every lane
+    if (lane == 0 && c + 1 == T + H) a.tile_ctr[static_cast<size_t>(u) * kCtrStride] = 0;
+  };
+  claim = __shfl_sync(kFull, claim, 0);
+  if (claim >= T) {
+    failed(claim);
+    wk.end_unit(a, u + p, lane);
+    return;
+  }
+  uint32_t* tb = tab;  // two 32-entry tables: batch parity s in tb + 32 s
+  const size_t ci = static_cast<size_t>(u) * kCtrStride;
+  int cur = claim, s = 0, stage = 0;
+  RowPrep rp = prep_row(a, v, kBatchRows * cur + lane);
+  int pend = 0;
+  if (lane == 0) pend = atomicAdd(a.tile_ctr + ci, 1);
+  tb[lane] = finish_row(a, v, rp);
+  __syncwarp();
+  mma_issue_tile_p<D>(wk.ring, tb, 0, lane, a);
+  cp_async_commit();
+  // The batch after cur: its row ids are loaded into rp a whole batch before its first tile is issued.
+  int nxt = -1;
+  // The outstanding claim: load its row ids and claim the batch after it. A claim is outstanding
+  // exactly while the last one resolved succeeded, i.e. while nxt >= 0.
+  auto resolve = [&]() {
+    const int c = __shfl_sync(kFull, pend, 0);
+    if (c < T) {
+      rp = prep_row(a, v, kBatchRows * c + lane);
+      if (lane == 0) pend = atomicAdd(a.tile_ctr + ci, 1);
+      return c;
+    }
+    failed(c);
+    return -1;
+  };
+  nxt = resolve();
+  while (true) {
+    const int nt = min(2, (v.R - kBatchRows * cur + 15) >> 4);  // tiles of batch cur (1: a final batch of <= 16 rows)
+    int after = -1;
+    for (int h = 0; h < nt; ++h) {
+      __syncwarp();  // every lane is done reading the stage (and the table) that is refilled next
+      if (h + 1 < nt) {
+        mma_issue_tile_p<D>(wk.ring + (stage ^ 1) * SB, tb + kBatchRows * s, 16, lane, a);
+      } else if (nxt >= 0) {  // cur's last tile: start the next batch, then prepare the one after it
+        tb[kBatchRows * (s ^ 1) + lane] = finish_row(a, v, rp);
+        __syncwarp();
+        mma_issue_tile_p<D>(wk.ring + (stage ^ 1) * SB, tb + kBatchRows * (s ^ 1), 0, lane, a);
+        after = resolve();
+      }
+      cp_async_commit();
+      cp_async_wait<1>();
+      __syncwarp();  // the tile's rows, staged by all lanes, are visible to every lane
+      const uint32_t vmask16 =
+          __ballot_sync(kFull, lane < 16 && tb[kBatchRows * s + 16 * h + lane] != kInvalidRow) & 0xFFFFu;
+      mma_compute_tile<D>(wk.st, wk.ring + stage * SB, vmask16, a.scale_log2, lane);
+      stage ^= 1;
+    }
+    if (nxt < 0) break;
+    cur = nxt;
+    nxt = after;
+    s ^= 1;
+  }
+  wk.end_unit(a, u + p, lane);
+}
+
+// Home warps of the unit whose rows occupy [c0, c0 + Ru) of a cost coordinate of length C split
+// evenly among N warps (the warp whose share holds position c is ceil((c + 1) N / C) - 1).
+__device__ __forceinline__ int home_warps(long long c0, int Ru, long long C, long long N) {
+  const long long wf = ((c0 + 1) * N + C - 1) / C - 1;
+  const long long wl = ((c0 + Ru) * N + C - 1) / C - 1;
+  return static_cast<int>(wl - wf + 1);
+}
+
+// One warp at position p: every unit whose rows its share meets, each visited until the unit's rows
+// run out.
+template <int D>
+__device__ void attend_dynamic(const StepArgs& a, const UnitRows& rows, MmaWorker<D>& wk, uint32_t* tab, int p,
+                               int lane) {
+  WarpRange wr;
+  if (!locate_range(a, rows, p, a.attend_warps, lane, wr)) return;
+  int u = wr.u;
+  long long P = wr.P;
+  int Ru = wr.Ru;
+  while (true) {
+    const long long first = P + a.unit_cost;
+    if (Ru > 0 && wr.s < first + Ru && wr.e > first)
+      visit_unit_dynamic<D>(a, wk, tab, u, p, home_warps(first, Ru, wr.R, wr.N), lane);
+    if (first + Ru >= wr.e) break;
+    P = first + Ru;
+    ++u;
+    Ru = rows(u);
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kAttendWarps * 32, 3) zr_attend_mma_kernel(StepArgs a) {
   extern __shared__ __align__(16) unsigned char attend_smem[];
@@ -1074,7 +1295,11 @@ __global__ void __launch_bounds__(kAttendWarps * 32, 3) zr_attend_mma_kernel(Ste
   wk.lb = LoadBases{static_cast<const char*>(a.k_pool) + chunk_off, static_cast<const char*>(a.v_pool) + chunk_off,
                     static_cast<const char*>(a.sum_k) + chunk_off, static_cast<const char*>(a.sum_v) + chunk_off,
                     l2_evict_first_policy()};
-  attend_balanced(a, stage_unit_rows(a, s_rows), wk, rowtab[warp], warp, lane);
+  const UnitRows rows = stage_unit_rows(a, s_rows);
+  if (a.dynamic)
+    attend_dynamic<D>(a, rows, wk, rowtab[warp], warp * static_cast<int>(gridDim.x) + blockIdx.x, lane);
+  else
+    attend_balanced(a, rows, wk, rowtab[warp], warp, lane);
 }
 
 // ------------------------------------------------------------------ attend: CUDA cores (f32, or any G)

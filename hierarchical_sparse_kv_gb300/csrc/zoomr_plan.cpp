@@ -125,6 +125,7 @@ void layout_workspace(zr::Plan& p) {
   p.ws.stage_marks = take(static_cast<size_t>(p.num_blocks) * sizeof(int32_t));
   p.ws.stage_rows = take(static_cast<size_t>(p.num_blocks) * p.Hkv * sizeof(uint32_t));
   p.ws.pf_list = take(U * zr::kSelPrefetchBlocks * sizeof(int32_t));
+  p.ws.tile_ctr = take(U * zr::kCtrStride * sizeof(int32_t));
   const bool cons = p.mode == zr::kConsensusPlan;
   p.ws.votes = cons ? take(static_cast<size_t>(p.B) * p.n_max * sizeof(int32_t)) : 0;
   p.ws.cruns = cons ? take(static_cast<size_t>(p.B) * (p.n_max + 1) * 2 * sizeof(int32_t)) : 0;
@@ -318,6 +319,10 @@ zr_status decode_into(zr_plan_t plan, void* workspace, const void* q, const void
   a.fixed_rows = plan->p.fixed_rows;
   a.fixed_window = 1;
   a.pf_blocks = plan->p.pf_blocks;
+  // The decode step keeps the even split: its attend CTAs are resident and waiting while the select kernel
+  // runs, and measured on the 8 x 16K-token workload the dynamic split's batch claims cost more there
+  // (878 against 887 steps/s) than they save at the tail.
+  a.dynamic = 0;
   return zr::launch_step(plan->p, a, stream, ev_start, ev_stop);
 }
 
@@ -336,6 +341,7 @@ StepArgs step_args(const Plan& p, void* workspace) {
   a.part_ml = reinterpret_cast<float2*>(ws + p.ws.part_ml);
   a.bigkeys = reinterpret_cast<uint32_t*>(ws + p.ws.bigkeys);
   a.pf_list = reinterpret_cast<int32_t*>(ws + p.ws.pf_list);
+  a.tile_ctr = reinterpret_cast<int32_t*>(ws + p.ws.tile_ctr);
   a.cruns = p.mode == kConsensusPlan ? reinterpret_cast<int32_t*>(ws + p.ws.cruns) : nullptr;
   a.cnruns = p.mode == kConsensusPlan ? reinterpret_cast<int32_t*>(ws + p.ws.cnruns) : nullptr;
   a.B = p.B;
@@ -352,6 +358,10 @@ StepArgs step_args(const Plan& p, void* workspace) {
   // different tokens (each KV head selects its own segments); consensus units share one token set,
   // whose block-table entries the next unit finds cached, and a start there costs little.
   a.unit_cost = p.mode == kConsensusPlan ? 0 : kUnitStartRows;
+  // Attend-only calls (consensus attention, steps between selections, the offloaded cache) take the dynamic
+  // split unless the plan is deterministic. It keeps a unit's ranges in shared memory, so plans with more
+  // range slots take the even split.
+  a.dynamic = !p.deterministic && p.k_max + 1 <= kRangeCache ? 1 : 0;
   a.fixed_rows = 0;  // set by the decode step and the attend-only calls (see decode_into)
   a.fixed_window = 0;
   a.pf_blocks = 0;
@@ -402,6 +412,12 @@ void zr_free(zr_plan_t plan) {
   if (!plan) return;
   if (plan->p.d_meta_base) cudaFree(plan->p.d_meta_base);
   delete plan;
+}
+
+zr_status zr_plan_set_deterministic(zr_plan_t plan, int32_t deterministic) {
+  if (!plan || (deterministic != 0 && deterministic != 1)) return ZR_EINVAL;
+  plan->p.deterministic = deterministic;
+  return ZR_OK;
 }
 
 const char* zr_status_string(zr_status s) {

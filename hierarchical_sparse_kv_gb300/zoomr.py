@@ -99,6 +99,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.zr_offload_map.restype = ctypes.c_int
     lib.zr_offload_stage.argtypes = [_P] * 6 + [ctypes.c_int32, _P, _P, _P]
     lib.zr_offload_stage.restype = ctypes.c_int
+    lib.zr_plan_set_deterministic.argtypes = [_P, ctypes.c_int32]
+    lib.zr_plan_set_deterministic.restype = ctypes.c_int
     lib.zr_free.argtypes = [_P]
     lib.zr_free.restype = None
     lib.zr_status_string.argtypes = [ctypes.c_int]
@@ -236,6 +238,13 @@ def zr_get_device_error(plan: int, workspace: torch.Tensor, stream=None) -> int:
     if st not in (ZR_OK, ZR_EDEVICE):
         raise ZoomrError(st, "zr_get_device_error")
     return code.value
+
+
+def zr_plan_set_deterministic(plan: int, deterministic: bool) -> None:
+    """Static split (outputs bit-identical across calls) or the default dynamic split of the rows."""
+    st = load().zr_plan_set_deterministic(plan, 1 if deterministic else 0)
+    if st != ZR_OK:
+        raise ZoomrError(st, "zr_plan_set_deterministic")
 
 
 def zr_free(plan: Optional[int]) -> None:
@@ -406,6 +415,11 @@ class DecodePlan:
     def device_error(self, stream=None) -> int:
         return zr_get_device_error(self.handle, self.ws, stream)
 
+    def set_deterministic(self, deterministic: bool = True):
+        """Bit-identical outputs across calls (static split) or the default dynamic split; returns self."""
+        zr_plan_set_deterministic(self.handle, deterministic)
+        return self
+
     def close(self):
         if getattr(self, "handle", None):
             zr_free(self.handle)
@@ -515,6 +529,11 @@ class ConsensusPlan:
 
     def device_error(self, stream=None) -> int:
         return zr_get_device_error(self.handle, self.ws, stream)
+
+    def set_deterministic(self, deterministic: bool = True):
+        """Bit-identical outputs across calls (static split) or the default dynamic split; returns self."""
+        zr_plan_set_deterministic(self.handle, deterministic)
+        return self
 
     def close(self):
         if getattr(self, "handle", None):

@@ -449,6 +449,29 @@ ZR_API zr_status zr_offload_stage(zr_plan_t plan, const void* workspace, const v
                                   const void* host_v_pool, const int32_t* stage_ids, const int32_t* n_staged,
                                   int32_t capacity, void* stage_k, void* stage_v, void* stream);
 
+/*
+ * zr_plan_set_deterministic -- choose how the gather-attention kernel of the
+ * attend-only calls (zr_consensus_attend, zr_decode_attend_reuse and their timed
+ * forms) splits a call's rows among its warps. The pages leave the schedule open;
+ * this is a deployment choice, not part of the method.
+ *   deterministic = 0 (the default of every plan): each unit's rows are handed out
+ *     in 32-row batches from a per-unit counter in the workspace, so the warps of
+ *     a unit keep streaming until its rows run out however fast their SMs run or
+ *     however late their CTAs start. Which warp takes which batch changes from
+ *     call to call, and with it the rounding of the output (within the documented
+ *     tolerance of the exact result; selections, ranges and every integer output
+ *     are unaffected). Plans whose units hold more than 94 ranges (k_max + 1 > 95)
+ *     always take the even split.
+ *   deterministic = 1: a fixed even split of the rows; the output bits of a plan
+ *     are identical across calls, streams and the entry points that share a kernel.
+ * zr_decode_attend (the decode step, select and attend) always takes the even
+ * split: its attend CTAs are resident while the select kernel runs.
+ * The counters return to zero by the end of every call, so a workspace zeroed once
+ * before its first use stays valid in both modes. Takes effect at the next call.
+ * Errors: ZR_EINVAL (null plan, or a value other than 0 or 1).
+ */
+ZR_API zr_status zr_plan_set_deterministic(zr_plan_t plan, int32_t deterministic);
+
 /* zr_free -- release the plan and its small device metadata (NULL is a no-op). */
 ZR_API void zr_free(zr_plan_t plan);
 

@@ -83,6 +83,11 @@ def test_plan_rejects_null_arguments(lib):
     lib.zr_free(None)  # no-op
 
 
+def test_deterministic_setter_checks_its_arguments(lib):
+    assert lib.zr_plan_set_deterministic(None, 1) == Z.ZR_EINVAL
+    assert lib.zr_plan_set_deterministic(None, 0) == Z.ZR_EINVAL
+
+
 def test_too_many_segments_is_unsupported(lib):
     n = 4097
     cfg = Z.zr_config(1, 4, 1, 64, 16, 300, 300, 0, Z.ZR_BF16)

@@ -100,7 +100,7 @@ def test_advance_rejects_shrinking_or_oversized_lengths():
                         seq_len_range=(100, 200), seg_len_range=(5, 40), topk=2, window=16, seed=42)
     st = W.make_structure(spec)
     lt = W.make_layer(st, 0, "cuda")
-    plan = Z.DecodePlan.from_structure(st)
+    plan = Z.DecodePlan.from_structure(st).set_deterministic()  # bit-equal outputs across calls
     bt = torch.from_numpy(st.block_tables.astype(np.int32)).cuda()
     out0 = torch.empty((2, 8, 128), device="cuda")
     out1 = torch.empty_like(out0)

@@ -8,6 +8,8 @@ set and the final token ranges must match bit for bit, and every layer's outputs
 
 from __future__ import annotations
 
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -201,7 +203,7 @@ def test_timed_attend_matches_and_times_the_kernel():
     """zr_consensus_attend_timed: the same outputs as zr_consensus_attend, with events around the
     gather-attention kernel (either one alone works too)."""
     st, lts = _setup(dtype="bf16", head_dim=128, num_q_heads=8, num_kv_heads=2, layers=1)
-    plan = Z.ConsensusPlan.from_structure(st)
+    plan = Z.ConsensusPlan.from_structure(st).set_deterministic()  # bit-equal outputs across calls
     bt = torch.from_numpy(st.block_tables.astype(np.int32)).cuda()
     sp = st.spec
     mk = _device_mean_keys(st, lts[0], bt)
@@ -220,3 +222,34 @@ def test_timed_attend_matches_and_times_the_kernel():
     assert e0.elapsed_time(e1) > 0
     assert plan.device_error() == 0
     plan.close()
+
+
+def test_dynamic_split_within_rounding_of_the_even_split():
+    """Consensus attention takes the dynamic split by default: ten calls on one workspace (the per-unit batch
+    counters return to zero after each) all equal the deterministic plan's output up to the order of the
+    sums, at the full 8B shape with 16K generated tokens (two layers)."""
+    st = W.make_consensus_structure(dataclasses.replace(W.CONSENSUS_WORKLOADS[1], layers=2))
+    lts = [W.make_consensus_layer(st, l, "cuda") for l in range(2)]
+    bt = torch.from_numpy(st.block_tables.astype(np.int32)).cuda()
+    sp = st.spec
+    outs = {}
+    for det in (True, False):
+        plan = Z.ConsensusPlan.from_structure(st).set_deterministic(det)
+        mks = [_device_mean_keys(st, lt, bt) for lt in lts]
+        for l, lt in enumerate(lts):
+            plan.vote(lt.q, mks[l])
+        plan.select()
+        got = []
+        for _ in range(1 if det else 5):
+            for lt in lts:
+                out = torch.full((st.batch, sp.num_q_heads, sp.head_dim), float("nan"), device="cuda")
+                plan.attend(lt.q, lt.k_pool, lt.v_pool, bt, out)
+                got.append(out)
+        torch.cuda.synchronize()
+        assert plan.device_error() == 0
+        outs[det] = got
+        plan.close()
+    ref = outs[True]
+    for i, out in enumerate(outs[False]):
+        assert torch.isfinite(out).all()
+        torch.testing.assert_close(out, ref[i % len(lts)], rtol=1e-5, atol=1e-5)

@@ -33,7 +33,7 @@ def test_decode_with_host_resident_pools(dtype, d):
     st = W.make_structure(spec)
     lt = W.make_layer(st, 0, "cuda")
     lt_host = dataclasses.replace(lt, k_pool=_pinned(lt.k_pool), v_pool=_pinned(lt.v_pool))
-    plan = Z.DecodePlan.from_structure(st)
+    plan = Z.DecodePlan.from_structure(st).set_deterministic()  # bit-equal outputs across calls
     bt = C.device_tables(st)
     out_dev, dbg_dev = C.run_gpu(plan, lt, bt)
     out_host, dbg_host = C.run_gpu(plan, lt_host, bt)
@@ -58,7 +58,7 @@ def test_consensus_with_host_resident_pools():
     outs = []
     for host in (False, True):
         pools = [(_pinned(lt.k_pool), _pinned(lt.v_pool)) if host else (lt.k_pool, lt.v_pool) for lt in lts]
-        plan = Z.ConsensusPlan.from_structure(st)
+        plan = Z.ConsensusPlan.from_structure(st).set_deterministic()  # bit-equal outputs across calls
         mks = []
         for (kp, vp) in pools:
             mk = torch.empty((st.total_segments, sp.num_kv_heads, sp.head_dim), dtype=torch.bfloat16, device="cuda")
@@ -209,7 +209,7 @@ def test_staged_decode_equals_the_hbm_step_and_overflow_is_reported():
                         seq_len_range=(300, 900), seg_len_range=(10, 60), topk=3, window=40, seed=62)
     st = W.make_structure(spec)
     lt = W.make_layer(st, 0, "cuda")
-    plan = Z.DecodePlan.from_structure(st)
+    plan = Z.DecodePlan.from_structure(st).set_deterministic()  # bit-equal outputs across calls
     bt = C.device_tables(st)
     ref = torch.empty(lt.q.shape, dtype=torch.float32, device="cuda")
     plan.run(lt.q, lt.k_pool, lt.v_pool, bt, lt.sum_k, lt.sum_v, ref)
