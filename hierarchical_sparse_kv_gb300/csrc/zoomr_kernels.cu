@@ -1473,11 +1473,19 @@ __global__ void __launch_bounds__(kAttendWarps * 32) zr_merge_comp_kernel(StepAr
 // 32 contiguous bytes, a whole sector. The CTA's first warp finds which attend warps hold the unit.
 constexpr int kMergeComp = 8;
 constexpr int kMergeBatch = 4;
-constexpr int kMergeWarps = 4;
+#ifndef ZR_MERGE_WARPS
+#define ZR_MERGE_WARPS 4
+#endif
+// Warps per merge CTA: the slices of one query head, at most ZR_MERGE_WARPS of them.
+template <int D>
+__host__ __device__ constexpr int merge_warps() {
+  return ZR_MERGE_WARPS < D / kMergeComp ? ZR_MERGE_WARPS : D / kMergeComp;
+}
 
 template <int D>
-__global__ void __launch_bounds__(kMergeWarps * 32, 8) zr_merge_part_kernel(StepArgs a) {
+__global__ void __launch_bounds__(merge_warps<D>() * 32, 32 / merge_warps<D>()) zr_merge_part_kernel(StepArgs a) {
   constexpr int NC = D / kMergeComp;
+  constexpr int kMergeWarps = merge_warps<D>();
   static_assert(NC % kMergeWarps == 0, "a CTA's slices belong to one query head");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int w = blockIdx.x * kMergeWarps + warp;
@@ -1691,8 +1699,8 @@ cudaError_t launch_for(const Plan& p, const StepArgs& a, cudaStream_t s, cudaEve
   if (e != cudaSuccess) return report("attend launch", e), e;
   if (ev1 && (e = record_event(ev1, s)) != cudaSuccess) return report("stop event record", e), e;
   if (p.merge_parts) {
-    e = launch_pdl(zr_merge_part_kernel<D>, dim3(p.B * p.Hq * (D / kMergeComp) / kMergeWarps),
-                   dim3(kMergeWarps * 32), 0, s, a);
+    e = launch_pdl(zr_merge_part_kernel<D>, dim3(p.B * p.Hq * (D / kMergeComp) / merge_warps<D>()),
+                   dim3(merge_warps<D>() * 32), 0, s, a);
   } else {
     const dim3 grid_merge((p.B * p.Hq * (D / 32) + kAttendWarps - 1) / kAttendWarps);
     e = launch_pdl(zr_merge_comp_kernel<D>, grid_merge, block, 0, s, a);
@@ -1714,8 +1722,8 @@ cudaError_t launch_attend_for(const Plan& p, const StepArgs& a, cudaStream_t s, 
   if (e != cudaSuccess) return report("attend launch", e), e;
   if (ev1 && (e = record_event(ev1, s)) != cudaSuccess) return report("stop event record", e), e;
   if (p.merge_parts) {
-    e = launch_pdl(zr_merge_part_kernel<D>, dim3(p.B * p.Hq * (D / kMergeComp) / kMergeWarps),
-                   dim3(kMergeWarps * 32), 0, s, a);
+    e = launch_pdl(zr_merge_part_kernel<D>, dim3(p.B * p.Hq * (D / kMergeComp) / merge_warps<D>()),
+                   dim3(merge_warps<D>() * 32), 0, s, a);
   } else {
     const dim3 grid_merge((p.B * p.Hq * (D / 32) + kAttendWarps - 1) / kAttendWarps);
     e = launch_pdl(zr_merge_comp_kernel<D>, grid_merge, block, 0, s, a);

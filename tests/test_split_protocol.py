@@ -1,0 +1,61 @@
+"""The dynamic split's claim protocol, modelled on the host (the gather-attention kernel's per-unit batch
+counter; no GPU).
+
+Each of a unit's H home warps claims 32-row batches with an atomic add on one counter: a first claim, then one
+claim at a time, each issued only after the previous one succeeded, until its first failing claim (a value >= T,
+the unit's batch count). The model runs the warps under random interleavings and checks what the kernel relies
+on: every batch is handed out exactly once, every warp fails exactly once, the counter ends at T + H, and exactly
+one claim (the last increment of the call) sees T + H - 1 and stores 0, leaving the counter ready for the next
+call. A planted mistake (a warp that stops after a success) must break it.
+"""
+
+from __future__ import annotations
+
+import random
+
+import pytest
+
+
+def _run(T: int, H: int, rng: random.Random, stop_early: int = -1):
+    """Interleave H warps' claims; returns (batches handed out, failures per warp, final counter, resets,
+    whether the planted mistake happened)."""
+    counter = 0
+    handed, failures, resets, planted = [], [0] * H, 0, False
+    live = list(range(H))
+    while live:
+        w = rng.choice(live)
+        c = counter
+        counter += 1  # the atomic add
+        if c < T:
+            handed.append(c)
+            if w == stop_early:  # planted mistake: this warp stops after a success, without its failing claim
+                planted = True
+                live.remove(w)
+        else:
+            failures[w] += 1
+            if c + 1 == T + H:
+                resets += 1
+                counter = 0  # the store of the warp whose failing claim is the call's last increment
+            live.remove(w)
+    return handed, failures, counter, resets, planted
+
+
+@pytest.mark.parametrize("T,H", [(1, 1), (5, 28), (138, 28), (40, 1), (3, 60), (0, 4)])
+def test_every_batch_once_and_the_counter_returns_to_zero(T, H):
+    rng = random.Random(T * 1000 + H)
+    for _ in range(200):
+        handed, failures, counter, resets, _ = _run(T, H, rng)
+        assert sorted(handed) == list(range(T))
+        assert failures == [1] * H
+        assert resets == 1 and counter == 0
+
+
+def test_a_warp_that_skips_its_failing_claim_leaves_the_counter_dirty():
+    rng = random.Random(7)
+    runs = 0
+    for _ in range(200):
+        _, _, counter, resets, planted = _run(10, 6, rng, stop_early=2)
+        if planted:
+            runs += 1
+            assert counter != 0 and resets == 0
+    assert runs > 100
