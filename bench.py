@@ -535,7 +535,7 @@ def run_zoomr(args):
         "scaling": "weak", "vs_baseline": None, "dtype": spec.dtype,
         "data": "synthetic (seeded N(0,1) K/V, segment-mean summaries + N(0,0.1), queries near segment means)",
         "config": config_dict(spec, {"graph": not args.no_graph, "replicas_per_gpu": 1, "l2": l2,
-                                     "split": "static" if args.deterministic else "dynamic"}),
+                                     "split": "even (the decode step always takes the even split of the rows)"}),
         "hbm_gbs": step_bytes / (ms * 1e-3) / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_kind": f"{peak_kind} copy bandwidth", "traffic": traffic,
@@ -989,7 +989,7 @@ def run_consensus(args):
         "unit": "steps/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_mixed,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": spec.dtype,
         "data": "synthetic (seeded N(0,1) K/V, queries near one summary segment's mean key)",
-        "config": {"split": "static" if args.deterministic else "dynamic", "workload": spec.name + ("" if L == spec.layers else f"_first{L}layers"), "batch": Bn,
+        "config": {"split": "even (deterministic plan)" if args.deterministic else "dynamic (attend-only calls)", "workload": spec.name + ("" if L == spec.layers else f"_first{L}layers"), "batch": Bn,
                    "prompt": spec.prompt_len, "generated": spec.gen_len, "layers": L, "q_heads": Hq, "kv_heads": H,
                    "head_dim": d, "top_k": spec.topk, "consensus": spec.consensus, "window": spec.window,
                    "regular_len": list(spec.reg_len_range), "summary_len": list(spec.sum_len_range),
@@ -1197,7 +1197,7 @@ def run_offload(args):
         "n_gpus": world, "steps": steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": spec.dtype,
         "data": "synthetic (seeded N(0,1) K/V, queries near one summary segment's mean key)",
-        "config": {"split": "static" if args.deterministic else "dynamic", "workload": spec.name + "_offload" + ("" if L == spec.layers else f"_first{L}layers"),
+        "config": {"split": "even (deterministic plan)" if args.deterministic else "dynamic (attend-only calls)", "workload": spec.name + "_offload" + ("" if L == spec.layers else f"_first{L}layers"),
                    "batch": Bn, "prompt": spec.prompt_len, "generated": spec.gen_len, "layers": L, "q_heads": Hq,
                    "kv_heads": H, "head_dim": d, "top_k": spec.topk, "consensus": spec.consensus,
                    "window": spec.window, "graph": True, "staging_slots": cap, "staging_pools": 2,
@@ -1358,7 +1358,7 @@ def run_generate(args):
         "n_gpus": world, "steps": args.steps * T, "warmup": args.warmup * T, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": spec.dtype,
         "data": "synthetic (seeded N(0,1) K/V and new rows, queries near one summary segment's mean key)",
-        "config": {"split": "static" if args.deterministic else "dynamic", "workload": spec.name + ("" if L == spec.layers else f"_first{L}layers") + "_generate",
+        "config": {"split": "even (deterministic plan)" if args.deterministic else "dynamic (attend-only calls)", "workload": spec.name + ("" if L == spec.layers else f"_first{L}layers") + "_generate",
                    "batch": Bn, "prompt": spec.prompt_len, "generated_at_start": spec.gen_len, "layers": L,
                    "q_heads": Hq, "kv_heads": H, "head_dim": d, "top_k": spec.topk, "consensus": spec.consensus,
                    "window": spec.window, "selection_interval": T, "graph": True,
@@ -1389,7 +1389,8 @@ def main(argv=None):
                     help="seeded workload (default: the 8 x 16K, 32-layer headline step)")
     ap.add_argument("--no-graph", action="store_true", help="launch eagerly instead of replaying CUDA graphs")
     ap.add_argument("--deterministic", action="store_true",
-                    help="the attend kernel's static split (bit-identical outputs) instead of the dynamic one")
+                    help="deterministic plans: the attend-only calls (consensus, generate, offload paths) take the even "
+                         "split of the rows instead of the dynamic one; the decode step always takes the even split")
     ap.add_argument("--max-graphs", type=int, default=64, help="distinct captured steps (each with its own events)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-oracle-accounting", action="store_true",
