@@ -1,5 +1,6 @@
-"""The dynamic split's claim protocol, modelled on the host (the gather-attention kernel's per-unit batch
-counter; no GPU).
+"""How the gather-attention kernels share a call's rows among their warps, modelled on the host (no GPU): the
+even split's shares, partial slots and the merge's warp ranges, and the dynamic split's claim protocol on its
+per-unit batch counter.
 
 Each of a unit's H home warps claims 32-row batches with an atomic add on one counter: a first claim, then one
 claim at a time, each issued only after the previous one succeeded, until its first failing claim (a value >= T,
@@ -59,3 +60,42 @@ def test_a_warp_that_skips_its_failing_claim_leaves_the_counter_dirty():
             runs += 1
             assert counter != 0 and resets == 0
     assert runs > 100
+
+
+# ---------------------------------------------------------------- the even split's bookkeeping
+# The attend kernels split the cost coordinate (every unit's rows, each unit preceded by X virtual rows) evenly over
+# N warps: warp w takes [floor(w C / N), floor((w + 1) C / N)). A warp writes one partial per unit whose rows its share
+# meets, into slot u + w; the merge (and the dynamic split, for its home-warp count H) finds a unit's first and last
+# warp from the unit's first row c0 and last row c1 alone: the warp holding position c is ceil((c + 1) N / C) - 1.
+
+def _shares(C: int, N: int):
+    return [(w * C // N, (w + 1) * C // N) for w in range(N)]
+
+
+def _merge_range(c0: int, c1: int, C: int, N: int):
+    wf = ((c0 + 1) * N + C - 1) // C - 1
+    wl = ((c1 + 1) * N + C - 1) // C - 1
+    return wf, wl
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_merge_range_and_slots_match_brute_force(seed):
+    rng = random.Random(seed)
+    U = rng.choice([1, 2, 7, 64, 300])
+    X = rng.choice([0, 48])
+    rows = [rng.randint(1, rng.choice([20, 600, 5000])) for _ in range(U)]
+    C = sum(rows) + U * X
+    N = min(rng.choice([1, 5, 456, 1824, 4096]), C)
+    shares = _shares(C, N)
+    assert shares[0][0] == 0 and shares[-1][1] == C and all(s < e for s, e in shares)
+    slots = set()
+    P = 0
+    for u, R in enumerate(rows):
+        c0 = P + X  # the unit's first row in the cost coordinate
+        brute = [w for w, (s, e) in enumerate(shares) if s < c0 + R and e > c0]
+        wf, wl = _merge_range(c0, c0 + R - 1, C, N)
+        assert brute == list(range(wf, wl + 1))
+        for w in brute:
+            assert u + w not in slots and u + w < U + N
+            slots.add(u + w)
+        P = c0 + R
