@@ -241,7 +241,8 @@ def zr_get_device_error(plan: int, workspace: torch.Tensor, stream=None) -> int:
 
 
 def zr_plan_set_deterministic(plan: int, deterministic: bool) -> None:
-    """Static split (outputs bit-identical across calls) or the default dynamic split of the rows."""
+    """The attend-only calls' even split of the rows (outputs bit-identical across calls) or their default dynamic
+    split; the decode step always takes the even split."""
     st = load().zr_plan_set_deterministic(plan, 1 if deterministic else 0)
     if st != ZR_OK:
         raise ZoomrError(st, "zr_plan_set_deterministic")
@@ -416,7 +417,8 @@ class DecodePlan:
         return zr_get_device_error(self.handle, self.ws, stream)
 
     def set_deterministic(self, deterministic: bool = True):
-        """Bit-identical outputs across calls (static split) or the default dynamic split; returns self."""
+        """Bit-identical outputs across calls (the even split of the rows in the attend-only calls too) or their
+        default dynamic split; returns self."""
         zr_plan_set_deterministic(self.handle, deterministic)
         return self
 
@@ -531,7 +533,8 @@ class ConsensusPlan:
         return zr_get_device_error(self.handle, self.ws, stream)
 
     def set_deterministic(self, deterministic: bool = True):
-        """Bit-identical outputs across calls (static split) or the default dynamic split; returns self."""
+        """Bit-identical outputs across calls (the even split of the rows in the attend-only calls too) or their
+        default dynamic split; returns self."""
         zr_plan_set_deterministic(self.handle, deterministic)
         return self
 
